@@ -1,0 +1,257 @@
+"""CPU oracle for the sparsely-gated MoE SwiGLU FFN forward -- TEST INFRASTRUCTURE.
+
+A thin ctypes binding over ``moe_oracle.c`` (plain C, fp64, one token at a time).
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package.  The product library never loads it.
+
+Every function takes numpy arrays holding the exact run-dtype values (fp32 arrays;
+bf16 values are exact in fp32) and returns float64 results.  ``forward`` chains the
+stages the way the layer does: route -> capacity-limited dispatch -> experts ->
+gate-weighted combine (plus unweighted shared experts).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_moe.so")
+_lock = threading.Lock()
+_lib = None
+
+GATE_SOFTMAX = 0
+GATE_SIGMOID = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2, no fast-math: IEEE double throughout)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+                               "-fno-fast-math", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            f32p = ctypes.POINTER(ctypes.c_float)
+            f64p = ctypes.POINTER(ctypes.c_double)
+            ppf = ctypes.POINTER(f32p)
+            c_int = ctypes.c_int
+            lib.oracle_capacity.restype = ctypes.c_int64
+            lib.oracle_capacity.argtypes = [ctypes.c_double, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64]
+            lib.oracle_route_tc.argtypes = [c_int, c_int, c_int, c_int, f32p, f32p, f32p, c_int, f32p,
+                                            c_int, i32p, f64p, f64p, f64p, c_int]
+            lib.oracle_route_ec.argtypes = [c_int, c_int, c_int, c_int, f32p, f32p, f32p, i32p, f64p,
+                                            f64p, f64p, c_int]
+            lib.oracle_dispatch_tc.argtypes = [c_int, c_int, c_int, ctypes.c_int64, i32p, i32p, i32p,
+                                               i32p, i32p]
+            lib.oracle_swiglu_expert.restype = None
+            lib.oracle_swiglu_expert.argtypes = [c_int, c_int, f32p, f32p, f32p, f32p, ctypes.c_double, f64p]
+            lib.oracle_forward_tc.argtypes = [c_int, c_int, c_int, c_int, i32p, f32p, i32p, f64p, i32p,
+                                              ppf, ppf, ppf, c_int, c_int, ppf, ppf, ppf, f64p, c_int]
+            lib.oracle_forward_ec.argtypes = [c_int, c_int, c_int, c_int, c_int, i32p, f32p, i32p, f64p,
+                                              ppf, ppf, ppf, c_int, c_int, ppf, ppf, ppf, f64p, c_int]
+            lib.oracle_max_threads.restype = c_int
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):  # torch tensor (any dtype) -> exact fp32 values on the host
+        a = a.detach().float().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _i32(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a, ctype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _ptr_array(mats):
+    """ctypes float** over a list of fp32 arrays (None entries allowed)."""
+    f32p = ctypes.POINTER(ctypes.c_float)
+    arr = (f32p * max(1, len(mats)))()
+    for i, m in enumerate(mats):
+        arr[i] = _ptr(m, ctypes.c_float) if m is not None else f32p()
+    return arr
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def capacity(C: float, T: int, k: int, E: int) -> int:
+    """floor(C*T*k/E); -1 for no limit (C <= 0)."""
+    return int(_load().oracle_capacity(float(C), int(T), int(k), int(E)))
+
+
+def route_tc(x, W_r, k, gate="softmax", logit_offset=None, sel_bias=None, renorm=True,
+             nthreads=1, want_scores=False):
+    """Token-choice routing -> (topk_idx[T,k] int32, topk_w[T,k] f64, gap[T] f64[, scores[T,E]])."""
+    x, W_r = _f32(x), _f32(W_r)
+    lo, sb = _f32(logit_offset), _f32(sel_bias)
+    T, d = x.shape
+    E = W_r.shape[1]
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    gap = np.empty((T,), np.float64)
+    sc = np.empty((T, E), np.float64) if want_scores else None
+    rc = _load().oracle_route_tc(T, d, E, k, _ptr(x, ctypes.c_float), _ptr(W_r, ctypes.c_float),
+                                 _ptr(lo, ctypes.c_float),
+                                 GATE_SIGMOID if gate == "sigmoid" else GATE_SOFTMAX,
+                                 _ptr(sb, ctypes.c_float), int(bool(renorm)),
+                                 _ptr(idx, ctypes.c_int32), _ptr(w, ctypes.c_double),
+                                 _ptr(gap, ctypes.c_double), _ptr(sc, ctypes.c_double), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_route_tc failed ({rc})")
+    return (idx, w, gap, sc) if want_scores else (idx, w, gap)
+
+
+def route_ec(x, W_r, cap, logit_offset=None, nthreads=1, want_scores=False):
+    """Expert Choice routing -> (ec_tok[E,cap] int32, ec_w[E,cap] f64, gap[E] f64[, S[T,E]])."""
+    x, W_r, lo = _f32(x), _f32(W_r), _f32(logit_offset)
+    T, d = x.shape
+    E = W_r.shape[1]
+    tok = np.empty((E, cap), np.int32)
+    w = np.empty((E, cap), np.float64)
+    gap = np.empty((E,), np.float64)
+    S = np.empty((T, E), np.float64) if want_scores else None
+    rc = _load().oracle_route_ec(T, d, E, cap, _ptr(x, ctypes.c_float), _ptr(W_r, ctypes.c_float),
+                                 _ptr(lo, ctypes.c_float), _ptr(tok, ctypes.c_int32),
+                                 _ptr(w, ctypes.c_double), _ptr(gap, ctypes.c_double),
+                                 _ptr(S, ctypes.c_double), nthreads)
+    if rc != 0:
+        raise ValueError(f"oracle_route_ec failed ({rc})")
+    return (tok, w, gap, S) if want_scores else (tok, w, gap)
+
+
+def dispatch_tc(topk_idx, E, cap=-1):
+    """Capacity-limited dispatch -> (off[E+1], cnt_raw[E], slot_of[T,k], row_token[A])."""
+    idx = _i32(topk_idx)
+    T, k = idx.shape
+    off = np.empty(E + 1, np.int32)
+    cnt = np.empty(E, np.int32)
+    slot = np.empty((T, k), np.int32)
+    row_token = np.full(T * k, -1, np.int32)
+    rc = _load().oracle_dispatch_tc(T, k, E, int(cap), _ptr(idx, ctypes.c_int32), _ptr(off, ctypes.c_int32),
+                                    _ptr(cnt, ctypes.c_int32), _ptr(slot, ctypes.c_int32),
+                                    _ptr(row_token, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError(f"oracle_dispatch_tc failed ({rc})")
+    return off, cnt, slot, row_token[: off[E]].copy()
+
+
+def swiglu_expert(x_row, W1, W3, W2, scale=1.0):
+    """(SiLU(x W1) * (x W3)) W2 for one token, fp64."""
+    x_row, W1, W3, W2 = _f32(x_row), _f32(W1), _f32(W3), _f32(W2)
+    d, f = W1.shape
+    out = np.zeros(d, np.float64)
+    _load().oracle_swiglu_expert(d, f, _ptr(x_row, ctypes.c_float), _ptr(W1, ctypes.c_float),
+                                 _ptr(W3, ctypes.c_float), _ptr(W2, ctypes.c_float), float(scale),
+                                 _ptr(out, ctypes.c_double))
+    return out
+
+
+def _expert_mats(W, needed):
+    """Per-expert fp32 host matrices for the experts in ``needed`` (others None)."""
+    return [(_f32(W[e]) if e in needed else None) for e in range(W.shape[0])]
+
+
+def forward_tc(x, topk_idx, topk_w, slot_of, W1, W3, W2, tokens, W1s=None, W3s=None, W2s=None,
+               nthreads=1):
+    """y[len(tokens), d] (f64) for token choice, given routing and dispatch results."""
+    x = _f32(x)
+    idx, slot = _i32(topk_idx), _i32(slot_of)
+    w = np.ascontiguousarray(topk_w, np.float64)
+    tok = _i32(np.asarray(tokens))
+    T, k = idx.shape
+    d = x.shape[1]
+    E, _, f = W1.shape
+    needed = set(int(e) for t in tok for j, e in enumerate(idx[t]) if slot[t, j] >= 0)
+    m1, m3, m2 = _expert_mats(W1, needed), _expert_mats(W3, needed), _expert_mats(W2, needed)
+    ns = 0 if W1s is None else W1s.shape[0]
+    fs = 0 if W1s is None else W1s.shape[2]
+    s1 = [_f32(W1s[s]) for s in range(ns)]
+    s3 = [_f32(W3s[s]) for s in range(ns)]
+    s2 = [_f32(W2s[s]) for s in range(ns)]
+    y = np.zeros((len(tok), d), np.float64)
+    _load().oracle_forward_tc(d, f, k, len(tok), _ptr(tok, ctypes.c_int32), _ptr(x, ctypes.c_float),
+                              _ptr(idx, ctypes.c_int32), _ptr(w, ctypes.c_double),
+                              _ptr(slot, ctypes.c_int32), _ptr_array(m1), _ptr_array(m3),
+                              _ptr_array(m2), ns, fs, _ptr_array(s1), _ptr_array(s3), _ptr_array(s2),
+                              _ptr(y, ctypes.c_double), nthreads)
+    return y
+
+
+def forward_ec(x, ec_tok, ec_w, W1, W3, W2, tokens, W1s=None, W3s=None, W2s=None, nthreads=1):
+    """y[len(tokens), d] (f64) for Expert Choice, given the expert selections."""
+    x = _f32(x)
+    et = _i32(ec_tok)
+    ew = np.ascontiguousarray(ec_w, np.float64)
+    tok = _i32(np.asarray(tokens))
+    E, cap = et.shape
+    d = x.shape[1]
+    f = W1.shape[2]
+    tokset = set(int(t) for t in tok)
+    needed = set(e for e in range(E) if tokset.intersection(et[e].tolist()))
+    m1, m3, m2 = _expert_mats(W1, needed), _expert_mats(W3, needed), _expert_mats(W2, needed)
+    ns = 0 if W1s is None else W1s.shape[0]
+    fs = 0 if W1s is None else W1s.shape[2]
+    s1 = [_f32(W1s[s]) for s in range(ns)]
+    s3 = [_f32(W3s[s]) for s in range(ns)]
+    s2 = [_f32(W2s[s]) for s in range(ns)]
+    y = np.zeros((len(tok), d), np.float64)
+    _load().oracle_forward_ec(d, f, E, cap, len(tok), _ptr(tok, ctypes.c_int32), _ptr(x, ctypes.c_float),
+                              _ptr(et, ctypes.c_int32), _ptr(ew, ctypes.c_double), _ptr_array(m1),
+                              _ptr_array(m3), _ptr_array(m2), ns, fs, _ptr_array(s1), _ptr_array(s3),
+                              _ptr_array(s2), _ptr(y, ctypes.c_double), nthreads)
+    return y
+
+
+def forward(inp: dict, wl, tokens=None, nthreads=1):
+    """The whole layer for ``tokens`` (default: all) of a workload's inputs.
+
+    Routing and dispatch always run over all T tokens (the capacity drop depends on
+    the global token order); the experts and the combine run for ``tokens`` only.
+    Returns a dict with y[len(tokens), d] and every intermediate the stages produce.
+    """
+    x = inp["x"]
+    T = x.shape[0]
+    tokens = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, np.int32)
+    res = {"tokens": tokens}
+    if wl.mode == "ec":
+        ec_tok, ec_w, gap, S = route_ec(x, inp["W_r"], wl.ec_capacity, inp.get("logit_offset"),
+                                        nthreads=nthreads, want_scores=True)
+        res.update(ec_tok=ec_tok, ec_w=ec_w, gap=gap, S=S)
+        res["y"] = forward_ec(x, ec_tok, ec_w, inp["W1"], inp["W3"], inp["W2"], tokens,
+                              inp.get("W1s"), inp.get("W3s"), inp.get("W2s"), nthreads=nthreads)
+        return res
+    idx, w, gap, sc = route_tc(x, inp["W_r"], wl.k, wl.gate, inp.get("logit_offset"), inp.get("sel_bias"),
+                               wl.renorm, nthreads=nthreads, want_scores=True)
+    cap = capacity(wl.capacity_factor, T, wl.k, wl.E)
+    off, cnt_raw, slot_of, row_token = dispatch_tc(idx, wl.E, cap)
+    res.update(topk_idx=idx, topk_w=w, gap=gap, scores=sc, cap=cap, off=off, cnt_raw=cnt_raw,
+               slot_of=slot_of, row_token=row_token)
+    res["y"] = forward_tc(x, idx, w, slot_of, inp["W1"], inp["W3"], inp["W2"], tokens,
+                          inp.get("W1s"), inp.get("W3s"), inp.get("W2s"), nthreads=nthreads)
+    return res

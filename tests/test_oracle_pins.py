@@ -1,0 +1,373 @@
+"""Pins for the CPU oracle: checks against facts other than the oracle itself.
+
+Each check is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong tie-break or drop order) fails:
+brute-force enumeration on tiny inputs, closed forms printed on the pages, special
+cases that reduce to library routines (scipy softmax / expit, numpy matmul), and
+invariants that characterise the result uniquely.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy.special import expit, softmax
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(1000 + seed)
+
+
+def _onehot_x(T, d):
+    x = np.zeros((T, d), np.float32)
+    x[np.arange(T), np.arange(T) % d] = 1.0
+    return x
+
+
+def _silu(z):
+    return z * expit(z)
+
+
+def _dense_swiglu(x, W1, W3, W2):
+    """Textbook matrix form, fp64: (SiLU(x W1) * (x W3)) W2."""
+    x = x.astype(np.float64)
+    return (_silu(x @ W1.astype(np.float64)) * (x @ W3.astype(np.float64))) @ W2.astype(np.float64)
+
+
+# --------------------------------------------------------------------------- capacity
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            rows.append(line.split('"')[0].split())
+    return rows
+
+
+def test_capacity_printed_examples():
+    rows = _golden_rows("capacity.txt")
+    assert rows
+    for C, T, k, E, want in rows:
+        assert oracle.capacity(float(C), int(T), int(k), int(E)) == int(want)
+
+
+def test_capacity_no_limit_and_floor():
+    assert oracle.capacity(0.0, 100, 2, 8) == -1
+    assert oracle.capacity(-1.0, 100, 2, 8) == -1
+    assert oracle.capacity(1.0, 10, 1, 3) == 3          # floor(10/3)
+    assert oracle.capacity(2.0, 7, 2, 4) == 7           # floor(28/4)
+
+
+# --------------------------------------------------------------------------- top-k selection
+
+def _integer_router(T, d, E, seed, lo=-3, hi=4):
+    """One-hot tokens over an integer W_r: logits are exact integers with many ties."""
+    r = _rng(seed)
+    Wr = r.integers(lo, hi, size=(d, E)).astype(np.float32)
+    return _onehot_x(T, d), Wr
+
+
+def _brute_topk(keys, k):
+    """Best k-subset by enumeration: max key sum, then lexicographically smallest."""
+    best, best_sum = None, None
+    for sub in itertools.combinations(range(len(keys)), k):
+        s = sum(keys[e] for e in sub)
+        if best is None or s > best_sum + 1e-12:
+            best, best_sum = sub, s
+    return sorted(best, key=lambda e: (-keys[e], e))
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (4, 2), (6, 3), (8, 2), (8, 3), (8, 8)])
+def test_topk_softmax_matches_bruteforce(E, k):
+    T, d = 48, 48
+    x, Wr = _integer_router(T, d, E, seed=E * 10 + k)
+    idx, w, gap = oracle.route_tc(x, Wr, k, "softmax", renorm=True)
+    for t in range(T):
+        u = Wr[t % d].astype(np.float64)          # softmax is monotone in the logits
+        assert list(idx[t]) == _brute_topk(list(u), k), t
+
+
+@pytest.mark.parametrize("E,k", [(5, 2), (8, 3)])
+def test_topk_sigmoid_bias_matches_bruteforce(E, k):
+    T, d = 40, 40
+    x, Wr = _integer_router(T, d, E, seed=77 + E)
+    b = (_rng(5).integers(-2, 3, size=E) * 0.25).astype(np.float32)
+    idx, w, gap = oracle.route_tc(x, Wr, k, "sigmoid", sel_bias=b, renorm=True)
+    for t in range(T):
+        u = Wr[t % d].astype(np.float64)
+        keys = list(expit(u) + b.astype(np.float64))
+        want = _brute_topk(keys, k)
+        assert list(idx[t]) == want, t
+        s = expit(u[want])
+        np.testing.assert_allclose(w[t], s / s.sum(), rtol=1e-13)   # weights ignore the bias
+
+
+def test_ties_go_to_lowest_index():
+    E, k, T, d = 8, 3, 4, 4
+    x = _onehot_x(T, d)
+    Wr = np.zeros((d, E), np.float32)                 # all logits equal
+    idx, w, gap = oracle.route_tc(x, Wr, k, "softmax", renorm=True)
+    assert (idx == np.array([0, 1, 2], np.int32)).all()
+    np.testing.assert_allclose(w, 1.0 / 3.0, rtol=1e-14)
+    assert (gap == 0.0).all()
+    Wr[:, 5] = 1.0                                      # one clear winner, then ties
+    idx, _, _ = oracle.route_tc(x, Wr, k, "softmax")
+    assert (idx == np.array([5, 0, 1], np.int32)).all()
+
+
+# --------------------------------------------------------------------------- gate weights
+
+def test_switch_top1_weight_is_softmax_max():
+    T, d, E = 64, 32, 16
+    r = _rng(3)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    idx, w, gap = oracle.route_tc(x, Wr, 1, "softmax", renorm=False)
+    p = softmax(x.astype(np.float64) @ Wr.astype(np.float64), axis=1)
+    np.testing.assert_array_equal(idx[:, 0], np.argmax(p, axis=1))
+    np.testing.assert_allclose(w[:, 0], p.max(axis=1), rtol=1e-12)
+
+
+def test_top2_renorm_is_sigmoid_of_logit_gap():
+    # renormalised top-2 softmax weights: w0 = e^{u0} / (e^{u0} + e^{u1}) = expit(u0 - u1)
+    T, d, E = 64, 32, 8
+    r = _rng(4)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    off = r.standard_normal(E).astype(np.float32)
+    idx, w, gap = oracle.route_tc(x, Wr, 2, "softmax", logit_offset=off, renorm=True)
+    u = x.astype(np.float64) @ Wr.astype(np.float64) + off
+    u0 = u[np.arange(T), idx[:, 0]]
+    u1 = u[np.arange(T), idx[:, 1]]
+    np.testing.assert_allclose(w[:, 0], expit(u0 - u1), rtol=1e-12)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, atol=1e-12)
+    assert (u0 >= u1).all()
+
+
+def test_logit_offset_shift_invariance_and_renorm_sum():
+    T, d, E, k = 50, 24, 12, 3
+    r = _rng(6)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    off = (np.round(r.standard_normal(E) * 1024) / 1024).astype(np.float32)   # +2 stays exact
+    i1, w1, _ = oracle.route_tc(x, Wr, k, "softmax", logit_offset=off, renorm=True)
+    i2, w2, _ = oracle.route_tc(x, Wr, k, "softmax", logit_offset=off + np.float32(2.0), renorm=True)
+    np.testing.assert_array_equal(i1, i2)
+    np.testing.assert_allclose(w1, w2, rtol=1e-12)
+    np.testing.assert_allclose(w1.sum(axis=1), 1.0, atol=1e-12)
+    # an offset changes the choice: a huge offset on expert 7 puts it first everywhere
+    off2 = off.copy()
+    off2[7] = 50.0
+    i3, _, _ = oracle.route_tc(x, Wr, k, "softmax", logit_offset=off2)
+    assert (i3[:, 0] == 7).all()
+
+
+def test_selection_bias_forces_choice_but_not_weight():
+    T, d, E, k = 30, 20, 10, 2
+    r = _rng(8)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    b = np.zeros(E, np.float32)
+    b[3] = 5.0
+    idx, w, _ = oracle.route_tc(x, Wr, k, "sigmoid", sel_bias=b, renorm=False)
+    s = expit(x.astype(np.float64) @ Wr.astype(np.float64))
+    assert (idx[:, 0] == 3).all()
+    np.testing.assert_allclose(w[:, 0], s[:, 3], rtol=1e-13)   # raw unbiased score
+
+
+# --------------------------------------------------------------------------- expert FFN
+
+def test_swiglu_unit_values_are_silu():
+    d, f = 4, 6
+    a = np.array([-3.0, -0.5, 0.0, 0.25, 1.0, 4.0])
+    W1 = np.zeros((d, f), np.float32)
+    W1[0] = a
+    W3 = np.zeros((d, f), np.float32)
+    W3[0] = 1.0
+    W2 = np.zeros((f, d), np.float32)
+    W2[np.arange(d), np.arange(d)] = 1.0               # h_c for c < d copied to out_c
+    x = np.zeros(d, np.float32)
+    x[0] = 1.0
+    out = oracle.swiglu_expert(x, W1, W3, W2)
+    np.testing.assert_allclose(out, _silu(a[:d]), rtol=1e-14, atol=1e-300)
+
+
+def test_swiglu_matches_dense_matrix_form_and_linearity():
+    d, f = 24, 40
+    r = _rng(9)
+    x = r.standard_normal((3, d)).astype(np.float32)
+    W1 = (r.standard_normal((d, f)) / math.sqrt(d)).astype(np.float32)
+    W3 = (r.standard_normal((d, f)) / math.sqrt(d)).astype(np.float32)
+    W2 = (r.standard_normal((f, d)) / math.sqrt(f)).astype(np.float32)
+    ref = _dense_swiglu(x, W1, W3, W2)
+    for t in range(3):
+        np.testing.assert_allclose(oracle.swiglu_expert(x[t], W1, W3, W2), ref[t], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(oracle.swiglu_expert(x[t], W1, W3, 2 * W2),
+                                   2 * oracle.swiglu_expert(x[t], W1, W3, W2), rtol=1e-13)
+        assert not oracle.swiglu_expert(x[t], np.zeros_like(W1), W3, W2).any()   # SiLU(0) = 0
+        # swapping W1 and W3 is NOT a symmetry (the gate is SiLU'd): a transposed role fails here
+        assert np.abs(oracle.swiglu_expert(x[t], W3, W1, W2) - ref[t]).max() > 1e-3
+
+
+# --------------------------------------------------------------------------- whole layer
+
+def _layer_inputs(T, d, E, f, seed):
+    r = _rng(seed)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    W1 = (r.standard_normal((E, d, f)) / math.sqrt(d)).astype(np.float32)
+    W3 = (r.standard_normal((E, d, f)) / math.sqrt(d)).astype(np.float32)
+    W2 = (r.standard_normal((E, f, d)) / math.sqrt(f)).astype(np.float32)
+    return x, Wr, W1, W3, W2
+
+
+def test_single_expert_is_dense_swiglu():
+    T, d, f = 20, 16, 32
+    x, Wr, W1, W3, W2 = _layer_inputs(T, d, 1, f, seed=11)
+    idx, w, _ = oracle.route_tc(x, Wr, 1, "softmax", renorm=False)
+    np.testing.assert_allclose(w, 1.0, rtol=0, atol=0)
+    off, cnt, slot, rows = oracle.dispatch_tc(idx, 1, -1)
+    y = oracle.forward_tc(x, idx, w, slot, W1, W3, W2, np.arange(T))
+    np.testing.assert_allclose(y, _dense_swiglu(x, W1[0], W3[0], W2[0]), rtol=1e-11, atol=1e-12)
+
+
+def test_k_equals_E_is_full_softmax_mixture():
+    T, d, E, f = 12, 16, 4, 24
+    x, Wr, W1, W3, W2 = _layer_inputs(T, d, E, f, seed=12)
+    for renorm in (True, False):
+        idx, w, _ = oracle.route_tc(x, Wr, E, "softmax", renorm=renorm)
+        off, cnt, slot, rows = oracle.dispatch_tc(idx, E, -1)
+        y = oracle.forward_tc(x, idx, w, slot, W1, W3, W2, np.arange(T))
+        p = softmax(x.astype(np.float64) @ Wr.astype(np.float64), axis=1)
+        ref = sum(p[:, [e]] * _dense_swiglu(x, W1[e], W3[e], W2[e]) for e in range(E))
+        np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_shared_experts_add_unweighted_and_drops_add_nothing():
+    T, d, E, f, fs = 16, 8, 4, 12, 10
+    x, Wr, W1, W3, W2 = _layer_inputs(T, d, E, f, seed=13)
+    r = _rng(14)
+    W1s = r.standard_normal((2, d, fs)).astype(np.float32)
+    W3s = r.standard_normal((2, d, fs)).astype(np.float32)
+    W2s = r.standard_normal((2, fs, d)).astype(np.float32)
+    idx, w, _ = oracle.route_tc(x, Wr, 2, "softmax")
+    cap = 3
+    off, cnt, slot, rows = oracle.dispatch_tc(idx, E, cap)
+    assert (slot < 0).any()
+    y = oracle.forward_tc(x, idx, w, slot, W1, W3, W2, np.arange(T), W1s, W3s, W2s)
+    ref = sum(_dense_swiglu(x, W1s[s], W3s[s], W2s[s]) for s in range(2))
+    for t in range(T):
+        for j in range(2):
+            if slot[t, j] >= 0:
+                e = idx[t, j]
+                ref[t] += w[t, j] * _dense_swiglu(x[t:t + 1], W1[e], W3[e], W2[e])[0]
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-11)
+
+
+# --------------------------------------------------------------------------- dispatch
+
+def _check_dispatch(idx, E, cap, off, cnt_raw, slot, rows):
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    np.testing.assert_array_equal(cnt_raw, np.bincount(flat, minlength=E))
+    kept_n = np.minimum(cnt_raw, cap) if cap >= 0 else cnt_raw
+    np.testing.assert_array_equal(np.diff(off), kept_n)
+    assert off[0] == 0
+    s = slot.reshape(-1)
+    assert (s >= 0).sum() == off[-1] == T * k - (s < 0).sum()
+    kept = np.sort(s[s >= 0])
+    np.testing.assert_array_equal(kept, np.arange(off[-1]))          # bijection onto rows
+    for e in range(E):
+        pos = np.nonzero(flat == e)[0]                                # (t, j) order
+        sl = s[pos]
+        n_keep = kept_n[e]
+        assert (sl[:n_keep] >= 0).all() and (sl[n_keep:] < 0).all()  # first cap kept, rest dropped
+        np.testing.assert_array_equal(sl[:n_keep], off[e] + np.arange(n_keep))
+    for i in np.nonzero(s >= 0)[0]:
+        assert rows[s[i]] == i // k
+
+
+@pytest.mark.parametrize("T,E,k,cap,skew", [(200, 8, 2, -1, 0.0), (300, 8, 2, 40, 1.5),
+                                            (257, 16, 1, 10, 2.0), (64, 4, 3, 0, 0.0),
+                                            (64, 4, 3, 1000, 0.5), (1, 3, 2, 1, 0.0)])
+def test_dispatch_invariants(T, E, k, cap, skew):
+    r = _rng(T + E + k)
+    p = np.arange(1, E + 1, dtype=np.float64) ** (-skew)
+    p /= p.sum()
+    idx = np.stack([r.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    off, cnt_raw, slot, rows = oracle.dispatch_tc(idx, E, cap)
+    _check_dispatch(idx, E, cap, off, cnt_raw, slot, rows)
+
+
+def test_dispatch_printed_capacity_drop_order():
+    # 15 tokens pick one expert whose capacity is 10 (capacity example of the GPT-4
+    # article, §3.2): the first 10 in token order are kept, the last 5 dropped
+    idx = np.zeros((15, 1), np.int32)
+    cap = oracle.capacity(1.25, 1024, 1, 128)
+    off, cnt_raw, slot, rows = oracle.dispatch_tc(idx, 128, cap)
+    assert cap == 10 and cnt_raw[0] == 15 and off[1] == 10 and off[-1] == 10
+    np.testing.assert_array_equal(slot[:, 0], list(range(10)) + [-1] * 5)
+
+
+# --------------------------------------------------------------------------- expert choice
+
+def test_expert_choice_selection():
+    T, d, E, cap = 96, 16, 6, 20
+    r = _rng(20)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = (r.standard_normal((d, E)) / math.sqrt(d)).astype(np.float32)
+    off = r.standard_normal(E).astype(np.float32)
+    tok, w, gap, S = oracle.route_ec(x, Wr, cap, off, want_scores=True)
+    ref_S = softmax(x.astype(np.float64) @ Wr.astype(np.float64) + off, axis=1)
+    np.testing.assert_allclose(S, ref_S, rtol=1e-12)
+    np.testing.assert_allclose(S.sum(axis=1), 1.0, atol=1e-13)
+    for e in range(E):
+        assert tok.shape[1] == cap                                   # exactly cap per expert
+        assert (np.diff(tok[e]) > 0).all()                           # ascending, distinct
+        want = np.sort(np.argsort(-ref_S[:, e], kind="stable")[:cap])
+        np.testing.assert_array_equal(tok[e], want)
+        np.testing.assert_allclose(w[e], ref_S[tok[e], e], rtol=1e-12)
+        srt = np.sort(ref_S[:, e])[::-1]
+        np.testing.assert_allclose(gap[e], srt[cap - 1] - srt[cap], rtol=1e-9, atol=1e-15)
+
+
+def test_expert_choice_ties_take_lower_tokens_and_layer_sum():
+    T, d, E, cap, f = 10, 4, 3, 4, 6
+    x = np.ones((T, d), np.float32)                                  # identical tokens: all tie
+    Wr = _rng(21).standard_normal((d, E)).astype(np.float32)
+    tok, w, gap = oracle.route_ec(x, Wr, cap)
+    np.testing.assert_array_equal(tok, np.tile(np.arange(cap), (E, 1)))
+    assert (gap == 0).all()
+    r = _rng(22)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    W1 = r.standard_normal((E, d, f)).astype(np.float32)
+    W3 = r.standard_normal((E, d, f)).astype(np.float32)
+    W2 = r.standard_normal((E, f, d)).astype(np.float32)
+    tok, w, gap, S = oracle.route_ec(x, Wr, cap, want_scores=True)
+    y = oracle.forward_ec(x, tok, w, W1, W3, W2, np.arange(T))
+    ref = np.zeros((T, d))
+    for e in range(E):
+        for t in tok[e]:
+            ref[t] += S[t, e] * _dense_swiglu(x[t:t + 1], W1[e], W3[e], W2[e])[0]
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-11)
+    untaken = sorted(set(range(T)) - set(tok.reshape(-1).tolist()))
+    assert all(not y[t].any() for t in untaken)                      # 0 experts -> zero output
+
+
+def test_threads_do_not_change_results():
+    T, d, E = 300, 32, 16
+    r = _rng(30)
+    x = r.standard_normal((T, d)).astype(np.float32)
+    Wr = r.standard_normal((d, E)).astype(np.float32)
+    a = oracle.route_tc(x, Wr, 4, "sigmoid", nthreads=1)
+    b = oracle.route_tc(x, Wr, 4, "sigmoid", nthreads=4)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u, v)
