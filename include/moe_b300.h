@@ -1,0 +1,215 @@
+/*
+ * moe_b300.h -- C ABI of the single-GPU sparsely-gated Mixture-of-Experts SwiGLU
+ * FFN forward for NVIDIA B300 (sm_103a).
+ *
+ * The layer (notation: T tokens, d model width, E routed experts, f expert hidden
+ * width, k experts per token):
+ *
+ *   u = x W_r (+ logit_offset)                       router logits        [T, E]
+ *   p = softmax(u) | sigmoid(u)                      scores
+ *   token choice: top-k of p (+ sel_bias) per token  -> topk_idx, topk_w
+ *   expert choice: top-cap of p[:, e] per expert     -> ec_tok, ec_w
+ *   capacity drop, permute x rows into expert order  -> off, slot_of, x_perm
+ *   per expert e: Y_e = (SiLU(X_e W1_e) * (X_e W3_e)) W2_e
+ *   y[t] = sum_j topk_w[t,j] Y[slot_of[t,j]]  (+ sum of shared experts on x_t)
+ *
+ * Sources (page title, section):
+ *   "技术日报 2026-04-14" (jsqmd.com): §3.1 Top-K gating and y = sum_i G(x)_i E_i(x);
+ *     §3.2 Switch top-1, capacity factor K_max = floor(C N_tokens / N_experts) and
+ *     overflow drop; §3.3 Expert Choice; §3.4 shared experts (DeepSeekMoE);
+ *     §3.5 sigmoid gate; §4.3 selection-only bias; §9.1 MoELayer (renormalised
+ *     top-k weights, shared experts summed unweighted).
+ *   "MoE稀疏架构" (cloud.baidu.com), §4 工作原理: the six-step forward.
+ *   lnwmold.com GPT-4 MoE article, §2.2: experts with W1, W2, W3.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device buffers are caller-owned device memory; the
+ *     library allocates nothing.  Scratch comes from `ws` (`ws_bytes` long, size
+ *     from moe_workspace_size for the same stage).
+ *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  No call synchronises the host, so a sequence of
+ *     calls can be captured in a CUDA graph.
+ *   - Arguments are checked before anything is launched.  A rejected call returns
+ *     a non-zero moe_status and has no side effect.
+ *   - Row-major layouts.  Device buffers must be 16-byte aligned; `ws` and the
+ *     packed weight buffer 256-byte aligned (any torch CUDA allocation is).
+ *   - dtype MOE_BF16: x, W_r, weights, x_perm, Y and y are bf16 (fp32 accumulate);
+ *     dtype MOE_F32: all of those are fp32 (no TF32 anywhere).
+ *     Scores and gate weights are always fp32; indices are int32.
+ *   - Device-side waits are bounded.  A wait that gives up sets a device error
+ *     word; moe_check_device_error reports it as MOE_ERR_TIMEOUT.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad size, mode or null pointer                      */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid but outside this build's limits, or not sm_103 */
+    MOE_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned                    */
+    MOE_ERR_WORKSPACE = 4,     /* ws_bytes smaller than moe_workspace_size()          */
+    MOE_ERR_CUDA = 5,          /* a CUDA runtime call failed                          */
+    MOE_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up                  */
+} moe_status;
+
+typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
+typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_mode;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum {
+    MOE_STAGE_ROUTE = 0,
+    MOE_STAGE_DISPATCH = 1,
+    MOE_STAGE_GROUPED_FFN = 2,
+    MOE_STAGE_COMBINE = 3,
+    MOE_STAGE_FORWARD = 4
+} moe_stage;
+
+/*
+ * Problem statement of one layer.
+ *   T >= 0 tokens; d model width; E routed experts (1..256); f expert hidden width.
+ *   k: experts per token, token choice only (1..min(8, E)).
+ *   gate: MOE_GATE_SOFTMAX ("技术日报" §3.2) or MOE_GATE_SIGMOID (§3.5).
+ *   mode: MOE_TOKEN_CHOICE (§3.1) or MOE_EXPERT_CHOICE (§3.3, softmax affinity).
+ *   renormalize: token choice; 1 divides the k selected scores by their sum (§9.1),
+ *     0 keeps the raw score (Switch top-1, §3.2).
+ *   capacity_factor: token choice; C > 0 limits every expert to
+ *     floor(C * T * k / E) assignments, kept in token order, the rest dropped
+ *     (§3.2); C <= 0 means no limit.
+ *   ec_capacity: expert choice; tokens each expert takes (1..T).
+ *   n_shared, f_shared: always-on shared experts (§3.4), each of hidden width
+ *     f_shared; their outputs are added unweighted.
+ *   dtype: MOE_BF16 or MOE_F32.
+ * Build limits: MOE_BF16 needs d % 128 == 0, f % 64 == 0, f_shared % 64 == 0;
+ * MOE_F32 needs d % 64 == 0, f % 64 == 0, f_shared % 64 == 0.
+ */
+typedef struct moe_config {
+    int32_t T, d, E, f, k;
+    int32_t gate;
+    int32_t mode;
+    int32_t renormalize;
+    float capacity_factor;
+    int32_t ec_capacity;
+    int32_t n_shared, f_shared;
+    int32_t dtype;
+} moe_config;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *moe_status_string(moe_status s);
+
+/* Checks a configuration against the rules above.  No CUDA call. */
+moe_status moe_validate_config(const moe_config *cfg);
+
+/* Capacity of one expert, floor(C*T*k/E) ("技术日报" §3.2), or -1 when
+ * unlimited (token choice with C <= 0).  Expert choice: ec_capacity.  No CUDA call. */
+moe_status moe_expert_capacity(const moe_config *cfg, int32_t *cap);
+
+/* Rows of the expert-ordered buffers x_perm / Y a caller must provide:
+ *   rows_routed = T*k (token choice) or E*ec_capacity (expert choice);
+ *   rows_total  = rows_routed + (n_shared > 0 ? T : 0).  No CUDA call. */
+moe_status moe_buffer_rows(const moe_config *cfg, int64_t *rows_routed, int64_t *rows_total);
+
+/* Scratch bytes a stage needs in `ws` (MOE_STAGE_FORWARD: the whole layer).  No CUDA call. */
+moe_status moe_workspace_size(const moe_config *cfg, moe_stage stage, size_t *bytes);
+
+/* Bytes of the packed expert-weight buffer moe_pack_weights writes.  No CUDA call. */
+moe_status moe_packed_weights_size(const moe_config *cfg, size_t *bytes);
+
+/*
+ * One-time re-layout of the expert weights into the operand layout of the grouped
+ * expert GEMM (not part of the timed forward).
+ *   W1, W3: [E][d][f], W2: [E][f][d] (the pages' per-expert x W1, h W2 layout);
+ *   W1s, W3s: [n_shared][d][f_shared], W2s: [n_shared][f_shared][d] (NULL when
+ *   n_shared == 0).  All in cfg->dtype, device memory, read only.
+ *   packed: device buffer of moe_packed_weights_size bytes, written on `stream`.
+ */
+moe_status moe_pack_weights(const moe_config *cfg, const void *W1, const void *W3, const void *W2,
+                            const void *W1s, const void *W3s, const void *W2s, void *packed,
+                            size_t packed_bytes, void *stream);
+
+/*
+ * Router ("技术日报" §3.1-§3.3, §3.5, §4.3; "MoE稀疏架构" §4 steps 1-2).
+ *   x: [T][d], W_r: [d][E] (cfg->dtype).  logit_offset: [E] fp32 added to the
+ *   logits before scoring, or NULL.  sel_bias: [E] fp32 added to the scores for
+ *   the token-choice selection only (weights use the unbiased score), or NULL.
+ * Token choice writes topk_idx[T][k] (int32, slots in descending key order, ties to
+ *   the lower expert index) and topk_w[T][k] (fp32).
+ * Expert choice writes topk_idx as ec_tok[E][cap] (int32, ascending token ids; ties
+ *   to the lower token index) and topk_w as ec_w[E][cap] = softmax score of that
+ *   token for that expert.
+ */
+moe_status moe_route(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
+                     const float *sel_bias, int32_t *topk_idx, float *topk_w, void *ws,
+                     size_t ws_bytes, void *stream);
+
+/*
+ * Capacity-limited dispatch ("技术日报" §3.2; "MoE稀疏架构" §4 step 3).
+ * Token choice: topk_idx[T][k] (values in [0, E)).  Assignments are visited in
+ *   token order, slots in order; the first `cap` assignments of each expert are
+ *   kept.  Writes
+ *     cnt_raw[E]   assignments per expert before the drop,
+ *     off[E+1]     exclusive prefix sum of the kept counts (off[E] = rows used),
+ *     slot_of[T][k] row of the assignment in x_perm, -1 when dropped,
+ *     x_perm[rows_routed][d] rows [0, off[E]) = x[token of the row] (rest untouched).
+ * Expert choice: topk_idx is ec_tok[E][cap]; writes off[e] = e*cap, cnt_raw[e] = cap,
+ *   slot_of[T][E] (row e*cap + r when expert e took the token as its r-th pick, else
+ *   -1) and x_perm[E*cap][d].
+ */
+moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *off,
+                        int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
+                        void *stream);
+
+/*
+ * Grouped SwiGLU experts over the ragged expert segments of x_perm ("lnwmold"
+ * §2.2 W1, W2, W3; SwiGLU: (SiLU(X W1) * (X W3)) W2).
+ *   x_perm[rows_routed][d], off[E+1] as written by moe_dispatch (read on the device;
+ *   no host synchronisation), packed: moe_pack_weights output, x: [T][d] input of
+ *   the shared experts (NULL when n_shared == 0).
+ *   Y[rows_total][d]: rows [0, off[E]) = expert outputs in x_perm order; with shared
+ *   experts, rows [rows_routed, rows_routed + T) = sum of the shared experts on x.
+ */
+moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int32_t *off,
+                           const void *packed, const void *x, void *Y, void *ws, size_t ws_bytes,
+                           void *stream);
+
+/*
+ * Gate-weighted combine back to token order ("技术日报" §3.1, §3.4, §9.1).
+ * Token choice: y[t] = sum_{j: slot_of[t][j] >= 0} topk_w[t][j] * Y[slot_of[t][j]]
+ *   (+ Y[rows_routed + t] with shared experts), slots in order.
+ * Expert choice: y[t] = sum_{e: slot_of[t][e] >= 0} ec_w[slot] * Y[slot]
+ *   (+ shared), experts in ascending order; `topk_w` is ec_w[E][cap].
+ *   y: [T][d] in cfg->dtype, fp32 accumulation.  Dropped or unpicked tokens get
+ *   only the shared part (zero without shared experts); the residual is the
+ *   caller's.
+ */
+moe_status moe_combine(const moe_config *cfg, const void *Y, const int32_t *slot_of, const float *topk_w,
+                       void *y, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * The whole layer: moe_route -> moe_dispatch -> moe_grouped_ffn -> moe_combine, with
+ * every intermediate carved from `ws` (moe_workspace_size(MOE_STAGE_FORWARD)).
+ *   x: [T][d]; W_r: [d][E]; logit_offset, sel_bias: as moe_route; packed: as
+ *   moe_grouped_ffn; y: [T][d] output.
+ */
+moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
+                       const float *sel_bias, const void *packed, void *y, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word.  Returns
+ * MOE_ERR_TIMEOUT if a bounded device-side wait gave up since the last check,
+ * MOE_ERR_INVALID_ARG if a kernel skipped an expert or token id outside its range
+ * (such an assignment is treated as dropped), MOE_OK otherwise.
+ */
+moe_status moe_check_device_error(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,139 @@
+// Gate-weighted combine back to token order ("技术日报 2026-04-14" §3.1:
+// y = sum_i G(x)_i E_i(x); §3.4 / §9.1: shared experts added unweighted;
+// "MoE稀疏架构" §4 step 5).
+//
+// One warp per token.  The warp first lists the token's (row, weight) pairs in
+// order -- slots j = 0..k-1 for token choice, experts e ascending for Expert
+// Choice -- then every lane accumulates 16-byte vectors of those Y rows in fp32
+// and writes the token's output row once.
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename T>
+struct Vec;   // 16 bytes of T
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+};
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+};
+
+template <typename T>
+__device__ __forceinline__ void accumulate(float (&acc)[Vec<T>::N], const uint4 &v, float w) {
+    if constexpr (sizeof(T) == 4) {
+        acc[0] = fmaf(w, __uint_as_float(v.x), acc[0]);
+        acc[1] = fmaf(w, __uint_as_float(v.y), acc[1]);
+        acc[2] = fmaf(w, __uint_as_float(v.z), acc[2]);
+        acc[3] = fmaf(w, __uint_as_float(v.w), acc[3]);
+    } else {
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack(const float (&acc)[Vec<T>::N]) {
+    uint4 v;
+    if constexpr (sizeof(T) == 4) {
+        v.x = __float_as_uint(acc[0]);
+        v.y = __float_as_uint(acc[1]);
+        v.z = __float_as_uint(acc[2]);
+        v.w = __float_as_uint(acc[3]);
+    } else {
+        __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    }
+    return v;
+}
+
+struct CombineArgs {
+    const uint4 *Y;
+    const int32_t *slot_of;
+    const float *w;
+    uint4 *y;
+    int T, E, k, mode, vecs;
+    int64_t shared_row0;   // first shared row of Y, -1 without shared experts
+};
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
+    __shared__ int s_row[kWarps][kMaxE];
+    __shared__ float s_w[kWarps][kMaxE];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int per_tok = (a.mode == MOE_EXPERT_CHOICE) ? a.E : a.k;
+    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+        int n = 0;
+        for (int j0 = 0; j0 < per_tok; j0 += 32) {
+            const int j = j0 + lane;
+            int row = -1;
+            float w = 0.f;
+            if (j < per_tok) {
+                row = a.slot_of[(size_t)t * per_tok + j];
+                if (row >= 0) w = (a.mode == MOE_EXPERT_CHOICE) ? a.w[row] : a.w[(size_t)t * per_tok + j];
+            }
+            const unsigned b = __ballot_sync(0xffffffffu, row >= 0);
+            if (row >= 0) {
+                const int p = n + __popc(b & ((1u << lane) - 1u));
+                s_row[warp][p] = row;
+                s_w[warp][p] = w;
+            }
+            n += __popc(b);
+        }
+        __syncwarp();
+        const uint4 *ys = a.shared_row0 >= 0 ? a.Y + (size_t)(a.shared_row0 + t) * a.vecs : nullptr;
+        for (int v = lane; v < a.vecs; v += 32) {
+            float acc[Vec<T>::N];
+#pragma unroll
+            for (int i = 0; i < Vec<T>::N; ++i) acc[i] = 0.f;
+            int i = 0;
+            for (; i + 1 < n; i += 2) {   // two rows in flight
+                const uint4 r0 = a.Y[(size_t)s_row[warp][i] * a.vecs + v];
+                const uint4 r1 = a.Y[(size_t)s_row[warp][i + 1] * a.vecs + v];
+                accumulate<T>(acc, r0, s_w[warp][i]);
+                accumulate<T>(acc, r1, s_w[warp][i + 1]);
+            }
+            if (i < n) accumulate<T>(acc, a.Y[(size_t)s_row[warp][i] * a.vecs + v], s_w[warp][i]);
+            if (ys) accumulate<T>(acc, ys[v], 1.f);
+            a.y[(size_t)t * a.vecs + v] = pack<T>(acc);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, const int32_t *slot_of,
+                           const float *w, void *y, cudaStream_t s) {
+    CombineArgs a;
+    a.Y = static_cast<const uint4 *>(Y);
+    a.slot_of = slot_of;
+    a.w = w;
+    a.y = static_cast<uint4 *>(y);
+    a.T = c.T;
+    a.E = c.E;
+    a.k = c.k;
+    a.mode = c.mode;
+    a.vecs = c.d * z.elt / 16;
+    a.shared_row0 = (c.n_shared > 0) ? z.rows_routed : -1;
+    int blocks = (c.T + kWarps - 1) / kWarps;
+    const int cap = num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (c.dtype == MOE_F32) combine_kernel<float><<<blocks, 32 * kWarps, 0, s>>>(a);
+    else combine_kernel<__nv_bfloat16><<<blocks, 32 * kWarps, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

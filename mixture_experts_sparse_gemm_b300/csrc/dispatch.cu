@@ -1,0 +1,194 @@
+// Capacity-limited dispatch: a stable counting sort of the (token, slot)
+// assignments by expert, with the capacity drop applied in token order, followed
+// by a 16-byte vectorised row gather of x into expert order.
+//
+// Follows "技术日报 2026-04-14" (jsqmd.com) §3.2 (capacity K_max and overflow drop)
+// and "MoE稀疏架构" (cloud.baidu.com) §4 step 3 (inputs distributed to the chosen
+// experts).  The kept assignments of expert e are its first cap assignments in
+// (token, slot) order; they occupy rows off[e] .. off[e+1]-1 in that order.
+//
+// Kernels (token choice):
+//   count  : one warp per chunk of 256 assignments -> per-chunk expert counts
+//   scan   : one CTA; per expert, running base over the chunks, raw count,
+//            capped count, and the exclusive scan of capped counts -> off[]
+//   rank   : one warp per chunk; __match_any_sync groups the lanes holding the
+//            same expert so ranks follow assignment order -> slot_of, row_token
+//   gather : one warp per destination row, 16-byte vectors -> x_perm
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kChunk = 256;          // assignments per warp-chunk
+constexpr int kWarpsPerCta = 4;
+
+__global__ void __launch_bounds__(32 * kWarpsPerCta)
+    dispatch_count_kernel(const int32_t *idx, int64_t n, int E, int nchunks, int32_t *chunk_cnt) {
+    extern __shared__ int cnt[];   // [kWarpsPerCta][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x * kWarpsPerCta + warp;
+    int *my = cnt + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    if (chunk < nchunks) {
+        for (int i = lane; i < kChunk; i += 32) {
+            const int64_t a = (int64_t)chunk * kChunk + i;
+            if (a < n) {
+                const int e = idx[a];
+                if ((unsigned)e < (unsigned)E) atomicAdd(&my[e], 1);
+            }
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) chunk_cnt[(size_t)chunk * E + e] = my[e];
+    }
+}
+
+__global__ void __launch_bounds__(256)
+    dispatch_scan_kernel(int32_t *chunk_cnt, int nchunks, int E, int cap, int32_t *cnt_raw, int32_t *off) {
+    __shared__ int kept[kMaxE];
+    const int e = threadIdx.x;
+    if (e < E) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int v = chunk_cnt[(size_t)c * E + e];
+            chunk_cnt[(size_t)c * E + e] = run;   // base of this chunk inside expert e
+            run += v;
+        }
+        cnt_raw[e] = run;
+        kept[e] = (cap < 0) ? run : min(run, cap);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int i = 0; i < E; ++i) {
+            off[i] = acc;
+            acc += kept[i];
+        }
+        off[E] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(32 * kWarpsPerCta)
+    dispatch_rank_kernel(const int32_t *idx, int64_t n, int k, int E, int nchunks, const int32_t *chunk_base,
+                         const int32_t *off, int cap, int32_t *slot_of, int32_t *row_token, unsigned *err) {
+    extern __shared__ int run[];   // [kWarpsPerCta][E]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x * kWarpsPerCta + warp;
+    if (chunk >= nchunks) return;
+    int *my = run + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = chunk_base[(size_t)chunk * E + e];
+    __syncwarp();
+    for (int step = 0; step < kChunk / 32; ++step) {
+        const int64_t a = (int64_t)chunk * kChunk + step * 32 + lane;
+        const int e_in = (a < n) ? idx[a] : -1;
+        const bool valid = (unsigned)e_in < (unsigned)E;   // out-of-range ids are dropped and flagged
+        if (a < n && !valid) {
+            slot_of[a] = -1;
+            atomicOr(err, kErrBadIndex);
+        }
+        const int e = valid ? e_in : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank_in = __popc(peers & ((1u << lane) - 1u));
+        const int base = valid ? my[e] : 0;
+        __syncwarp();
+        if (valid && rank_in == 0) my[e] = base + __popc(peers);
+        __syncwarp();
+        if (valid) {
+            const int r = base + rank_in;
+            const int slot = (cap < 0 || r < cap) ? off[e] + r : -1;
+            slot_of[a] = slot;
+            if (slot >= 0) row_token[slot] = (int32_t)(a / k);
+        }
+    }
+}
+
+// x_perm[row] = x[row_token[row]] for row < *rows (read on the device).
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint4 *__restrict__ x, int vecs, const int32_t *__restrict__ row_token,
+                       const int32_t *__restrict__ rows_dev, int64_t rows_host, uint4 *__restrict__ x_perm) {
+    const int64_t rows = rows_dev ? (int64_t)*rows_dev : rows_host;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31;
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+        const uint4 *src = x + (size_t)row_token[r] * vecs;
+        uint4 *dst = x_perm + (size_t)r * vecs;
+        int v = lane;
+        for (; v + 96 < vecs; v += 128) {
+            const uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
+            dst[v] = a0;
+            dst[v + 32] = a1;
+            dst[v + 64] = a2;
+            dst[v + 96] = a3;
+        }
+        for (; v < vecs; v += 32) dst[v] = src[v];
+    }
+}
+
+// Expert choice: off[e] = e*cap, cnt_raw[e] = cap, slot_of[t][e] = e*cap + r.
+__global__ void ec_slots_kernel(const int32_t *ec_tok, int T, int E, int cap, int32_t *off, int32_t *cnt_raw,
+                                int32_t *slot_of, unsigned *err) {
+    const int64_t n = (int64_t)E * cap;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t first = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int64_t e = first; e <= E; e += stride) {
+        off[e] = (int32_t)(e * cap);
+        if (e < E) cnt_raw[e] = cap;
+    }
+    for (int64_t i = first; i < n; i += stride) {
+        const int e = (int)(i / cap);
+        const int t = ec_tok[i];
+        if ((unsigned)t < (unsigned)T) slot_of[(size_t)t * E + e] = (int32_t)i;
+        else atomicOr(err, kErrBadIndex);
+    }
+}
+
+int gather_grid(int64_t rows) {
+    const int64_t warps_needed = rows;
+    int64_t blocks = (warps_needed + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+}  // namespace
+
+size_t dispatch_tc_scratch_ints(int64_t assignments, int E) {
+    const int64_t nchunks = (assignments + kChunk - 1) / kChunk;
+    return (size_t)(nchunks * E) + (size_t)assignments;   // chunk counts + row_token
+}
+
+cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
+                               int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
+                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s) {
+    const int64_t n = (int64_t)c.T * c.k;
+    const int nchunks = (int)((n + kChunk - 1) / kChunk);
+    const int blocks = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
+    const size_t smem = sizeof(int) * kWarpsPerCta * c.E;
+    dispatch_count_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.E, nchunks, chunk_cnt);
+    dispatch_scan_kernel<<<1, 256, 0, s>>>(chunk_cnt, nchunks, c.E, cap, cnt_raw, off);
+    dispatch_rank_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.k, c.E, nchunks, chunk_cnt, off,
+                                                                 cap, slot_of, row_token, err);
+    const int elt = c.dtype == MOE_F32 ? 4 : 2;
+    const int vecs = c.d * elt / 16;
+    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,
+                                                      static_cast<uint4 *>(x_perm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
+                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s) {
+    const int64_t n = (int64_t)c.E * c.ec_capacity;
+    cudaError_t ce = cudaMemsetAsync(slot_of, 0xff, sizeof(int32_t) * (size_t)c.T * c.E, s);
+    if (ce != cudaSuccess) return ce;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > num_sms() * 4) blocks = num_sms() * 4;
+    ec_slots_kernel<<<blocks, 256, 0, s>>>(ec_tok, c.T, c.E, c.ec_capacity, off, cnt_raw, slot_of, err);
+    const int elt = c.dtype == MOE_F32 ? 4 : 2;
+    const int vecs = c.d * elt / 16;
+    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, ec_tok, nullptr, n,
+                                                      static_cast<uint4 *>(x_perm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,149 @@
+// Internal declarations shared by the CUDA translation units of the MoE library.
+// Nothing here is part of the C ABI (that is include/moe_b300.h).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_b300.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;     // routed experts
+constexpr int kMaxK = 8;       // experts per token (token choice)
+constexpr int kGroup = 64;     // W1/W3 interleave width of the packed up-projection
+
+// bits of the device error word
+constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrBadIndex = 2u;     // an expert or token id outside its range was skipped
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------------------- sizes
+struct Sizes {
+    int64_t rows_routed;   // T*k (token choice) or E*cap (expert choice)
+    int64_t rows_total;    // + T when shared experts exist
+    int32_t cap;           // per-expert capacity, -1 unlimited
+    int32_t fs_tot;        // n_shared * f_shared
+    int32_t elt;           // bytes per element of cfg->dtype
+};
+Sizes sizes_of(const moe_config &c);
+
+// Byte offsets inside the packed weight buffer.
+//   w13 : [E][2f][d]      up-projection, K-major, W1/W3 interleaved in groups of kGroup rows
+//   w2  : [E][d][f]       down-projection, K-major
+//   w13s: [2*fs_tot][d]   shared experts merged along the hidden dimension
+//   w2s : [d][fs_tot]
+struct PackedLayout {
+    size_t w13, w2, w13s, w2s, total;
+};
+PackedLayout packed_layout(const moe_config &c);
+
+// ----------------------------------------------------------------------------- grouped segments
+// Segment s < E is routed expert s (rows off[s]..off[s+1] of the expert-ordered
+// buffer); segment E, when present, is the merged shared expert over all T tokens.
+struct GroupedShape {
+    const int32_t *off;   // device [E+1]
+    int E;
+    int shared_rows;      // T when shared experts exist, else 0
+    int nblk_routed;      // N tiles per routed segment
+    int nblk_shared;      // N tiles of the shared segment
+};
+
+// ----------------------------------------------------------------------------- launchers
+cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_r,
+                              const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
+                              float *topk_w, float *scores_t, unsigned *err, cudaStream_t s);
+cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
+                             cudaStream_t s);
+cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
+                               int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
+                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);
+size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
+cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
+                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s);
+cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, const int32_t *slot_of,
+                           const float *w, void *y, cudaStream_t s);
+cudaError_t launch_pack(const moe_config &c, const void *W1, const void *W3, const void *W2,
+                        const void *W1s, const void *W3s, const void *W2s, void *packed, cudaStream_t s);
+cudaError_t launch_ffn_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                            const void *packed, const void *x, void *H, void *Hs, void *Y,
+                            cudaStream_t s);
+
+// tcgen05 path (bf16)
+struct TcFfnScratch {
+    void *H;      // [rows_routed][f] bf16
+    void *Hs;     // [T][fs_tot] bf16
+};
+cudaError_t launch_ffn_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                               const void *packed, const void *x, void *H, void *Hs, void *Y,
+                               unsigned *err, cudaStream_t s);
+cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r,
+                                 const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
+                                 float *topk_w, float *scores_t, void *wr_t, unsigned *err,
+                                 cudaStream_t s);
+size_t route_tcgen05_scratch_bytes(const moe_config &c);
+bool route_tcgen05_supported(const moe_config &c);
+
+int num_sms();
+
+// ----------------------------------------------------------------------------- device helpers
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Tile table of a grouped problem, built once per CTA in shared memory:
+// tile_start[s] = first tile of segment s (tile_start[S] = total tiles).
+// Segment tiles are ordered N-block-major with the M-block fastest, so the
+// CTAs that share a weight tile run at the same time.
+template <int BM>
+__device__ __forceinline__ int build_tile_table(const GroupedShape &g, int *tile_start, int *seg_row0,
+                                                int *seg_rows) {
+    const int S = g.E + (g.shared_rows > 0 ? 1 : 0);
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        int r0, n;
+        if (s < g.E) {
+            r0 = g.off[s];
+            n = g.off[s + 1] - r0;
+        } else {
+            r0 = 0;
+            n = g.shared_rows;
+        }
+        seg_row0[s] = r0;
+        seg_rows[s] = n;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = 0;
+        for (int s = 0; s < S; ++s) {
+            tile_start[s] = acc;
+            const int nb = (s < g.E) ? g.nblk_routed : g.nblk_shared;
+            acc += ((seg_rows[s] + BM - 1) / BM) * nb;
+        }
+        tile_start[S] = acc;
+    }
+    __syncthreads();
+    return S;
+}
+
+template <int BM>
+__device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *tile_start, const int *seg_rows,
+                                            int S, int tile, int &s, int &mb, int &nb) {
+    int lo = 0, hi = S - 1;   // last s with tile_start[s] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    s = lo;
+    const int local = tile - tile_start[s];
+    const int mblk = (seg_rows[s] + BM - 1) / BM;
+    mb = local % mblk;
+    nb = local / mblk;
+}
+
+}  // namespace moe

@@ -1,0 +1,319 @@
+// Router on CUDA cores: logits, scores, token-choice top-k and the Expert Choice
+// column selection.
+//
+// Follows "技术日报 2026-04-14" (jsqmd.com) §3.1 (KeepTopK / Softmax gating), §3.2
+// (softmax score p_i, Switch top-1), §3.3 (Expert Choice: each expert takes the top
+// tokens of its column), §3.5 (sigmoid score), §4.3 (bias used for selection only),
+// §9.1 (weights renormalised over the selected k).
+//
+// route_simt_kernel: one CTA computes the logits of 32 tokens for all E experts
+// (fp32 FMA over d, x and W_r staged through shared memory), then every warp
+// scores 4 tokens and selects their top-k with warp shuffles: each lane holds the
+// keys of experts lane, lane+32, ...; k rounds of a warp arg-max on (key, -index)
+// give the slots in descending key order with ties to the lower expert index.
+#include <float.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kTM = 32;    // tokens per CTA
+constexpr int kKC = 32;    // d-chunk staged per step
+constexpr int kThreads = 256;
+
+struct RouteArgs {
+    const void *x;
+    const void *Wr;
+    const float *logit_offset;
+    const float *sel_bias;
+    int T, d, E, k, gate, mode, renorm;
+    int32_t *topk_idx;
+    float *topk_w;
+    float *scores_t;   // expert choice: [E][T]
+};
+
+template <typename Tin, int NPT>
+__global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
+    extern __shared__ float smem[];
+    float *xs = smem;                       // [kTM][kKC + 1]
+    float *wsm = xs + kTM * (kKC + 1);      // [kKC][E]   later reused as logits [kTM][E]
+    const Tin *x = static_cast<const Tin *>(a.x);
+    const Tin *Wr = static_cast<const Tin *>(a.Wr);
+    const int E = a.E, d = a.d;
+    const int t0 = blockIdx.x * kTM;
+    const int tid = threadIdx.x;
+
+    float acc[NPT];
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) acc[i] = 0.f;
+
+    for (int k0 = 0; k0 < d; k0 += kKC) {
+        for (int i = tid; i < kTM * kKC; i += kThreads) {
+            const int m = i / kKC, kk = i % kKC;
+            const int t = t0 + m;
+            xs[m * (kKC + 1) + kk] = (t < a.T && k0 + kk < d) ? to_f32(x[(size_t)t * d + k0 + kk]) : 0.f;
+        }
+        for (int i = tid; i < kKC * E; i += kThreads) {
+            const int kk = i / E, e = i % E;
+            wsm[i] = (k0 + kk < d) ? to_f32(Wr[(size_t)(k0 + kk) * E + e]) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < NPT; ++i) {
+            const int o = tid + i * kThreads;
+            if (o < kTM * E) {
+                const int m = o / E, e = o % E;
+                float s = acc[i];
+#pragma unroll 8
+                for (int kk = 0; kk < kKC; ++kk) s = fmaf(xs[m * (kKC + 1) + kk], wsm[kk * E + e], s);
+                acc[i] = s;
+            }
+        }
+        __syncthreads();
+    }
+    float *lg = wsm;   // [kTM][E]
+#pragma unroll
+    for (int i = 0; i < NPT; ++i) {
+        const int o = tid + i * kThreads;
+        if (o < kTM * E) {
+            const int e = o % E;
+            lg[o] = acc[i] + (a.logit_offset ? a.logit_offset[e] : 0.f);
+        }
+    }
+    __syncthreads();
+
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int kPerLane = kMaxE / 32;
+    for (int m = warp; m < kTM; m += kThreads / 32) {
+        const int t = t0 + m;
+        if (t >= a.T) break;
+        float u[kPerLane], p[kPerLane];
+        float mx = -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            u[i] = (e < E) ? lg[m * E + e] : -FLT_MAX;
+            mx = fmaxf(mx, u[i]);
+        }
+        if (a.gate == MOE_GATE_SIGMOID) {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) p[i] = 1.f / (1.f + expf(-u[i]));
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) {
+                const int e = lane + 32 * i;
+                p[i] = (e < E) ? expf(u[i] - mx) : 0.f;
+                sum += p[i];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            const float inv = 1.f / sum;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) p[i] *= inv;
+        }
+
+        if (a.mode == MOE_EXPERT_CHOICE) {
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) a.scores_t[(size_t)e * a.T + t] = p[i];
+            }
+            continue;
+        }
+
+        float key[kPerLane];
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            key[i] = (e < E) ? p[i] + (a.sel_bias ? a.sel_bias[e] : 0.f) : -FLT_MAX;
+        }
+        unsigned chosen = 0;     // bit i: expert lane + 32 i already selected
+        float wsum = 0.f, wj = 0.f;
+        int ij = 0;
+        for (int j = 0; j < a.k; ++j) {
+            float bk = -FLT_MAX, bp = 0.f;
+            int bi = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E && !(chosen >> i & 1u) && key[i] > bk) {   // ascending e: ties keep the lower
+                    bk = key[i];
+                    bi = e;
+                    bp = p[i];
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+                if (ok > bk || (ok == bk && oi < bi)) {
+                    bk = ok;
+                    bi = oi;
+                    bp = op;
+                }
+            }
+            if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
+            wsum += bp;
+            if (lane == j) {
+                ij = bi;
+                wj = bp;
+            }
+        }
+        if (lane < a.k) {
+            a.topk_idx[(size_t)t * a.k + lane] = ij;
+            a.topk_w[(size_t)t * a.k + lane] = a.renorm ? wj / wsum : wj;
+        }
+    }
+}
+
+template <typename Tin, int NPT>
+cudaError_t launch_npt(const RouteArgs &a, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (kTM * (kKC + 1) + kKC * a.E);
+    auto kern = route_simt_kernel<Tin, NPT>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const int grid = (a.T + kTM - 1) / kTM;
+    kern<<<grid, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_typed(const RouteArgs &a, cudaStream_t s) {
+    const int npt = (kTM * a.E + kThreads - 1) / kThreads;
+    if (npt <= 1) return launch_npt<Tin, 1>(a, s);
+    if (npt <= 2) return launch_npt<Tin, 2>(a, s);
+    if (npt <= 4) return launch_npt<Tin, 4>(a, s);
+    if (npt <= 8) return launch_npt<Tin, 8>(a, s);
+    if (npt <= 16) return launch_npt<Tin, 16>(a, s);
+    return launch_npt<Tin, 32>(a, s);
+}
+
+// ----------------------------------------------------------------------------- expert choice
+// One CTA per expert.  The column S[:, e] (non-negative floats, so their bit
+// patterns order like the values) goes through a 4-pass, 8-bit radix select for
+// the cap-th largest key K; every token with key > K is taken, plus the lowest
+// token indices among those with key == K until cap are taken.  The taken tokens
+// are written in ascending token order with a block-wide ordered compaction.
+constexpr int kEcThreads = 1024;
+
+__device__ __forceinline__ int block_exclusive_scan_flag(bool flag, int *warp_tot, int &block_total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned b = __ballot_sync(0xffffffffu, flag);
+    const int in_warp = __popc(b & ((1u << lane) - 1u));
+    if (lane == 0) warp_tot[warp] = __popc(b);
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int v = (lane < nw) ? warp_tot[lane] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (lane < nw) warp_tot[32 + lane] = incl - v;
+        if (lane == 31) warp_tot[64] = incl;
+    }
+    __syncthreads();
+    const int r = warp_tot[32 + warp] + in_warp;
+    block_total = warp_tot[64];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scores_t, int T, int cap,
+                                                                 int32_t *ec_tok, float *ec_w) {
+    __shared__ unsigned hist[256];
+    __shared__ int warp_tot[65];
+    __shared__ unsigned s_digit;
+    __shared__ int s_remaining;
+    const int e = blockIdx.x;
+    const unsigned *col = reinterpret_cast<const unsigned *>(scores_t + (size_t)e * T);
+
+    unsigned prefix = 0, mask = 0;
+    int remaining = cap;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        for (int t = threadIdx.x; t < T; t += blockDim.x) {
+            const unsigned u = col[t];
+            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int cum = 0;
+            unsigned dg = 0;
+            for (int b = 255; b >= 0; --b) {
+                const int h = (int)hist[b];
+                if (cum + h >= remaining) {
+                    dg = (unsigned)b;
+                    break;
+                }
+                cum += h;
+            }
+            s_digit = dg;
+            s_remaining = remaining - cum;
+        }
+        __syncthreads();
+        prefix |= s_digit << shift;
+        mask |= 255u << shift;
+        remaining = s_remaining;
+        __syncthreads();
+    }
+    const unsigned K = prefix;   // remaining = ties at K still to take
+    int eq_base = 0, out_base = 0;
+    for (int base = 0; base < T; base += blockDim.x) {
+        const int t = base + threadIdx.x;
+        const unsigned u = (t < T) ? col[t] : 0u;
+        const bool gt = (t < T) && u > K;
+        const bool eq = (t < T) && u == K;
+        int eq_tot, sel_tot;
+        const int eq_rank = eq_base + block_exclusive_scan_flag(eq, warp_tot, eq_tot);
+        const bool sel = gt || (eq && eq_rank < remaining);
+        const int pos = out_base + block_exclusive_scan_flag(sel, warp_tot, sel_tot);
+        if (sel && pos < cap) {
+            ec_tok[(size_t)e * cap + pos] = t;
+            ec_w[(size_t)e * cap + pos] = __uint_as_float(u);
+        }
+        eq_base += eq_tot;
+        out_base += sel_tot;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
+                              const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t,
+                              unsigned *err, cudaStream_t s) {
+    (void)err;
+    RouteArgs a;
+    a.x = x;
+    a.Wr = W_r;
+    a.logit_offset = logit_offset;
+    a.sel_bias = sel_bias;
+    a.T = c.T;
+    a.d = c.d;
+    a.E = c.E;
+    a.k = c.k;
+    a.gate = c.gate;
+    a.mode = c.mode;
+    a.renorm = c.renormalize;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.scores_t = scores_t;
+    if (c.dtype == MOE_F32) return launch_typed<float>(a, s);
+    return launch_typed<__nv_bfloat16>(a, s);
+}
+
+cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
+                             cudaStream_t s) {
+    ec_select_kernel<<<c.E, kEcThreads, 0, s>>>(scores_t, c.T, c.ec_capacity, ec_tok, ec_w);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -62,6 +62,8 @@ def _load():
                                               ppf, ppf, ppf, c_int, c_int, ppf, ppf, ppf, f64p, c_int]
             lib.oracle_forward_ec.argtypes = [c_int, c_int, c_int, c_int, c_int, i32p, f32p, i32p, f64p,
                                               ppf, ppf, ppf, c_int, c_int, ppf, ppf, ppf, f64p, c_int]
+            lib.oracle_expert_rows.restype = None
+            lib.oracle_expert_rows.argtypes = [c_int, c_int, c_int, f32p, f32p, f32p, f32p, f64p, f64p, c_int]
             lib.oracle_max_threads.restype = c_int
             _lib = lib
     return _lib
@@ -177,6 +179,131 @@ def _expert_mats(W, needed):
     return [(_f32(W[e]) if e in needed else None) for e in range(W.shape[0])]
 
 
+def expert_rows(X, W1, W3, W2, scale=None, nthreads=1):
+    """out[r] = scale[r] * (SiLU(X[r] W1) * (X[r] W3)) W2 for every row of X, fp64."""
+    X, W1, W3, W2 = _f32(X), _f32(W1), _f32(W3), _f32(W2)
+    n, d = X.shape
+    f = W1.shape[1]
+    sc = None if scale is None else np.ascontiguousarray(scale, np.float64)
+    out = np.empty((n, d), np.float64)
+    if n:
+        _load().oracle_expert_rows(d, f, n, _ptr(X, ctypes.c_float), _ptr(W1, ctypes.c_float),
+                                   _ptr(W3, ctypes.c_float), _ptr(W2, ctypes.c_float),
+                                   _ptr(sc, ctypes.c_double), _ptr(out, ctypes.c_double), nthreads)
+    return out
+
+
+def combine_tc(Y, slot_of, topk_w, tokens=None, Y_shared=None):
+    """Gate-weighted combine, token choice: y[t] = sum over kept slots j (in slot
+    order) of topk_w[t, j] * Y[slot_of[t, j]], plus Y_shared[t] when given."""
+    Y = np.asarray(Y, np.float64)
+    slot = _i32(slot_of)
+    w = np.asarray(topk_w, np.float64)
+    T, k = slot.shape
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    y = np.zeros((len(tokens), Y.shape[1]), np.float64)
+    for n, t in enumerate(tokens):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                y[n] += w[t, j] * Y[slot[t, j]]
+        if Y_shared is not None:
+            y[n] += np.asarray(Y_shared[t], np.float64)
+    return y
+
+
+def combine_ec(Y, slot_of, ec_w, tokens=None, Y_shared=None):
+    """Gate-weighted combine, Expert Choice: y[t] = sum over experts e (ascending)
+    that took t of ec_w[row] * Y[row], row = slot_of[t, e]; plus Y_shared[t]."""
+    Y = np.asarray(Y, np.float64)
+    slot = _i32(slot_of)
+    w = np.asarray(ec_w, np.float64).reshape(-1)
+    T, E = slot.shape
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens)
+    y = np.zeros((len(tokens), Y.shape[1]), np.float64)
+    for n, t in enumerate(tokens):
+        for e in range(E):
+            r = slot[t, e]
+            if r >= 0:
+                y[n] += w[r] * Y[r]
+        if Y_shared is not None:
+            y[n] += np.asarray(Y_shared[t], np.float64)
+    return y
+
+
+def _shared_sum(x_rows, W1s, W3s, W2s, nthreads):
+    out = None
+    for s in range(W1s.shape[0]):
+        o = expert_rows(x_rows, W1s[s], W3s[s], W2s[s], None, nthreads)
+        out = o if out is None else out + o
+    return out
+
+
+def forward_tc_streamed(x, topk_idx, topk_w, slot_of, W1, W3, W2, tokens, W1s=None, W3s=None, W2s=None,
+                        nthreads=1):
+    """Same result as ``forward_tc``, bit for bit, but visits one expert at a time
+    so only one expert's weights are on the host at once (large layers).
+
+    For token t: y[t] = ((0 + c_0) + c_1) + ... over kept slots in slot order,
+    c_j = topk_w[t, j] * E_{idx[t, j]}(x_t), then + each shared expert in order.
+    """
+    idx, slot = _i32(topk_idx), _i32(slot_of)
+    w = np.ascontiguousarray(topk_w, np.float64)
+    tok = np.asarray(tokens, np.int64)
+    k = idx.shape[1]
+    d = x.shape[1]
+    contrib = {}
+    by_expert = {}
+    for n, t in enumerate(tok):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                by_expert.setdefault(int(idx[t, j]), []).append((n, j))
+    for e, pairs in sorted(by_expert.items()):
+        rows = np.stack([_f32(x[int(tok[n])]) for n, _ in pairs])
+        sc = np.array([w[tok[n], j] for n, j in pairs], np.float64)
+        out = expert_rows(rows, W1[e], W3[e], W2[e], sc, nthreads)
+        for (n, j), o in zip(pairs, out):
+            contrib[(n, j)] = o
+    y = np.zeros((len(tok), d), np.float64)
+    for n in range(len(tok)):
+        for j in range(k):
+            if (n, j) in contrib:
+                y[n] = y[n] + contrib[(n, j)]
+    if W1s is not None and W1s.shape[0] > 0:
+        xs = np.stack([_f32(x[int(t)]) for t in tok])
+        for s in range(W1s.shape[0]):
+            y = y + expert_rows(xs, W1s[s], W3s[s], W2s[s], None, nthreads)
+    return y
+
+
+def forward_ec_streamed(x, ec_tok, ec_w, W1, W3, W2, tokens, W1s=None, W3s=None, W2s=None, nthreads=1):
+    """Same result as ``forward_ec``, bit for bit, one expert at a time."""
+    et = _i32(ec_tok)
+    ew = np.ascontiguousarray(ec_w, np.float64)
+    tok = np.asarray(tokens, np.int64)
+    E, cap = et.shape
+    d = x.shape[1]
+    pos = {int(t): n for n, t in enumerate(tok)}
+    contrib = {}
+    for e in range(E):
+        pairs = [(pos[int(t)], r) for r, t in enumerate(et[e]) if int(t) in pos]
+        if not pairs:
+            continue
+        rows = np.stack([_f32(x[int(tok[n])]) for n, _ in pairs])
+        sc = np.array([ew[e, r] for _, r in pairs], np.float64)
+        out = expert_rows(rows, W1[e], W3[e], W2[e], sc, nthreads)
+        for (n, _), o in zip(pairs, out):
+            contrib.setdefault(n, []).append(o)   # experts visited in ascending order
+    y = np.zeros((len(tok), d), np.float64)
+    for n, parts in contrib.items():
+        for o in parts:
+            y[n] = y[n] + o
+    if W1s is not None and W1s.shape[0] > 0:
+        xs = np.stack([_f32(x[int(t)]) for t in tok])
+        for s in range(W1s.shape[0]):
+            y = y + expert_rows(xs, W1s[s], W3s[s], W2s[s], None, nthreads)
+    return y
+
+
 def forward_tc(x, topk_idx, topk_w, slot_of, W1, W3, W2, tokens, W1s=None, W3s=None, W2s=None,
                nthreads=1):
     """y[len(tokens), d] (f64) for token choice, given routing and dispatch results."""
@@ -243,7 +370,7 @@ def forward(inp: dict, wl, tokens=None, nthreads=1):
         ec_tok, ec_w, gap, S = route_ec(x, inp["W_r"], wl.ec_capacity, inp.get("logit_offset"),
                                         nthreads=nthreads, want_scores=True)
         res.update(ec_tok=ec_tok, ec_w=ec_w, gap=gap, S=S)
-        res["y"] = forward_ec(x, ec_tok, ec_w, inp["W1"], inp["W3"], inp["W2"], tokens,
+        res["y"] = forward_ec_streamed(x, ec_tok, ec_w, inp["W1"], inp["W3"], inp["W2"], tokens,
                               inp.get("W1s"), inp.get("W3s"), inp.get("W2s"), nthreads=nthreads)
         return res
     idx, w, gap, sc = route_tc(x, inp["W_r"], wl.k, wl.gate, inp.get("logit_offset"), inp.get("sel_bias"),
@@ -252,6 +379,6 @@ def forward(inp: dict, wl, tokens=None, nthreads=1):
     off, cnt_raw, slot_of, row_token = dispatch_tc(idx, wl.E, cap)
     res.update(topk_idx=idx, topk_w=w, gap=gap, scores=sc, cap=cap, off=off, cnt_raw=cnt_raw,
                slot_of=slot_of, row_token=row_token)
-    res["y"] = forward_tc(x, idx, w, slot_of, inp["W1"], inp["W3"], inp["W2"], tokens,
+    res["y"] = forward_tc_streamed(x, idx, w, slot_of, inp["W1"], inp["W3"], inp["W2"], tokens,
                           inp.get("W1s"), inp.get("W3s"), inp.get("W2s"), nthreads=nthreads)
     return res

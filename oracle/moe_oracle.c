@@ -284,6 +284,21 @@ void oracle_swiglu_expert(int d, int f, const float *x, const float *W1, const f
 }
 
 /*
+ * One expert applied to n rows: out[r][:] = scale[r] * E(X[r]) (scale NULL = 1).
+ * Same arithmetic as oracle_swiglu_expert, rows spread over threads.
+ */
+void oracle_expert_rows(int d, int f, int n, const float *X, const float *W1, const float *W3,
+                        const float *W2, const double *scale, double *out, int nthreads)
+{
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads > 0 ? nthreads : 1)
+    for (int r = 0; r < n; ++r) {
+        double *o = out + (size_t)r * d;
+        for (int i = 0; i < d; ++i) o[i] = 0.0;
+        oracle_swiglu_expert(d, f, X + (size_t)r * d, W1, W3, W2, scale ? scale[r] : 1.0, o);
+    }
+}
+
+/*
  * Layer output of a list of tokens, token choice ([P2] §3.1 y = sum_i G_i E_i(x),
  * §3.4 and §9.1 shared experts added unweighted):
  *   y[t] = sum_{j : slot_of[t][j] >= 0} topk_w[t][j] * E_{topk_idx[t][j]}(x_t)

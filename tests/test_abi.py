@@ -1,0 +1,119 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point the
+header declares, and its host-side logic (config validation, capacity, buffer
+and workspace sizing, argument checks that run before any CUDA call) behaves."""
+import os
+import re
+
+import pytest
+import torch
+
+from mixture_experts_sparse_gemm_b300 import binding as B
+from mixture_experts_sparse_gemm_b300 import build as build_mod
+from workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_b300.h")
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build_mod.build()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return sorted(set(re.findall(r"^(?:moe_status|const char \*)\s*(moe_\w+)\(", text, flags=re.M)))
+
+
+def test_every_declared_function_is_exported():
+    names = declared_functions()
+    assert len(names) >= 12
+    assert set(names) == set(B.EXPORTS)
+    L = B.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings():
+    for code, name in [(0, "MOE_OK"), (1, "MOE_ERR_INVALID_ARG"), (2, "MOE_ERR_UNSUPPORTED"),
+                       (3, "MOE_ERR_MISALIGNED"), (4, "MOE_ERR_WORKSPACE"), (5, "MOE_ERR_CUDA"),
+                       (6, "MOE_ERR_TIMEOUT")]:
+        assert B.status_string(code) == name
+    assert B.status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_workload_configs_are_valid(name):
+    cfg = B.config_from_workload(WORKLOADS[name])
+    assert B.moe_validate_config(cfg) == B.MOE_OK
+    assert B.moe_workspace_size(cfg) > 0
+    assert B.moe_packed_weights_size(cfg) > 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(k=9, E=16), B.MOE_ERR_UNSUPPORTED),
+    (dict(k=3, E=2), B.MOE_ERR_INVALID_ARG),
+    (dict(k=0), B.MOE_ERR_INVALID_ARG),
+    (dict(E=300, k=2), B.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), B.MOE_ERR_INVALID_ARG),
+    (dict(d=100), B.MOE_ERR_UNSUPPORTED),
+    (dict(f=100), B.MOE_ERR_UNSUPPORTED),
+    (dict(capacity_factor=float("nan")), B.MOE_ERR_INVALID_ARG),
+    (dict(mode="ec", ec_capacity=0), B.MOE_ERR_INVALID_ARG),
+    (dict(mode="ec", ec_capacity=65), B.MOE_ERR_INVALID_ARG),
+    (dict(mode="ec", ec_capacity=8, gate="sigmoid"), B.MOE_ERR_UNSUPPORTED),
+    (dict(n_shared=1, f_shared=0), B.MOE_ERR_INVALID_ARG),
+    (dict(n_shared=1, f_shared=96), B.MOE_ERR_UNSUPPORTED),
+])
+def test_config_rejections(kw, want):
+    base = dict(T=64, d=256, E=8, f=128, k=2)
+    base.update(kw)
+    cfg = B.config(**base)
+    assert B.moe_validate_config(cfg) == want
+
+
+def test_capacity_follows_printed_examples():
+    with open(os.path.join(GOLDEN, "capacity.txt"), encoding="utf-8") as fh:
+        rows = [ln.split('"')[0].split() for ln in fh if ln.strip() and not ln.startswith("#")]
+    for C, T, k, E, want in rows:
+        cfg = B.config(T=int(T), d=128, E=int(E), f=64, k=int(k), capacity_factor=float(C))
+        assert B.moe_expert_capacity(cfg) == int(want)
+    assert B.moe_expert_capacity(B.config(T=100, d=128, E=8, f=64, k=2)) == -1
+    assert B.moe_expert_capacity(B.config(T=100, d=128, E=8, f=64, mode="ec", ec_capacity=17)) == 17
+
+
+def test_buffer_rows():
+    assert B.moe_buffer_rows(B.config(T=100, d=128, E=8, f=64, k=2)) == (200, 200)
+    assert B.moe_buffer_rows(B.config(T=100, d=128, E=8, f=64, k=2, n_shared=1, f_shared=64)) == (200, 300)
+    assert B.moe_buffer_rows(B.config(T=100, d=128, E=8, f=64, mode="ec", ec_capacity=25)) == (200, 200)
+
+
+def test_argument_checks_run_before_any_cuda_call():
+    cfg = B.config(T=64, d=256, E=8, f=128, k=2)
+    L = B.lib()
+    import ctypes
+    c = ctypes.byref(cfg)
+    A = 0x10000          # aligned fake device addresses: never dereferenced, the checks fail first
+    ws_need = B.moe_workspace_size(cfg, B.MOE_STAGE_DISPATCH)
+    assert L.moe_route(c, None, A, None, None, A, A, A, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route(c, A + 8, A, None, None, A, A, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_route(c, A, A, None, None, A + 2, A, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_dispatch(c, A, A, A, A, A, A, A, ws_need - 1, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_dispatch(c, A, A, A, A, A, A, A + 64, ws_need, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_combine(c, A, A, None, A, None, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_forward(c, A, A, None, None, A + 128, A, A, 1 << 40, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_forward(None, A, A, None, None, A, A, A, 1 << 40, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_grouped_ffn(c, A, A, A, None, A, A, 0, None) == B.MOE_ERR_WORKSPACE
+    ec = B.config(T=64, d=256, E=8, f=128, mode="ec", ec_capacity=8)
+    assert L.moe_route(ctypes.byref(ec), A, A, None, A, A, A, A, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_weights(c, A, A, A, None, None, None, A, 10, None) == B.MOE_ERR_WORKSPACE
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_valid_call_without_gpu_reports_cuda_error():
+    cfg = B.config(T=64, d=256, E=8, f=128, k=2)
+    import ctypes
+    A = 0x10000
+    st = B.lib().moe_combine(ctypes.byref(cfg), A, A, A, A, None, 0, None)
+    assert st == B.MOE_ERR_CUDA

@@ -1,0 +1,376 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bars:
+  * integer outputs (routing indices, offsets, slot table, drop mask, row
+    gather) bit-exact; tokens whose oracle gap between the k-th and (k+1)-th key
+    is below 1e-4 are reported and left out of the index comparison;
+  * bf16 outputs: max |err| <= 2e-2 * max |y_ref|; fp32: <= 1e-4 * max |y_ref|;
+  * gate weights (fp32 on the GPU, fp64 in the oracle): |err| <= 2e-5.
+Stage tests feed both sides the same seeded integer/float inputs; end-to-end
+tests compare the routing and the layer output (sampled tokens at full size).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_sparse_gemm_b300 import binding as B
+from mixture_experts_sparse_gemm_b300 import build as build_mod
+from mixture_experts_sparse_gemm_b300.layer import MoELayer
+from workloads import WORKLOADS, make_inputs, random_assignment, random_rows, random_weights
+
+pytestmark = pytest.mark.gpu
+
+GAP = 1e-4
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+NTH = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built(cuda_device):
+    build_mod.build()
+    B.lib()
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy() if t.dtype != torch.int32 else t.cpu().numpy()
+
+
+def rel_err(got, ref):
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30))
+
+
+def _layer(wl, inp):
+    cfg = B.config_from_workload(wl)
+    return cfg, MoELayer(cfg, inp["W1"], inp["W3"], inp["W2"], inp.get("W1s"), inp.get("W3s"), inp.get("W2s"))
+
+
+def _check_device_error():
+    torch.cuda.synchronize()
+    B.moe_check_device_error()
+
+
+# ------------------------------------------------------------------------------------------ route
+
+SMALL_TC = {
+    "ragged_top2": WORKLOADS["mixtral_T256"].with_(T=333, d=256, f=128, name="ragged_top2"),
+    "sigmoid_top8_e256": WORKLOADS["deepseek_v3"].with_(T=200, d=384, f=128, f_shared=128, name="sig8"),
+    "top1_cap": WORKLOADS["switch_top1_cap1.25"].with_(T=1000, d=256, f=128, E=16, name="top1cap"),
+    "t1": WORKLOADS["mixtral_T16"].with_(T=1, d=128, f=64, name="t1"),
+}
+ROUTE_CASES = ["tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T4096", "deepseek_v3"] + list(SMALL_TC)
+
+
+def _wl(name):
+    return WORKLOADS[name] if name in WORKLOADS else SMALL_TC[name]
+
+
+@pytest.mark.parametrize("name", ROUTE_CASES)
+def test_route_token_choice(name, cuda_device):
+    wl = _wl(name)
+    inp = make_inputs(wl, cuda_device, weights=False)
+    cfg = B.config_from_workload(wl)
+    ws = torch.empty(max(1, B.moe_workspace_size(cfg, B.MOE_STAGE_ROUTE)), dtype=torch.uint8, device=cuda_device)
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device=cuda_device)
+    w = torch.empty(wl.T, wl.k, dtype=torch.float32, device=cuda_device)
+    B.moe_route(cfg, inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"], idx, w, ws)
+    _check_device_error()
+    oi, ow, gap = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                  wl.renorm, nthreads=NTH)
+    keep = gap >= GAP
+    gi, gw = _np(idx), _np(w)
+    print(f"{name}: {int((~keep).sum())} of {wl.T} tokens within {GAP} of a tie, excluded")
+    assert (~keep).mean() < 0.02
+    np.testing.assert_array_equal(gi[keep], oi[keep])
+    assert np.abs(gw[keep] - ow[keep]).max() <= 2e-5
+
+
+EC_CASES = {
+    "expert_choice_zipf": WORKLOADS["expert_choice_zipf"],
+    "ec_small": WORKLOADS["expert_choice_zipf"].with_(T=1000, d=256, E=16, f=128, ec_capacity=100, name="ec_small"),
+    "ec_cap_eq_T": WORKLOADS["expert_choice_zipf"].with_(T=77, d=128, E=4, f=64, ec_capacity=77, name="ec_full"),
+}
+
+
+def _check_ec_selection(gt, gw, ot, S, cap, tau=1e-6):
+    """Exactly cap ascending tokens per expert; every token clearly above the
+    oracle boundary taken, every token clearly below it not taken."""
+    E = gt.shape[0]
+    ambiguous = set()
+    for e in range(E):
+        assert (np.diff(gt[e]) > 0).all() and len(gt[e]) == cap
+        col = S[:, e]
+        srt = np.sort(col)[::-1]
+        hi_b = srt[cap - 1]
+        lo_b = srt[cap] if cap < len(col) else -np.inf
+        taken = np.zeros(len(col), bool)
+        taken[gt[e]] = True
+        assert taken[col > hi_b + tau].all()
+        assert not taken[col < lo_b - tau].any()
+        if hi_b - lo_b >= 2 * tau:
+            np.testing.assert_array_equal(gt[e], ot[e])
+        else:
+            ambiguous.update(np.nonzero(np.abs(col - hi_b) <= 2 * tau)[0].tolist())
+        np.testing.assert_allclose(gw[e], col[gt[e]], atol=2e-6, rtol=0)
+    return ambiguous
+
+
+@pytest.mark.parametrize("name", list(EC_CASES))
+def test_route_expert_choice(name, cuda_device):
+    wl = EC_CASES[name]
+    inp = make_inputs(wl, cuda_device, weights=False)
+    cfg = B.config_from_workload(wl)
+    ws = torch.empty(B.moe_workspace_size(cfg, B.MOE_STAGE_ROUTE), dtype=torch.uint8, device=cuda_device)
+    tok = torch.empty(wl.E, wl.ec_capacity, dtype=torch.int32, device=cuda_device)
+    w = torch.empty(wl.E, wl.ec_capacity, dtype=torch.float32, device=cuda_device)
+    B.moe_route(cfg, inp["x"], inp["W_r"], inp["logit_offset"], None, tok, w, ws)
+    _check_device_error()
+    ot, ow, gap, S = oracle.route_ec(inp["x"], inp["W_r"], wl.ec_capacity, inp["logit_offset"], nthreads=NTH,
+                                     want_scores=True)
+    amb = _check_ec_selection(_np(tok), _np(w), ot, S, wl.ec_capacity)
+    print(f"{name}: {len(amb)} tokens at a near-tie expert boundary")
+
+
+# ------------------------------------------------------------------------------------------ dispatch
+
+DISPATCH_CASES = [
+    # T, E, k, capacity factor, skew, d, dtype
+    (8192, 64, 1, 1.25, 1.0, 1024, "bf16"),
+    (8192, 64, 1, 1.25, 0.0, 1024, "bf16"),
+    (4096, 256, 8, 0.0, 0.5, 256, "bf16"),
+    (1000, 8, 2, 1.0, 1.5, 128, "bf16"),
+    (257, 16, 3, 0.3, 2.0, 256, "bf16"),
+    (1, 4, 2, 0.0, 0.0, 128, "bf16"),
+    (300, 8, 2, 0.01, 0.0, 128, "bf16"),     # capacity 0: every assignment dropped
+    (500, 8, 2, 1.25, 1.0, 64, "f32"),
+]
+
+
+@pytest.mark.parametrize("T,E,k,C,skew,d,dt", DISPATCH_CASES)
+def test_dispatch_token_choice(T, E, k, C, skew, d, dt, cuda_device):
+    cfg = B.config(T=T, d=d, E=E, f=64, k=k, capacity_factor=C, dtype=dt)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    idx = random_assignment(T, E, k, seed=T + E + k, skew=skew, device=cuda_device)
+    x = random_rows(T, d, seed=T, dtype=tdt, device=cuda_device)
+    ws = torch.empty(B.moe_workspace_size(cfg, B.MOE_STAGE_DISPATCH), dtype=torch.uint8, device=cuda_device)
+    off = torch.empty(E + 1, dtype=torch.int32, device=cuda_device)
+    cnt = torch.empty(E, dtype=torch.int32, device=cuda_device)
+    slot = torch.empty(T, k, dtype=torch.int32, device=cuda_device)
+    x_perm = torch.empty(T * k, d, dtype=tdt, device=cuda_device)
+    B.moe_dispatch(cfg, idx, x, off, cnt, slot, x_perm, ws)
+    _check_device_error()
+    cap = oracle.capacity(C, T, k, E)
+    assert cap == B.moe_expert_capacity(cfg)
+    o_off, o_cnt, o_slot, o_rows = oracle.dispatch_tc(idx, E, cap)
+    np.testing.assert_array_equal(_np(off), o_off)
+    np.testing.assert_array_equal(_np(cnt), o_cnt)
+    np.testing.assert_array_equal(_np(slot), o_slot)
+    A = int(o_off[-1])
+    assert torch.equal(x_perm[:A], x[torch.from_numpy(o_rows).long().to(cuda_device)])
+
+
+def test_dispatch_expert_choice(cuda_device):
+    wl = EC_CASES["ec_small"]
+    inp = make_inputs(wl, "cpu", weights=False)
+    ot, ow, gap = oracle.route_ec(inp["x"], inp["W_r"], wl.ec_capacity, inp["logit_offset"], nthreads=NTH)
+    cfg = B.config_from_workload(wl)
+    x = inp["x"].to(cuda_device)
+    tok = torch.from_numpy(ot).to(cuda_device)
+    off = torch.empty(wl.E + 1, dtype=torch.int32, device=cuda_device)
+    cnt = torch.empty(wl.E, dtype=torch.int32, device=cuda_device)
+    slot = torch.empty(wl.T, wl.E, dtype=torch.int32, device=cuda_device)
+    x_perm = torch.empty(wl.E * wl.ec_capacity, wl.d, dtype=torch.bfloat16, device=cuda_device)
+    B.moe_dispatch(cfg, tok, x, off, cnt, slot, x_perm, None)
+    _check_device_error()
+    cap = wl.ec_capacity
+    np.testing.assert_array_equal(_np(off), np.arange(wl.E + 1) * cap)
+    np.testing.assert_array_equal(_np(cnt), np.full(wl.E, cap))
+    want = -np.ones((wl.T, wl.E), np.int32)
+    for e in range(wl.E):
+        want[ot[e], e] = e * cap + np.arange(cap)
+    np.testing.assert_array_equal(_np(slot), want)
+    assert torch.equal(x_perm, x[tok.reshape(-1).long()])
+
+
+# ------------------------------------------------------------------------------------------ experts
+
+FFN_CASES = [
+    # T, d, E, f, k, skew, n_shared, f_shared, dtype
+    (700, 256, 8, 384, 2, 1.2, 0, 0, "bf16"),      # f % 128 != 0: 128-wide up tiles; empty experts
+    (300, 384, 4, 256, 2, 0.0, 2, 128, "bf16"),    # d % 256 != 0: 128-wide down tiles; shared experts
+    (1024, 1024, 8, 512, 1, 0.0, 0, 0, "bf16"),    # several full 128-row tiles per expert
+    (129, 128, 3, 64, 1, 0.0, 1, 64, "bf16"),
+    (200, 128, 8, 256, 2, 1.0, 1, 64, "f32"),      # CUDA-core fp32 path
+]
+
+
+@pytest.mark.parametrize("T,d,E,f,k,skew,ns,fs,dt", FFN_CASES)
+def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
+    cfg = B.config(T=T, d=d, E=E, f=f, k=k, n_shared=ns, f_shared=fs, dtype=dt)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    g = torch.Generator(device="cpu").manual_seed(T * 7 + d)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).to(tdt)
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).to(tdt)
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).to(tdt)
+    Ws = None
+    if ns:
+        Ws = [(torch.randn(ns, d, fs, generator=g) / d ** 0.5).to(tdt),
+              (torch.randn(ns, d, fs, generator=g) / d ** 0.5).to(tdt),
+              (torch.randn(ns, fs, d, generator=g) / fs ** 0.5).to(tdt)]
+    x = random_rows(T, d, seed=d + T, dtype=tdt)
+    idx = random_assignment(T, E, k, seed=5 + T, skew=skew)
+    o_off, _, o_slot, o_rows = oracle.dispatch_tc(idx, E, -1)
+    x_perm = torch.zeros(T * k, d, dtype=tdt)
+    x_perm[: len(o_rows)] = x[torch.from_numpy(o_rows).long()]
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws) if Ws else (None,) * 3)
+    Y = layer.grouped_ffn(x_perm.to(dev), torch.from_numpy(o_off).to(dev), x.to(dev))
+    _check_device_error()
+    Yn = _np(Y)
+    ref = np.zeros((T * k + (T if ns else 0), d))
+    for e in range(E):
+        a, b = int(o_off[e]), int(o_off[e + 1])
+        if b > a:
+            ref[a:b] = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
+    A = int(o_off[-1])
+    assert rel_err(Yn[:A], ref[:A]) <= TOL[dt]
+    if ns:
+        sref = sum(oracle.expert_rows(x, Ws[0][s], Ws[1][s], Ws[2][s], nthreads=NTH) for s in range(ns))
+        assert rel_err(Yn[T * k:], sref) <= TOL[dt]
+
+
+# ------------------------------------------------------------------------------------------ combine
+
+@pytest.mark.parametrize("T,E,k,C,d,ns,dt", [(1000, 8, 2, 1.0, 256, 0, "bf16"), (4096, 256, 8, 0.0, 7168, 1, "bf16"),
+                                             (333, 16, 1, 1.25, 128, 1, "f32")])
+def test_combine_token_choice(T, E, k, C, d, ns, dt, cuda_device):
+    cfg = B.config(T=T, d=d, E=E, f=64, k=k, capacity_factor=C, n_shared=ns, f_shared=64 if ns else 0, dtype=dt)
+    tdt = torch.float32 if dt == "f32" else torch.bfloat16
+    idx = random_assignment(T, E, k, seed=3 * T, skew=1.0)
+    cap = oracle.capacity(C, T, k, E)
+    _, _, o_slot, _ = oracle.dispatch_tc(idx, E, cap)
+    rows_total = T * k + (T if ns else 0)
+    Y = random_rows(rows_total, d, seed=T + 1, dtype=tdt)
+    w = random_weights((T, k), seed=T)
+    layer_y = torch.empty(T, d, dtype=tdt, device=cuda_device)
+    B.moe_combine(cfg, Y.to(cuda_device), torch.from_numpy(o_slot).to(cuda_device), w.to(cuda_device), layer_y)
+    _check_device_error()
+    Yf = Y.float().numpy()
+    ref = oracle.combine_tc(Yf, o_slot, w.numpy(), Y_shared=Yf[T * k:] if ns else None)
+    assert rel_err(_np(layer_y), ref) <= TOL[dt] / 4
+
+
+def test_combine_expert_choice(cuda_device):
+    T, E, cap, d = 1000, 16, 100, 256
+    cfg = B.config(T=T, d=d, E=E, f=64, mode="ec", ec_capacity=cap)
+    wl = EC_CASES["ec_small"]
+    inp = make_inputs(wl, "cpu", weights=False)
+    ot, ow, _ = oracle.route_ec(inp["x"], inp["W_r"], cap, inp["logit_offset"], nthreads=NTH)
+    slot = -np.ones((T, E), np.int32)
+    for e in range(E):
+        slot[ot[e], e] = e * cap + np.arange(cap)
+    Y = random_rows(E * cap, d, seed=17)
+    w = torch.from_numpy(ow.astype(np.float32))
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=cuda_device)
+    B.moe_combine(cfg, Y.to(cuda_device), torch.from_numpy(slot).to(cuda_device), w.to(cuda_device), y)
+    _check_device_error()
+    ref = oracle.combine_ec(Y.float().numpy(), slot, w.numpy())
+    assert rel_err(_np(y), ref) <= TOL["bf16"] / 4
+
+
+# ------------------------------------------------------------------------------------------ whole layer
+
+def _sample_tokens(T, n, seed, must=()):
+    rng = np.random.default_rng(seed)
+    pick = set(rng.choice(T, size=min(n, T), replace=False).tolist()) | set(int(t) for t in must)
+    return np.array(sorted(pick), np.int64)
+
+
+E2E_CASES = {
+    "tiny_top2_fp32": (None, 0),
+    "switch_top1_cap1.25": (48, 0),
+    "mixtral_T16": (None, 0),
+    "mixtral_T256": (24, 0),
+    "mixtral_T4096": (16, 0),
+    "mixtral_T16384": (12, 0),
+    "deepseek_v3": (6, 0),
+    "expert_choice_zipf": (16, 0),
+}
+E2E_SMALL = {
+    "small_top2_ragged": WORKLOADS["mixtral_T256"].with_(T=333, d=256, f=384, name="small_top2_ragged"),
+    "small_sigmoid_shared": WORKLOADS["deepseek_v3"].with_(T=150, d=256, E=32, f=128, f_shared=192,
+                                                            name="small_sigmoid_shared"),
+    "small_switch_drops": WORKLOADS["switch_top1_cap1.25"].with_(T=600, d=256, E=8, f=256, capacity_factor=0.8,
+                                                                  logit_offsets="normal_var0.5",
+                                                                  name="small_switch_drops"),
+    "small_ec": EC_CASES["ec_small"],
+    "small_fp32_shared": WORKLOADS["tiny_top2_fp32"].with_(T=100, n_shared=2, f_shared=64, name="small_fp32_sh"),
+}
+
+
+def _run_e2e(wl, n_sample, cuda_device):
+    inp = make_inputs(wl, cuda_device)
+    cfg, layer = _layer(wl, inp)
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    r_idx, r_w = layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    _check_device_error()
+    T = wl.T
+    if wl.mode == "ec":
+        ot, ow, gap, S = oracle.route_ec(inp["x"], inp["W_r"], wl.ec_capacity, inp["logit_offset"], nthreads=NTH,
+                                         want_scores=True)
+        amb = _check_ec_selection(_np(r_idx), _np(r_w), ot, S, wl.ec_capacity)
+        counts = np.bincount(ot.reshape(-1), minlength=T)
+        must = [int(np.argmax(counts))] + np.nonzero(counts == 0)[0][:4].tolist()
+        toks = np.arange(T) if n_sample is None else _sample_tokens(T, n_sample, T, must)
+        toks = np.array([t for t in toks if t not in amb], np.int64)
+        ref = oracle.forward_ec_streamed(inp["x"], ot, ow, inp["W1"], inp["W3"], inp["W2"], toks, inp.get("W1s"),
+                                         inp.get("W3s"), inp.get("W2s"), nthreads=NTH)
+    else:
+        oi, ow, gap = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                      wl.renorm, nthreads=NTH)
+        gi = _np(r_idx)
+        near = gap < GAP
+        np.testing.assert_array_equal(gi[~near], oi[~near])
+        cap = oracle.capacity(wl.capacity_factor, T, wl.k, wl.E)
+        o_off, o_cnt, o_slot, _ = oracle.dispatch_tc(oi, wl.E, cap)
+        g_off, g_cnt, g_slot, _ = oracle.dispatch_tc(gi, wl.E, cap)   # the GPU's own choices, dispatched
+        same = (gi == oi).all(axis=1) & ((g_slot >= 0) == (o_slot >= 0)).all(axis=1)
+        dropped = np.nonzero((o_slot < 0).any(axis=1))[0]
+        toks = np.arange(T) if n_sample is None else _sample_tokens(T, n_sample, T, dropped[:64])
+        toks = np.array([t for t in toks if same[t]], np.int64)
+        print(f"{wl.name}: {int(near.sum())} near-tie tokens, {len(dropped)} tokens with a dropped slot")
+        ref = oracle.forward_tc_streamed(inp["x"], oi, ow, o_slot, inp["W1"], inp["W3"], inp["W2"], toks,
+                                         inp.get("W1s"), inp.get("W3s"), inp.get("W2s"), nthreads=NTH)
+    got = _np(y)[toks]
+    err = rel_err(got, ref)
+    print(f"{wl.name}: {len(toks)} tokens compared, max|err|/max|ref| = {err:.3e}")
+    assert err <= TOL[wl.dtype]
+    return err
+
+
+@pytest.mark.parametrize("name", list(E2E_CASES))
+def test_forward_full_size(name, cuda_device):
+    n, _ = E2E_CASES[name]
+    _run_e2e(WORKLOADS[name], n, cuda_device)
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", list(E2E_SMALL))
+def test_forward_small_all_tokens(name, cuda_device):
+    _run_e2e(E2E_SMALL[name], None, cuda_device)
+
+
+def test_forward_empty_batch(cuda_device):
+    wl = WORKLOADS["mixtral_T16"].with_(T=0, d=128, f=64)
+    cfg = B.config_from_workload(wl)
+    dev = cuda_device
+    E, d, f = wl.E, wl.d, wl.f
+    W = torch.zeros(E, d, f, dtype=torch.bfloat16, device=dev)
+    layer = MoELayer(cfg, W, W, torch.zeros(E, f, d, dtype=torch.bfloat16, device=dev))
+    x = torch.zeros(1, d, dtype=torch.bfloat16, device=dev)
+    y = torch.zeros(1, d, dtype=torch.bfloat16, device=dev)
+    B.moe_forward(cfg, x, torch.zeros(d, E, dtype=torch.bfloat16, device=dev), None, None, layer.packed, y,
+                  layer.workspace())
+    _check_device_error()

@@ -371,3 +371,67 @@ def test_threads_do_not_change_results():
     b = oracle.route_tc(x, Wr, 4, "sigmoid", nthreads=4)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u, v)
+
+
+# --------------------------------------------------------------------------- streamed forms and combine
+
+def test_streamed_forward_is_bitwise_equal_to_direct():
+    T, d, E, f = 40, 16, 6, 24
+    x, Wr, W1, W3, W2 = _layer_inputs(T, d, E, f, seed=40)
+    r = _rng(41)
+    W1s = r.standard_normal((2, d, 8)).astype(np.float32)
+    W3s = r.standard_normal((2, d, 8)).astype(np.float32)
+    W2s = r.standard_normal((2, 8, d)).astype(np.float32)
+    idx, w, _ = oracle.route_tc(x, Wr, 3, "sigmoid", renorm=True)
+    off, cnt, slot, rows = oracle.dispatch_tc(idx, E, 15)
+    toks = np.array([0, 5, 7, 39, 12], np.int32)
+    a = oracle.forward_tc(x, idx, w, slot, W1, W3, W2, toks, W1s, W3s, W2s, nthreads=3)
+    b = oracle.forward_tc_streamed(x, idx, w, slot, W1, W3, W2, toks, W1s, W3s, W2s, nthreads=2)
+    np.testing.assert_array_equal(a, b)
+    tok, ew, gap = oracle.route_ec(x, Wr, 9)
+    a = oracle.forward_ec(x, tok, ew, W1, W3, W2, toks, W1s, W3s, W2s)
+    b = oracle.forward_ec_streamed(x, tok, ew, W1, W3, W2, toks, W1s, W3s, W2s, nthreads=4)
+    np.testing.assert_array_equal(a, b)
+
+
+def test_combine_definitions():
+    T, k, d, E = 6, 2, 5, 4
+    r = _rng(50)
+    Y = r.standard_normal((T * k + T, d))
+    slot = np.array([[0, 1], [2, -1], [3, 4], [-1, -1], [5, 6], [7, 8]], np.int32)
+    w = np.zeros((T, k))
+    w[0, 0] = 1.0                                          # one-hot weight picks a row
+    y = oracle.combine_tc(Y, slot, w)
+    np.testing.assert_array_equal(y[0], Y[0])
+    assert not y[1:].any()
+    w = r.random((T, k))
+    ys = oracle.combine_tc(Y, slot, w, Y_shared=Y[T * k:])
+    np.testing.assert_allclose(ys[3], Y[T * k + 3])        # all slots dropped: shared part only
+    np.testing.assert_allclose(ys[1], w[1, 0] * Y[2] + Y[T * k + 1])
+    y2 = oracle.combine_tc(2 * Y, slot, w)
+    np.testing.assert_allclose(y2, 2 * oracle.combine_tc(Y, slot, w))   # linear in Y
+    # expert choice: slot_of[t, e] = row, weight of a row = ec_w flat at that row
+    cap = 2
+    ec_tok = np.array([[0, 3], [1, 3], [2, 5], [0, 4]], np.int32)
+    ec_w = r.random((E, cap))
+    slot_ec = -np.ones((T, E), np.int32)
+    for e in range(E):
+        for rr, t in enumerate(ec_tok[e]):
+            slot_ec[t, e] = e * cap + rr
+    yec = oracle.combine_ec(Y, slot_ec, ec_w)
+    np.testing.assert_allclose(yec[3], ec_w[0, 1] * Y[1] + ec_w[1, 1] * Y[3])
+    np.testing.assert_allclose(yec[0], ec_w[0, 0] * Y[0] + ec_w[3, 0] * Y[6])
+
+
+def test_forward_equals_combine_of_expert_rows():
+    # the layer is the combine of per-row expert outputs: forward == combine(E(x_perm))
+    T, d, E, f, k = 30, 16, 5, 20, 2
+    x, Wr, W1, W3, W2 = _layer_inputs(T, d, E, f, seed=60)
+    idx, w, _ = oracle.route_tc(x, Wr, k, "softmax", renorm=True)
+    off, cnt, slot, row_token = oracle.dispatch_tc(idx, E, 10)
+    Y = np.zeros((T * k, d))
+    for e in range(E):
+        rows = row_token[off[e]:off[e + 1]]
+        Y[off[e]:off[e + 1]] = oracle.expert_rows(x[rows], W1[e], W3[e], W2[e])
+    np.testing.assert_allclose(oracle.combine_tc(Y, slot, w), oracle.forward_tc(x, idx, w, slot, W1, W3, W2, np.arange(T)),
+                               rtol=1e-12, atol=1e-13)
