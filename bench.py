@@ -1,0 +1,505 @@
+#!/usr/bin/env python3
+"""MoE-layer forward benchmark on B300.
+
+One step = one pass of the whole layer (route -> capacity dispatch -> grouped
+SwiGLU experts (up, down) -> combine) over one batch of synthetic tokens, every
+stage called through the C ABI on one CUDA stream, with CUDA events between the
+stages.  Default workload: Switch-style top-1 with capacity factor 1.25, bf16,
+T=8192, d=1024, E=64, d_ff=4096 (its 1.61 GB of expert weights stream through
+HBM every step, so the per-step working set is larger than the 126 MB L2).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
+    python bench.py --impl reference ...     # the CPU oracle on the same workload
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun), every rank runs its own
+replica on its own batch (no data exchange; the layer is replicated, tokens are
+independent), timing is the max over ranks, value = all ranks' tokens / time.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s as % of B300 bf16 peak"
+DEFAULT_WORKLOAD = "switch_top1_cap1.25"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+STAGES = ("route", "dispatch", "ffn_up", "ffn_down", "combine")
+KERNEL_SOURCES = {   # files whose content defines each stage's kernels (for the ncu traffic record)
+    "ffn_up": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
+    "ffn_down": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
+    "route": ["csrc/route.cu", "csrc/route_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
+    "dispatch": ["csrc/dispatch.cu"],
+    "combine": ["csrc/combine.cu"],
+}
+
+
+# ------------------------------------------------------------------------------------ helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash(stage):
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[stage]:
+        with open(os.path.join(ROOT, "mixture_experts_sparse_gemm_b300", rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(stage, workload):
+    """DRAM bytes per launch from the committed ncu record, if the kernel source
+    still matches the one that was profiled; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = kernel_hash(stage)
+    with open(path) as fh:
+        for line in fh:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == stage and parts[1] == workload:
+                if parts[3] == want:
+                    return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.t0 = time.time()
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self, bus_id, t_lo, t_hi):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        rows, window = [], []
+        with open(self.f.name) as fh:
+            for line in fh:
+                c = [x.strip() for x in line.split(",")]
+                if len(c) < 11:
+                    continue
+                if bus_id and bus_id.lower() not in c[2].lower():
+                    continue
+                rows.append(c)
+                try:
+                    ts = datetime.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if t_lo - 0.25 <= ts <= t_hi + 0.25:
+                    window.append(c)
+        os.unlink(self.f.name)
+        rows = window if window else rows   # samples inside the timed region when there are any
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        mx = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[7 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------------ work model
+def work_model(wl, off, E_used):
+    """Algorithmic bytes and FLOPs per stage launch (bf16 b = 2 or fp32 b = 4).
+    A = assignments computed; touched = experts with at least one row."""
+    b = 4 if wl.dtype == "f32" else 2
+    T, d, E, f = wl.T, wl.d, wl.E, wl.f
+    A = int(off[-1])
+    touched = int(E_used)
+    kslots = wl.k if wl.mode == "tc" else E
+    fs = wl.n_shared * wl.f_shared
+    Ts = T if wl.n_shared else 0
+    m = {}
+    m["route"] = {"bytes": T * d * b + d * E * b + (T * wl.k * 8 if wl.mode == "tc" else 3 * T * E * 4 + E * wl.ec_capacity * 8),
+                  "flops": 2 * T * d * E}
+    m["dispatch"] = {"bytes": (T * wl.k * 4 * 3 if wl.mode == "tc" else E * wl.ec_capacity * 4 + T * E * 4) + 2 * A * d * b,
+                     "flops": 0}
+    m["ffn_up"] = {"bytes": touched * 2 * d * f * b + A * d * b + A * f * b + (2 * d * fs * b + Ts * d * b + Ts * fs * b),
+                   "flops": 4 * A * d * f + 4 * Ts * d * fs}
+    m["ffn_down"] = {"bytes": touched * d * f * b + A * f * b + A * d * b + (d * fs * b + Ts * fs * b + Ts * d * b),
+                     "flops": 2 * A * d * f + 2 * Ts * d * fs}
+    m["combine"] = {"bytes": A * d * b + T * kslots * 8 + T * d * b + Ts * d * b, "flops": 2 * A * d}
+    return m, A, touched
+
+
+# ------------------------------------------------------------------------------------ our arm
+def run_gpu(args):
+    from mixture_experts_sparse_gemm_b300 import binding as B
+    from mixture_experts_sparse_gemm_b300 import build as build_mod
+    from mixture_experts_sparse_gemm_b300.layer import MoELayer
+
+    ws_n, rank, local = dist_env()
+    if ws_n > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        build_mod.build()
+    if ws_n > 1:
+        dist.barrier()
+    B.lib()
+
+    wl = WORKLOADS[args.workload]
+    if args.T:
+        wl = wl.with_(T=args.T)
+    if ws_n > 1:   # each replica gets its own batch of tokens
+        wl = wl.with_(index=wl.index + 1000 * rank) if rank else wl
+    inp = make_inputs(wl, dev)
+    cfg = B.config_from_workload(wl)
+    layer = MoELayer(cfg, inp["W1"], inp["W3"], inp["W2"], inp.get("W1s"), inp.get("W3s"), inp.get("W2s"))
+    stream = torch.cuda.current_stream()
+    T, d = wl.T, wl.d
+    dt = layer.dtype
+    rows_routed, rows_total = layer.rows_routed, layer.rows_total
+    ec = wl.mode == "ec"
+    sel = (wl.E, wl.ec_capacity) if ec else (T, wl.k)
+    slots = (T, wl.E) if ec else (T, wl.k)
+    idx = torch.empty(sel, dtype=torch.int32, device=dev)
+    gw = torch.empty(sel, dtype=torch.float32, device=dev)
+    off = torch.empty(wl.E + 1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
+    slot_of = torch.empty(slots, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(rows_routed, d, dtype=dt, device=dev)
+    H = torch.empty(rows_routed, wl.f, dtype=dt, device=dev)
+    fs = wl.n_shared * wl.f_shared
+    Hs = torch.empty(T, fs, dtype=dt, device=dev) if fs else None
+    Y = torch.empty(rows_total, d, dtype=dt, device=dev)
+    y = torch.empty(T, d, dtype=dt, device=dev)
+    ws_route = layer.workspace(B.MOE_STAGE_ROUTE)
+    ws_disp = layer.workspace(B.MOE_STAGE_DISPATCH)
+    x, Wr, lo, sb = inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        B.moe_grouped_ffn_up(cfg, x_perm, off, layer.packed, x, H, Hs, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        B.moe_grouped_ffn_down(cfg, H, Hs, off, layer.packed, Y, stream)
+        if ev is not None:
+            ev[4].record(stream)
+        B.moe_combine(cfg, Y, slot_of, gw, y, None, stream)
+        if ev is not None:
+            ev[5].record(stream)
+
+    def barrier():
+        if ws_n > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if ws_n == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- device-resident timed region
+    clocks = ClockSampler()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    B.moe_check_device_error(stream)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    t_lo = time.time()
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_hi = time.time()
+    barrier()
+    total_ms = evs[0][0].elapsed_time(evs[K - 1][5])
+    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)])) for j, s in enumerate(STAGES)}
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+        bus = f"{bus:02x}:" if isinstance(bus, int) else None
+    except Exception:
+        bus = None
+    clk = clocks.stop(bus, t_lo, t_hi)
+    B.moe_check_device_error(stream)
+    total_ms = max_over_ranks(total_ms)
+
+    # ---- moe_forward (single entry point), device resident: cross-check
+    fw_ws = layer.workspace()
+    for _ in range(args.warmup):
+        layer.forward(x, Wr, lo, sb, out=y, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fwd_ms = e0.elapsed_time(e1) / K
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty(T, d, dtype=dt).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(args.warmup):
+        x_dev.copy_(x_host, non_blocking=True)
+        B.moe_forward(cfg, x_dev, Wr, lo, sb, layer.packed, y, fw_ws, stream)
+        y_host.copy_(y, non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        x_dev.copy_(x_host, non_blocking=True)
+        B.moe_forward(cfg, x_dev, Wr, lo, sb, layer.packed, y, fw_ws, stream)
+        y_host.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    B.moe_check_device_error(stream)
+
+    # ---- work model and roofline
+    peaks, peak_src = load_peaks()
+    offs = off.cpu().numpy()
+    model, A, touched = work_model(wl, offs, int((np.diff(offs) > 0).sum()))
+    bw = peaks["hbm_gbs"]
+    stage_info = {}
+    for s in STAGES:
+        t_s = stage_ms[s] * 1e-3
+        gbs = model[s]["bytes"] / t_s / 1e9
+        tfl = model[s]["flops"] / t_s / 1e12
+        t_mem = model[s]["bytes"] / (bw * 1e9)
+        t_cmp = model[s]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
+        bound = "tensor" if (s.startswith("ffn") and t_cmp > t_mem) else "hbm"
+        stage_info[s] = {"ms": round(stage_ms[s], 5), "GB/s": round(gbs, 1), "TFLOP/s": round(tfl, 2),
+                         "bound": bound,
+                         "frac": round(gbs / bw if bound == "hbm" else tfl / peaks["bf16_tflops_sustained"], 4)}
+    dom = max(STAGES, key=lambda s: stage_ms[s])
+    di = stage_info[dom]
+    if di["bound"] == "hbm":
+        roof = {"bound": "hbm", "achieved": di["GB/s"], "peak": bw, "unit": "GB/s",
+                "frac": round(di["GB/s"] / bw, 4)}
+    else:
+        p = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": di["TFLOP/s"], "peak": p, "unit": "TFLOP/s",
+                "frac": round(di["TFLOP/s"] / p, 4)}
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["traffic"] = recorded_traffic(dom, wl.name)
+    roof["algorithmic_bytes_per_launch"] = model[dom]["bytes"]
+
+    step_ms = total_ms / K
+    ffn_s = (stage_ms["ffn_up"] + stage_ms["ffn_down"]) * 1e-3
+    gemm_flops = model["ffn_up"]["flops"] + model["ffn_down"]["flops"]
+    gemm_tflops = gemm_flops / ffn_s / 1e12
+    layer_bytes = sum(model[s]["bytes"] for s in STAGES)
+    layer_flops = sum(model[s]["flops"] for s in ("ffn_up", "ffn_down"))
+    layer_roof_ms = max(layer_flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (bw * 1e9)) * 1e3
+    value = ws_n * T * K / (total_ms * 1e-3)
+    x_bytes = T * d * x.element_size()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws_n,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; random-init expert weights)",
+        "config": {"workload": wl.name, "T": T, "d": d, "E": wl.E, "d_ff": wl.f, "k": wl.k, "gate": wl.gate,
+                   "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
+                   "n_shared": wl.n_shared, "f_shared": wl.f_shared,
+                   "assignments_computed": A, "experts_touched": touched,
+                   "l2": "inputs larger than L2: the expert weights read per step exceed 126 MB"
+                         if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2",
+                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+        "grouped_gemm": {"tflops": round(gemm_tflops, 2),
+                         "pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
+                         "bf16_peak_tflops": peaks["bf16_tflops"], "flops_per_step": gemm_flops},
+        "layer_roofline": {"ms": round(layer_roof_ms, 5), "frac": round(layer_roof_ms / step_ms, 4),
+                           "bytes_per_step": layer_bytes, "flops_per_step": layer_flops},
+        "stages": stage_info,
+        "forward_ms": round(fwd_ms, 5),
+        "roofline": roof,
+        "e2e": {"value": round(ws_n * T * K / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": T * d * y.element_size(),
+                "ms_per_step": round(e2e_ms / K, 5)},
+        "gpu_launches": K * B.moe_launch_count(cfg, B.MOE_STAGE_FORWARD),
+        "clocks": clk,
+    }
+    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
+    if ws_n > 1:
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ------------------------------------------------------------------------------------ oracle arms
+def _oracle_host_inputs(wl, inp):
+    """Host fp32 copies of the workload (exact run-dtype values) for the oracle."""
+    h = {}
+    for k, v in inp.items():
+        h[k] = None if v is None else np.ascontiguousarray(v.detach().float().cpu().numpy())
+    return h
+
+
+def _oracle_setup(oracle, wl, h):
+    """Routing and capacity dispatch of the whole batch, once: which slots are
+    dropped depends on the global token order, so the sampled steps reuse it."""
+    if wl.mode == "ec":
+        tok, w, _ = oracle.route_ec(h["x"], h["W_r"], wl.ec_capacity, h["logit_offset"])
+        return {"ec_tok": tok, "ec_w": w}
+    idx, w, _ = oracle.route_tc(h["x"], h["W_r"], wl.k, wl.gate, h["logit_offset"], h["sel_bias"], wl.renorm)
+    cap = oracle.capacity(wl.capacity_factor, wl.T, wl.k, wl.E)
+    _, _, slot, _ = oracle.dispatch_tc(idx, wl.E, cap)
+    return {"idx": idx, "w": w, "slot": slot, "cap": cap}
+
+
+def _oracle_step(oracle, wl, h, st, tokens):
+    """One oracle step over a token sample, one thread: the sample's routing
+    (scores and top-k, or the Expert Choice affinities and a proportional
+    column top-cap), the capacity dispatch of the batch, then experts + combine
+    for the sample.  Returns seconds."""
+    t0 = time.perf_counter()
+    xs = h["x"][tokens]
+    if wl.mode == "ec":
+        cap = max(1, wl.ec_capacity * len(tokens) // wl.T)
+        oracle.route_ec(xs, h["W_r"], cap, h["logit_offset"])
+        oracle.forward_ec_streamed(h["x"], st["ec_tok"], st["ec_w"], h["W1"], h["W3"], h["W2"], tokens,
+                                   h.get("W1s"), h.get("W3s"), h.get("W2s"))
+    else:
+        oracle.route_tc(xs, h["W_r"], wl.k, wl.gate, h["logit_offset"], h["sel_bias"], wl.renorm)
+        oracle.dispatch_tc(st["idx"], wl.E, st["cap"])
+        oracle.forward_tc_streamed(h["x"], st["idx"], st["w"], st["slot"], h["W1"], h["W3"], h["W2"], tokens,
+                                   h.get("W1s"), h.get("W3s"), h.get("W2s"))
+    return time.perf_counter() - t0
+
+
+def _sample_tokens(wl, n, seed=20261202):
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(wl.T, size=min(max(1, n), wl.T), replace=False)).astype(np.int64)
+
+
+def _sample_text(wl, n):
+    return (f"fp64 C oracle, 1 thread; per step a seeded sample of {n} of the {wl.T} tokens: their routing, "
+            f"the capacity dispatch of the batch, their experts + combine; tokens/s = sample tokens / step time")
+
+
+def cpu_baseline(wl, inp, n_tokens):
+    import oracle
+    oracle.build()
+    h = _oracle_host_inputs(wl, inp)
+    st = _oracle_setup(oracle, wl, h)
+    toks = _sample_tokens(wl, n_tokens)
+    dt = _oracle_step(oracle, wl, h, st, toks)
+    return {"value": round(len(toks) / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": _sample_text(wl, len(toks)) + f" ({dt:.1f} s)", "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    ws_n, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    if args.T:
+        wl = wl.with_(T=args.T)
+    inp = make_inputs(wl, "cpu")
+    h = _oracle_host_inputs(wl, inp)
+    del inp
+    st = _oracle_setup(oracle, wl, h)
+    # size the per-step sample so that warm-up + timed steps take about args.ref_budget seconds
+    probe = _sample_tokens(wl, 4, seed=1)
+    per_tok = _oracle_step(oracle, wl, h, st, probe) / len(probe)
+    n = int(max(1, min(args.ref_tokens, args.ref_budget / max(1, args.steps + args.warmup) / per_tok)))
+    for i in range(args.warmup):
+        _oracle_step(oracle, wl, h, st, _sample_tokens(wl, n, seed=100 + i))
+    wall = []
+    for i in range(args.steps):
+        wall.append(_oracle_step(oracle, wl, h, st, _sample_tokens(wl, n, seed=1000 + i)))
+    value = n * len(wall) / sum(wall)
+    sample = _sample_text(wl, n)
+    return {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(wall)), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "d_ff": wl.f, "k": wl.k},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--T", type=int, default=0, help="override the token count")
+    ap.add_argument("--cpu-tokens", type=int, default=768, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=256, help="largest oracle sample per reference step")
+    ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds the reference arm aims to take")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

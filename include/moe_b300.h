@@ -178,6 +178,20 @@ moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int3
                            void *stream);
 
 /*
+ * The two halves of moe_grouped_ffn, for callers that keep the hidden activations.
+ * moe_grouped_ffn_up:   H[rows_routed][f] rows [0, off[E]) = SiLU(X W1) * (X W3) of
+ *   each row's expert; with shared experts Hs[T][n_shared*f_shared] = the merged
+ *   shared hidden activations of x (Hs may be NULL when n_shared == 0).
+ * moe_grouped_ffn_down: Y rows [0, off[E]) = H W2 of each row's expert; with shared
+ *   experts rows [rows_routed, rows_routed + T) = Hs times the merged shared W2.
+ * H, Hs in cfg->dtype.  Neither call needs workspace.
+ */
+moe_status moe_grouped_ffn_up(const moe_config *cfg, const void *x_perm, const int32_t *off,
+                              const void *packed, const void *x, void *H, void *Hs, void *stream);
+moe_status moe_grouped_ffn_down(const moe_config *cfg, const void *H, const void *Hs, const int32_t *off,
+                                const void *packed, void *Y, void *stream);
+
+/*
  * Gate-weighted combine back to token order ("技术日报" §3.1, §3.4, §9.1).
  * Token choice: y[t] = sum_{j: slot_of[t][j] >= 0} topk_w[t][j] * Y[slot_of[t][j]]
  *   (+ Y[rows_routed + t] with shared experts), slots in order.
@@ -199,6 +213,10 @@ moe_status moe_combine(const moe_config *cfg, const void *Y, const int32_t *slot
 moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
                        const float *sel_bias, const void *packed, void *y, void *ws, size_t ws_bytes,
                        void *stream);
+
+/* Number of CUDA kernels one call of `stage` enqueues for this configuration
+ * (memsets not counted; MOE_STAGE_FORWARD: the whole layer).  No CUDA call. */
+moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *kernels);
 
 /*
  * Waits for `stream`, then reads and clears the device error word.  Returns

@@ -23,7 +23,8 @@ MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, M
 
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
            "moe_workspace_size", "moe_packed_weights_size", "moe_pack_weights", "moe_route", "moe_dispatch",
-           "moe_grouped_ffn", "moe_combine", "moe_forward", "moe_check_device_error")
+           "moe_grouped_ffn", "moe_grouped_ffn_up", "moe_grouped_ffn_down", "moe_combine", "moe_forward",
+           "moe_launch_count", "moe_check_device_error")
 
 
 class MoeError(RuntimeError):
@@ -64,6 +65,9 @@ def lib():
             "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_grouped_ffn": [cfgp, vp, vp, vp, vp, vp, vp, sz, vp],
+            "moe_grouped_ffn_up": [cfgp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_grouped_ffn_down": [cfgp, vp, vp, vp, vp, vp, vp],
+            "moe_launch_count": [cfgp, ctypes.c_int, i32p],
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, sz, vp],
             "moe_forward": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_check_device_error": [vp],
@@ -170,6 +174,22 @@ def moe_dispatch(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, ws, stream=Non
 def moe_grouped_ffn(cfg, x_perm, off, packed, x, Y, ws, stream=None):
     _check(lib().moe_grouped_ffn(ctypes.byref(cfg), _p(x_perm), _p(off), _p(packed), _p(x), _p(Y), _p(ws),
                                  _nbytes(ws), _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_grouped_ffn_up(cfg, x_perm, off, packed, x, H, Hs, stream=None):
+    _check(lib().moe_grouped_ffn_up(ctypes.byref(cfg), _p(x_perm), _p(off), _p(packed), _p(x), _p(H), _p(Hs),
+                                    _stream(stream)), "moe_grouped_ffn_up")
+
+
+def moe_grouped_ffn_down(cfg, H, Hs, off, packed, Y, stream=None):
+    _check(lib().moe_grouped_ffn_down(ctypes.byref(cfg), _p(H), _p(Hs), _p(off), _p(packed), _p(Y),
+                                      _stream(stream)), "moe_grouped_ffn_down")
+
+
+def moe_launch_count(cfg, stage=MOE_STAGE_FORWARD) -> int:
+    n = ctypes.c_int32()
+    _check(lib().moe_launch_count(ctypes.byref(cfg), int(stage), ctypes.byref(n)), "moe_launch_count")
+    return n.value
 
 
 def moe_combine(cfg, Y, slot_of, topk_w, y, ws=None, stream=None):

@@ -9,6 +9,8 @@
 //   up   : tile 64 rows x 64 hidden columns (one packed group = 64 W1 + 64 W3 rows)
 //   down : tile 64 rows x 64 output columns
 // Each of the 256 threads owns a 4x4 block of the tile (x2 for gate/up).
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -113,14 +115,12 @@ __global__ void __launch_bounds__(kThreads) ffn_simt_kernel(SimtArgs a) {
 }
 
 template <typename T>
-cudaError_t run(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off, const void *packed,
-                const void *x, void *H, void *Hs, void *Y, cudaStream_t s) {
+cudaError_t run_up(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off, const void *packed,
+                   const void *x, void *H, void *Hs, cudaStream_t s) {
     const PackedLayout L = packed_layout(c);
     const char *pk = static_cast<const char *>(packed);
     const int shared_rows = c.n_shared > 0 ? c.T : 0;
     const int64_t max_tiles_m = (z.rows_routed + kBM - 1) / kBM + c.E + (shared_rows + kBM - 1) / kBM;
-    int grid = num_sms() * 4;
-
     SimtArgs up{};
     up.g = GroupedShape{off, c.E, shared_rows, c.f / kBN, z.fs_tot / kBN};
     up.A0 = x_perm;
@@ -134,9 +134,19 @@ cudaError_t run(const moe_config &c, const Sizes &z, const void *x_perm, const i
     up.ldc0 = c.f;
     up.ldc1 = z.fs_tot;
     up.b_rows0 = 2 * c.f;
-    int g1 = (int)std::min<int64_t>(grid, max_tiles_m * (c.f / kBN > 0 ? c.f / kBN : 1));
-    ffn_simt_kernel<T, true><<<g1 > 0 ? g1 : 1, kThreads, 0, s>>>(up);
+    const int nb = std::max(c.f, z.fs_tot) / kBN;
+    const int g1 = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms() * 4, max_tiles_m * nb));
+    ffn_simt_kernel<T, true><<<g1, kThreads, 0, s>>>(up);
+    return cudaGetLastError();
+}
 
+template <typename T>
+cudaError_t run_down(const moe_config &c, const Sizes &z, const void *H, const void *Hs, const int32_t *off,
+                     const void *packed, void *Y, cudaStream_t s) {
+    const PackedLayout L = packed_layout(c);
+    const char *pk = static_cast<const char *>(packed);
+    const int shared_rows = c.n_shared > 0 ? c.T : 0;
+    const int64_t max_tiles_m = (z.rows_routed + kBM - 1) / kBM + c.E + (shared_rows + kBM - 1) / kBM;
     SimtArgs dn{};
     dn.g = GroupedShape{off, c.E, shared_rows, c.d / kBN, c.d / kBN};
     dn.A0 = H;
@@ -150,17 +160,23 @@ cudaError_t run(const moe_config &c, const Sizes &z, const void *x_perm, const i
     dn.ldc0 = c.d;
     dn.ldc1 = c.d;
     dn.b_rows0 = c.d;
-    int g2 = (int)std::min<int64_t>(grid, max_tiles_m * (c.d / kBN));
-    ffn_simt_kernel<T, false><<<g2 > 0 ? g2 : 1, kThreads, 0, s>>>(dn);
+    const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms() * 4, max_tiles_m * (c.d / kBN)));
+    ffn_simt_kernel<T, false><<<g2, kThreads, 0, s>>>(dn);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_ffn_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
-                            const void *packed, const void *x, void *H, void *Hs, void *Y, cudaStream_t s) {
-    if (c.dtype == MOE_F32) return run<float>(c, z, x_perm, off, packed, x, H, Hs, Y, s);
-    return run<__nv_bfloat16>(c, z, x_perm, off, packed, x, H, Hs, Y, s);
+cudaError_t launch_ffn_up_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                               const void *packed, const void *x, void *H, void *Hs, cudaStream_t s) {
+    if (c.dtype == MOE_F32) return run_up<float>(c, z, x_perm, off, packed, x, H, Hs, s);
+    return run_up<__nv_bfloat16>(c, z, x_perm, off, packed, x, H, Hs, s);
+}
+
+cudaError_t launch_ffn_down_simt(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
+                                 const int32_t *off, const void *packed, void *Y, cudaStream_t s) {
+    if (c.dtype == MOE_F32) return run_down<float>(c, z, H, Hs, off, packed, Y, s);
+    return run_down<__nv_bfloat16>(c, z, H, Hs, off, packed, Y, s);
 }
 
 }  // namespace moe

@@ -165,10 +165,20 @@ moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, c
     const Sizes z = sizes_of(c);
     void *H = ws + L.H;
     void *Hs = ws + L.Hs;
-    cudaError_t e = (c.dtype == MOE_BF16) ? launch_ffn_tcgen05(c, z, x_perm, off, packed, x, H, Hs, Y, err, s)
-                                          : launch_ffn_simt(c, z, x_perm, off, packed, x, H, Hs, Y, s);
+    cudaError_t e = (c.dtype == MOE_BF16) ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
+                                          : launch_ffn_up_simt(c, z, x_perm, off, packed, x, H, Hs, s);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = (c.dtype == MOE_BF16) ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
+                              : launch_ffn_down_simt(c, z, H, Hs, off, packed, Y, s);
     return from_cuda(e);
 }
+
+// kernels enqueued per stage; mirrors the launch sequence of the do_* bodies above
+int route_launches(const moe_config &c) {
+    const int base = (c.dtype == MOE_BF16 && route_tcgen05_supported(c)) ? route_tcgen05_launches(c) : 1;
+    return base + (c.mode == MOE_EXPERT_CHOICE ? 1 : 0);
+}
+int dispatch_launches(const moe_config &c) { return c.mode == MOE_EXPERT_CHOICE ? 2 : 4; }
 
 }  // namespace
 
@@ -405,6 +415,60 @@ moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int3
     st = device_setup(&err);
     if (st != MOE_OK || c.T == 0) return st;
     return do_ffn(c, x_perm, off, packed, x, Y, static_cast<char *>(ws), err, static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_ffn_up(const moe_config *cfg, const void *x_perm, const int32_t *off, const void *packed,
+                              const void *x, void *H, void *Hs, void *stream) {
+    moe_status st = moe_validate_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    MOE_REQUIRE(x_perm && off && packed && H, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(c.n_shared == 0 || (x && Hs), MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(aligned16(x_perm) && aligned16(x) && aligned16(H) && aligned16(Hs) && aligned4(off),
+                MOE_ERR_MISALIGNED);
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(packed) & 255u) == 0, MOE_ERR_MISALIGNED);
+    unsigned *err = nullptr;
+    st = device_setup(&err);
+    if (st != MOE_OK || c.T == 0) return st;
+    const Sizes z = sizes_of(c);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(c.dtype == MOE_BF16 ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
+                                         : launch_ffn_up_simt(c, z, x_perm, off, packed, x, H, Hs, s));
+}
+
+moe_status moe_grouped_ffn_down(const moe_config *cfg, const void *H, const void *Hs, const int32_t *off,
+                                const void *packed, void *Y, void *stream) {
+    moe_status st = moe_validate_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    MOE_REQUIRE(H && off && packed && Y, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(c.n_shared == 0 || Hs, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(aligned16(H) && aligned16(Hs) && aligned16(Y) && aligned4(off), MOE_ERR_MISALIGNED);
+    MOE_REQUIRE((reinterpret_cast<uintptr_t>(packed) & 255u) == 0, MOE_ERR_MISALIGNED);
+    unsigned *err = nullptr;
+    st = device_setup(&err);
+    if (st != MOE_OK || c.T == 0) return st;
+    const Sizes z = sizes_of(c);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(c.dtype == MOE_BF16 ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
+                                         : launch_ffn_down_simt(c, z, H, Hs, off, packed, Y, s));
+}
+
+moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *kernels) {
+    moe_status st = moe_validate_config(cfg);
+    if (st != MOE_OK) return st;
+    if (!kernels) return MOE_ERR_INVALID_ARG;
+    const moe_config &c = *cfg;
+    const int empty = c.T == 0;
+    switch (stage) {
+        case MOE_STAGE_ROUTE: *kernels = empty ? 0 : route_launches(c); break;
+        case MOE_STAGE_DISPATCH: *kernels = empty ? 0 : dispatch_launches(c); break;
+        case MOE_STAGE_GROUPED_FFN: *kernels = empty ? 0 : 2; break;
+        case MOE_STAGE_COMBINE: *kernels = empty ? 0 : 1; break;
+        case MOE_STAGE_FORWARD: *kernels = empty ? 0 : route_launches(c) + dispatch_launches(c) + 2 + 1; break;
+        default: return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
 }
 
 moe_status moe_combine(const moe_config *cfg, const void *Y, const int32_t *slot_of, const float *topk_w, void *y,

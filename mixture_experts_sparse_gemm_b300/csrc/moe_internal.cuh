@@ -67,24 +67,23 @@ cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, c
                            const float *w, void *y, cudaStream_t s);
 cudaError_t launch_pack(const moe_config &c, const void *W1, const void *W3, const void *W2,
                         const void *W1s, const void *W3s, const void *W2s, void *packed, cudaStream_t s);
-cudaError_t launch_ffn_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
-                            const void *packed, const void *x, void *H, void *Hs, void *Y,
-                            cudaStream_t s);
-
+cudaError_t launch_ffn_up_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                               const void *packed, const void *x, void *H, void *Hs, cudaStream_t s);
+cudaError_t launch_ffn_down_simt(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
+                                 const int32_t *off, const void *packed, void *Y, cudaStream_t s);
 // tcgen05 path (bf16)
-struct TcFfnScratch {
-    void *H;      // [rows_routed][f] bf16
-    void *Hs;     // [T][fs_tot] bf16
-};
-cudaError_t launch_ffn_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
-                               const void *packed, const void *x, void *H, void *Hs, void *Y,
-                               unsigned *err, cudaStream_t s);
+cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                                  const void *packed, const void *x, void *H, void *Hs, unsigned *err,
+                                  cudaStream_t s);
+cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
+                                    const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s);
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r,
                                  const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
                                  float *topk_w, float *scores_t, void *wr_t, unsigned *err,
                                  cudaStream_t s);
 size_t route_tcgen05_scratch_bytes(const moe_config &c);
 bool route_tcgen05_supported(const moe_config &c);
+int route_tcgen05_launches(const moe_config &c);
 
 int num_sms();
 

@@ -1,13 +1,86 @@
-// Router logits on the tensor cores: not enabled yet; the CUDA-core router runs.
-#include "moe_internal.cuh"
+// Router on the tensor cores (bf16): the logits u = x W_r are one dense GEMM
+// [T, d] x [d, E], so they run on tcgen05 through the persistent GEMM of
+// tc_gemm.cuh (M = 128 tokens per tile, N = E rounded up to 16..256, K = d), and
+// the whole scoring step lives in its TMEM epilogue: one thread per token reads
+// its row of E logits, applies the logit offset, scores them (softmax or
+// sigmoid, "技术日报 2026-04-14" §3.2 / §3.5), selects the top k on
+// score + selection bias (§3.1, §4.3) and writes indices and (renormalised,
+// §9.1) weights; for Expert Choice (§3.3) it writes the softmax scores
+// expert-major for the column selection.  The logits never reach HBM.
+//
+// W_r arrives as [d][E] (the pages' x W_r); the MMA wants it K-major, so a small
+// transpose writes W_r^T [Npad][d] (zero rows E..Npad-1) into the workspace.
+#include "tc_gemm.cuh"
 
 namespace moe {
+namespace {
 
-bool route_tcgen05_supported(const moe_config &) { return false; }
-size_t route_tcgen05_scratch_bytes(const moe_config &) { return 0; }
-cudaError_t launch_route_tcgen05(const moe_config &, const void *, const void *, const float *, const float *,
-                                 int32_t *, float *, float *, void *, unsigned *, cudaStream_t) {
-    return cudaErrorNotSupported;
+int padded_n(int E) {
+    int n = 16;
+    while (n < E) n *= 2;
+    return n;   // 16, 32, 64, 128 or 256
+}
+
+// wr_t[e][i] = W_r[i][e] for e < E, 0 for E <= e < npad; seg = {0, T}
+__global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __nv_bfloat16 *__restrict__ wr_t,
+                                        int d, int E, int npad, int32_t *seg, int T) {
+    __shared__ __nv_bfloat16 tile[32][34];
+    const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+    for (int ii = threadIdx.y; ii < 32; ii += blockDim.y) {
+        const int i = i0 + ii, e = e0 + threadIdx.x;
+        tile[ii][threadIdx.x] = (i < d && e < E) ? Wr[(size_t)i * E + e] : __float2bfloat16_rn(0.f);
+    }
+    __syncthreads();
+    for (int ee = threadIdx.y; ee < 32; ee += blockDim.y) {
+        const int e = e0 + ee, i = i0 + threadIdx.x;
+        if (e < npad && i < d) wr_t[(size_t)e * d + i] = tile[threadIdx.x][ee];
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) {
+        seg[0] = 0;
+        seg[1] = T;
+    }
+}
+
+}  // namespace
+
+bool route_tcgen05_supported(const moe_config &c) { return c.dtype == MOE_BF16 && c.E <= kMaxE && c.d % 64 == 0; }
+
+size_t route_tcgen05_scratch_bytes(const moe_config &c) {
+    return align_up((size_t)padded_n(c.E) * c.d * 2, 256) + 256;
+}
+
+int route_tcgen05_launches(const moe_config &) { return 2; }
+
+cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
+                                 const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t, void *wr_t,
+                                 unsigned *err, cudaStream_t s) {
+    const int npad = padded_n(c.E);
+    char *scratch = static_cast<char *>(wr_t);
+    __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(scratch);
+    int32_t *seg = reinterpret_cast<int32_t *>(scratch + align_up((size_t)npad * c.d * 2, 256));
+    const dim3 tg((npad + 31) / 32, (c.d + 31) / 32);
+    transpose_router_kernel<<<tg, dim3(32, 8), 0, s>>>(static_cast<const __nv_bfloat16 *>(W_r), wt, c.d, c.E, npad,
+                                                       seg, c.T);
+    CUtensorMap a0, b0;
+    bool ok = make_tmap_bf16(&a0, x, (uint64_t)c.T, c.d, kBM);
+    ok = ok && make_tmap_bf16(&b0, wt, (uint64_t)npad, c.d, npad);
+    if (!ok) return cudaErrorInvalidValue;
+    TcArgs g{};
+    g.g = GroupedShape{seg, 1, 0, 1, 0};
+    g.K0 = c.d;
+    g.K1 = c.d;
+    g.b_rows0 = npad;
+    g.route = RouteEpi{logit_offset, sel_bias, topk_idx, topk_w, scores_t, c.T, c.E, c.k, c.gate, c.mode,
+                       c.renormalize};
+    g.err = err;
+    const int64_t tiles = (c.T + kBM - 1) / kBM;
+    switch (npad) {
+        case 16: return launch_gemm<16, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+        case 32: return launch_gemm<32, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+        case 64: return launch_gemm<64, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+        case 128: return launch_gemm<128, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+        default: return launch_gemm<256, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+    }
 }
 
 }  // namespace moe

@@ -1,0 +1,426 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (bf16 in, fp32
+// accumulate in TMEM), shared by the expert GEMMs and the router.
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer: 128x64 A tile + BNx64 B tile per stage, 128-byte
+//               swizzle, into a STAGES-deep shared-memory ring (full/empty mbarriers)
+//   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16)
+//               per stage into one of two TMEM accumulators
+//   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
+//               thread), then the epilogue of the instantiation; it overlaps the
+//               next tile's main loop through the second accumulator
+// Tiles never straddle segments: the tile table is built on the device from
+// off[] (segment s < E = routed expert s, segment E = merged shared experts), and
+// a segment's last M tile reads rows past its end (the next segment's rows, or
+// zero fill beyond the tensor) whose results are never stored.
+//
+// Epilogues:
+//   kEpiSwiGLU  up projection.  The packed B rows of a tile alternate 64 W1
+//               columns and the same 64 W3 columns, so a thread holds gate and up
+//               values of the same hidden columns: H = SiLU(gate) * up, bf16.
+//   kEpiStore   down projection: bf16 rows of Y.
+//   kEpiRoute   router: one row = one token's E logits.  Softmax or sigmoid score,
+//               selection-only bias, top-k by insertion in ascending expert order
+//               (ties keep the lower index), renormalised weights; or, for Expert
+//               Choice, the softmax scores written expert-major.
+#pragma once
+
+#include <float.h>
+
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kEpiSwiGLU = 0;
+constexpr int kEpiStore = 1;
+constexpr int kEpiRoute = 2;
+
+template <int BN>
+struct TcCfg {
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
+    static constexpr int kBarBytes = (2 * kStages + 5) * 8;
+    static constexpr int kMiscBytes = 64 + sizeof(int) * (3 * (kMaxE + 2));
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kMiscBytes;
+};
+
+struct RouteEpi {
+    const float *logit_offset;   // [E] or null
+    const float *sel_bias;       // [E] or null
+    int32_t *topk_idx;           // [T][k]
+    float *topk_w;               // [T][k]
+    float *scores_t;             // expert choice: [E][T]
+    int T, E, k, gate, mode, renorm;
+};
+
+struct TcArgs {
+    GroupedShape g;
+    int K0, K1;        // reduction width, routed / shared
+    int b_rows0;       // packed B rows per routed segment
+    void *C0;          // routed output rows (bf16)
+    void *C1;          // shared output rows (bf16)
+    int ldc0, ldc1;    // output row pitch in elements
+    RouteEpi route;
+    unsigned *err;
+};
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Router epilogue of one token row (all 32 lanes of the warp take part in the
+// TMEM loads; `valid` says whether this lane's row is a token).
+template <int BN>
+__device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid, int T) {
+    const int E = r.E;
+    constexpr int kChunks = BN / 16;
+    const bool softmax = r.gate == MOE_GATE_SOFTMAX;
+    float mx = -FLT_MAX, inv = 1.f;
+    if (softmax) {
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = c * 16 + i;
+                if (e < E) mx = fmaxf(mx, __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f));
+            }
+        }
+        float sum = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = c * 16 + i;
+                if (e < E) sum += expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx);
+            }
+        }
+        inv = 1.f / sum;
+    }
+    float tk[kMaxK], tp[kMaxK];
+    int ti[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+        tk[j] = -FLT_MAX;
+        tp[j] = 0.f;
+        ti[j] = 0x7fffffff;
+    }
+    const int k = r.k;
+    const bool ec = r.mode == MOE_EXPERT_CHOICE;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e = c * 16 + i;
+            if (e >= E) continue;
+            const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
+            const float p = softmax ? expf(u - mx) * inv : 1.f / (1.f + expf(-u));
+            if (ec) {
+                if (valid) r.scores_t[(size_t)e * T + t] = p;
+                continue;
+            }
+            const float key = p + (r.sel_bias ? r.sel_bias[e] : 0.f);
+            // keep the best kMaxK in (key desc, index asc) order; the first k of
+            // them are the top k.  Experts arrive in ascending order and only a
+            // strictly larger key moves up, so a tie keeps the lower index first.
+            if (key > tk[kMaxK - 1]) {
+                tk[kMaxK - 1] = key;
+                ti[kMaxK - 1] = e;
+                tp[kMaxK - 1] = p;
+#pragma unroll
+                for (int j = kMaxK - 1; j > 0; --j) {
+                    if (tk[j] > tk[j - 1]) {
+                        const float a = tk[j], b = tp[j];
+                        const int q = ti[j];
+                        tk[j] = tk[j - 1];
+                        tp[j] = tp[j - 1];
+                        ti[j] = ti[j - 1];
+                        tk[j - 1] = a;
+                        tp[j - 1] = b;
+                        ti[j - 1] = q;
+                    }
+                }
+            }
+        }
+    }
+    if (!ec && valid) {
+        float wsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+            if (j < k) wsum += tp[j];
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+                r.topk_idx[(size_t)t * k + j] = ti[j];
+                r.topk_w[(size_t)t * k + j] = r.renorm ? tp[j] / wsum : tp[j];
+            }
+        }
+    }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                           const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                           TcArgs a) {
+    using C = TcCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *tiles = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + (size_t)C::kStages * C::kStageBytes);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + C::kStages;
+    uint64_t *tfull = bars + 2 * C::kStages;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *drain = tempty + 2;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *tile_start = reinterpret_cast<int *>(tmem_holder + 16);
+    int *seg_row0 = tile_start + (kMaxE + 2);
+    int *seg_rows = seg_row0 + (kMaxE + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&tfull[i]), 1);
+            mbar_init(smem_u32(&tempty[i]), 4);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+        prefetch_tmap(&tmA0);
+        prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmB0);
+        prefetch_tmap(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
+        fence_before();
+    }
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const int S = build_tile_table<kBM>(a.g, tile_start, seg_row0, seg_rows);
+    const int total = tile_start[S];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                int s, mb, nb;
+                decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
+                const bool routed = s < a.g.E;
+                const CUtensorMap *mA = routed ? &tmA0 : &tmA1;
+                const CUtensorMap *mB = routed ? &tmB0 : &tmB1;
+                const int arow = seg_row0[s] + mb * kBM;
+                const int brow = (routed ? s * a.b_rows0 : 0) + nb * BN;
+                const int nk = (routed ? a.K0 : a.K1) / kBK;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[stage]);
+                    uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
+                    mbar_arrive_expect_tx(fb, C::kStageBytes);
+                    tma_load_2d(smem_u32(st), mA, kb * kBK, arow, fb);
+                    tma_load_2d(smem_u32(st + C::kABytes), mB, kb * kBK, brow, fb);
+                    ++issued;
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // leave no copy in flight: wait (bounded) for the last stages issued
+                const int n = issued < C::kStages ? issued : C::kStages;
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < n; ++i) {
+                    if (--st < 0) {
+                        st = C::kStages - 1;
+                        ph ^= 1u;
+                    }
+                    const uint32_t fb = smem_u32(&full[st]);
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(fb, ph) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+                int s, mb, nb;
+                decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
+                const int nk = ((s < a.g.E) ? a.K0 : a.K1) / kBK;
+                const int acc = it & 1;
+                const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+                if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_after();
+                    const uint32_t sa = smem_u32(tiles + (size_t)stage * C::kStageBytes);
+                    const uint64_t adesc = sdesc_k128(sa);
+                    const uint64_t bdesc = sdesc_k128(sa + C::kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // advance 16 bf16 = 32 bytes inside the swizzle atom (encoded >> 4)
+                        mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), kIdesc,
+                                 (kb | kk) != 0);
+                    }
+                    mma_commit(smem_u32(&empty[stage]));
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&tfull[acc]));
+            }
+            // every MMA issued has finished before TMEM is released
+            mma_commit(smem_u32(drain));
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- epilogue
+        const int quarter = warp & 3;   // TMEM lanes [32*quarter, 32*quarter + 32)
+        const int row = quarter * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            int s, mb, nb;
+            decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, a.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            fence_after();
+            const bool routed = s < a.g.E;
+            const int rows = min(kBM, seg_rows[s] - mb * kBM);
+            const int grow = seg_row0[s] + mb * kBM + row;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+            if constexpr (EPI == kEpiRoute) {
+                route_epilogue<BN>(a.route, taddr, grow, row < rows, a.route.T);
+            } else {
+                __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? a.C0 : a.C1);
+                const int ldc = routed ? a.ldc0 : a.ldc1;
+                if constexpr (EPI == kEpiSwiGLU) {
+#pragma unroll 1
+                    for (int grp = 0; grp < BN / 128; ++grp) {
+#pragma unroll 1
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t g[16], u[16];
+                            tmem_ld16(taddr + grp * 128 + c * 16, g);
+                            tmem_ld16(taddr + grp * 128 + 64 + c * 16, u);
+                            tmem_ld_wait();
+                            uint32_t o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                                const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                                o[i] = pack_bf16x2(h0, h1);
+                            }
+                            if (row < rows) {
+                                uint4 *dst = reinterpret_cast<uint4 *>(Cp + (size_t)grow * ldc + nb * (BN / 2) +
+                                                                       grp * 64 + c * 16);
+                                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c = 0; c < BN / 16; ++c) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + c * 16, v);
+                        tmem_ld_wait();
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        if (row < rows) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(Cp + (size_t)grow * ldc + nb * BN + c * 16);
+                            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                }
+            }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
+                        const TcArgs &args, int64_t max_tiles, cudaStream_t s) {
+    auto kern = tc_grouped_gemm_kernel<BN, EPI>;
+    const size_t smem = TcCfg<BN>::kSmem;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    int grid = num_sms();
+    if (max_tiles < grid) grid = (int)(max_tiles > 1 ? max_tiles : 1);
+    kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace moe

@@ -94,9 +94,15 @@ EC_CASES = {
 }
 
 
-def _check_ec_selection(gt, gw, ot, S, cap, tau=1e-6):
+def _check_ec_selection(gt, gw, ot, S, cap, tau=1e-5):
     """Exactly cap ascending tokens per expert; every token clearly above the
-    oracle boundary taken, every token clearly below it not taken."""
+    oracle boundary taken, every token clearly below it not taken.
+
+    tau bounds the GPU's error on a score: the logits are an fp32 tensor-core
+    accumulation over d (about d/16 rounding steps of 2^-23 relative), which moves
+    a softmax score of ~0.3 by up to ~2e-6; tau = 1e-5 leaves a 5x margin.
+    Experts whose oracle boundary gap is below 2*tau are checked for validity
+    only, and their boundary tokens are reported as ambiguous."""
     E = gt.shape[0]
     ambiguous = set()
     for e in range(E):
@@ -113,7 +119,7 @@ def _check_ec_selection(gt, gw, ot, S, cap, tau=1e-6):
             np.testing.assert_array_equal(gt[e], ot[e])
         else:
             ambiguous.update(np.nonzero(np.abs(col - hi_b) <= 2 * tau)[0].tolist())
-        np.testing.assert_allclose(gw[e], col[gt[e]], atol=2e-6, rtol=0)
+        np.testing.assert_allclose(gw[e], col[gt[e]], atol=2e-5, rtol=0)
     return ambiguous
 
 
