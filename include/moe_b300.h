@@ -165,6 +165,31 @@ moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const vo
                         void *stream);
 
 /*
+ * moe_dispatch for callers that cannot allocate device memory.  (The paper has
+ * no counterpart; this is an interface convenience of the library.)
+ *
+ * Some callers cannot provide a workspace: a plugin inside a host framework that
+ * owns all device memory and hands over only the layer's inputs and outputs, or
+ * a latency-critical serving loop where a cudaMalloc could synchronise the
+ * device.  This call takes the same arguments and writes the same outputs as
+ * moe_dispatch, minus `ws`: its scratch is a 512 KiB array compiled into the
+ * library, present on every GPU that loads the library until the process exits.
+ *   - Token choice: T * k must not exceed MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS,
+ *     otherwise MOE_ERR_UNSUPPORTED is returned and nothing is launched.  Expert
+ *     choice needs no scratch and has no extra limit.
+ *   - The first call on a device looks up the array's address on that device;
+ *     make that first call before any stream capture.
+ *   - The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ *     routine).  All calls share the array and it keeps the last call's
+ *     contents; nothing in it needs clearing between calls, but calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on it and
+ *     must be serialised by the caller.
+ */
+#define MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS 65536
+moe_status moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *off,
+                                int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *stream);
+
+/*
  * Grouped SwiGLU experts over the ragged expert segments of x_perm ("lnwmold"
  * §2.2 W1, W2, W3; SwiGLU: (SiLU(X W1) * (X W3)) W2).
  *   x_perm[rows_routed][d], off[E+1] as written by moe_dispatch (read on the device;

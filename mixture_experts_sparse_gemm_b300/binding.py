@@ -24,7 +24,8 @@ MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, M
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
            "moe_workspace_size", "moe_packed_weights_size", "moe_pack_weights", "moe_route", "moe_dispatch",
            "moe_grouped_ffn", "moe_grouped_ffn_up", "moe_grouped_ffn_down", "moe_combine", "moe_forward",
-           "moe_launch_count", "moe_check_device_error")
+           "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc")
+MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS = 65536
 
 
 class MoeError(RuntimeError):
@@ -71,6 +72,7 @@ def lib():
             "moe_combine": [cfgp, vp, vp, vp, vp, vp, sz, vp],
             "moe_forward": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_check_device_error": [vp],
+            "moe_dispatch_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -169,6 +171,13 @@ def moe_route(cfg, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, ws, stream=
 def moe_dispatch(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, ws, stream=None):
     _check(lib().moe_dispatch(ctypes.byref(cfg), _p(topk_idx), _p(x), _p(off), _p(cnt_raw), _p(slot_of), _p(x_perm),
                               _p(ws), _nbytes(ws), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate device
+    memory; scratch comes from a fixed array inside the library (see the header)."""
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(cfg), _p(topk_idx), _p(x), _p(off), _p(cnt_raw), _p(slot_of),
+                                      _p(x_perm), _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_grouped_ffn(cfg, x_perm, off, packed, x, Y, ws, stream=None):

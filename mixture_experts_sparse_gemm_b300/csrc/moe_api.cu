@@ -212,6 +212,8 @@ PackedLayout packed_layout(const moe_config &c) {
     return L;
 }
 
+moe_status device_ready(unsigned **err_word) { return device_setup(err_word); }
+
 int num_sms() {
     int dev = 0;
     if (current_device(dev) != cudaSuccess || g_sm_count[dev] <= 0) return 148;

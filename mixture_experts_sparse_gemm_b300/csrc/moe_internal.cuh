@@ -86,6 +86,8 @@ bool route_tcgen05_supported(const moe_config &c);
 int route_tcgen05_launches(const moe_config &c);
 
 int num_sms();
+// architecture check and device error word of the current device (set up once per device)
+moe_status device_ready(unsigned **err_word);
 
 // ----------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ float to_f32(float v) { return v; }
