@@ -284,22 +284,43 @@ def run_gpu(args):
     torch.cuda.synchronize()
     fwd_ms = e0.elapsed_time(e1) / K
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    x_host = x.cpu().pin_memory()
-    y_host = torch.empty(T, d, dtype=dt).pin_memory()
-    x_dev = torch.empty_like(x)
-    for _ in range(args.warmup):
-        x_dev.copy_(x_host, non_blocking=True)
-        B.moe_forward(cfg, x_dev, Wr, lo, sb, layer.packed, y, fw_ws, stream)
-        y_host.copy_(y, non_blocking=True)
+    # ---- end to end through the C ABI with host buffers (pinned): every step copies its
+    # tokens host -> device, runs moe_forward and copies its output device -> host.  The
+    # copies of neighbouring steps overlap the compute on their own streams (double
+    # buffers), as a serving loop would run it.
+    x_host = [x.cpu().pin_memory(), x.cpu().pin_memory()]
+    y_host = [torch.empty(T, d, dtype=dt).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    y_dev = [torch.empty_like(y) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_done[b])          # step i-2 finished reading x_dev[b]
+                x_dev[b].copy_(x_host[b], non_blocking=True)
+                ev_in[b].record(s_in)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])             # step i-2's output has left y_dev[b]
+            B.moe_forward(cfg, x_dev[b], Wr, lo, sb, layer.packed, y_dev[b], fw_ws, stream)
+            ev_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[b])
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+                ev_out[b].record(s_out)
+
+    e2e_steps(args.warmup)
     barrier()
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(K):
-        x_dev.copy_(x_host, non_blocking=True)
-        B.moe_forward(cfg, x_dev, Wr, lo, sb, layer.packed, y, fw_ws, stream)
-        y_host.copy_(y, non_blocking=True)
-    e1.record(stream)
+    e0.record(s_in)
+    e2e_steps(K)
+    e1.record(s_out)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1))

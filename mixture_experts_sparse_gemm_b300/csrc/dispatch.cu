@@ -102,6 +102,104 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
     }
 }
 
+// The same three steps in one CTA of 32 warps, for up to kPlanMax assignments:
+// pass 1 counts per expert (shared-memory atomics), caps and scans them into
+// off[]; pass 2 walks the assignments in rounds of 32 chunks of 256, each round
+// counting per warp, turning the counts into per-warp bases (carried across
+// rounds), and ranking each warp's chunk in order as dispatch_rank_kernel does.
+constexpr int kPlanWarps = 32;
+constexpr int64_t kPlanMax = 65536;
+
+__global__ void __launch_bounds__(32 * kPlanWarps)
+    dispatch_plan_kernel(const int32_t *idx, int n, int k, int E, int cap, int32_t *cnt_raw, int32_t *off,
+                         int32_t *slot_of, int32_t *row_token, unsigned *err) {
+    extern __shared__ int sm[];
+    int *wcnt = sm;                        // [kPlanWarps][E]
+    int *run = wcnt + kPlanWarps * E;      // [E] running rank base per expert
+    int *offs = run + E;                   // [E + 1]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = tid; e < E; e += blockDim.x) run[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int e = idx[i];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&run[e], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {   // kept counts and their exclusive scan, 32 experts per step
+        int carry = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            int kept = 0;
+            if (e < E) {
+                cnt_raw[e] = run[e];
+                kept = (cap < 0) ? run[e] : min(run[e], cap);
+            }
+            int incl = kept;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (e < E) offs[e] = carry + incl - kept;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) offs[E] = carry;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += blockDim.x) {
+        off[e] = offs[e];
+        if (e < E) run[e] = 0;
+    }
+    __syncthreads();
+    int *my = wcnt + warp * E;
+    for (int base = 0; base < n; base += kPlanWarps * kChunk) {
+        const int c0 = base + warp * kChunk;
+        for (int e = lane; e < E; e += 32) my[e] = 0;
+        __syncwarp();
+        for (int i = lane; i < kChunk; i += 32) {
+            const int a = c0 + i;
+            if (a < n) {
+                const int e = idx[a];
+                if ((unsigned)e < (unsigned)E) atomicAdd(&my[e], 1);
+            }
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += blockDim.x) {   // per-warp bases, in chunk order
+            int s = run[e];
+            for (int w = 0; w < kPlanWarps; ++w) {
+                const int c = wcnt[w * E + e];
+                wcnt[w * E + e] = s;
+                s += c;
+            }
+            run[e] = s;
+        }
+        __syncthreads();
+        for (int step = 0; step < kChunk / 32; ++step) {
+            const int a = c0 + step * 32 + lane;
+            const int e_in = (a < n) ? idx[a] : -1;
+            const bool valid = (unsigned)e_in < (unsigned)E;
+            if (a < n && !valid) {
+                slot_of[a] = -1;
+                atomicOr(err, kErrBadIndex);
+            }
+            const int e = valid ? e_in : -1 - lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int rank_in = __popc(peers & ((1u << lane) - 1u));
+            const int b = valid ? my[e] : 0;
+            __syncwarp();
+            if (valid && rank_in == 0) my[e] = b + __popc(peers);
+            __syncwarp();
+            if (valid) {
+                const int r = b + rank_in;
+                const int slot = (cap < 0 || r < cap) ? offs[e] + r : -1;
+                slot_of[a] = slot;
+                if (slot >= 0) row_token[slot] = a / k;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // x_perm[row] = x[row_token[row]] for row < *rows (read on the device).
 __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, int vecs, const int32_t *__restrict__ row_token,
@@ -153,6 +251,8 @@ int gather_grid(int64_t rows) {
 
 }  // namespace
 
+int dispatch_tc_launches(int64_t assignments) { return assignments <= kPlanMax ? 2 : 4; }
+
 size_t dispatch_tc_scratch_ints(int64_t assignments, int E) {
     const int64_t nchunks = (assignments + kChunk - 1) / kChunk;
     return (size_t)(nchunks * E) + (size_t)assignments;   // chunk counts + row_token
@@ -162,13 +262,19 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s) {
     const int64_t n = (int64_t)c.T * c.k;
-    const int nchunks = (int)((n + kChunk - 1) / kChunk);
-    const int blocks = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
-    const size_t smem = sizeof(int) * kWarpsPerCta * c.E;
-    dispatch_count_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.E, nchunks, chunk_cnt);
-    dispatch_scan_kernel<<<1, 256, 0, s>>>(chunk_cnt, nchunks, c.E, cap, cnt_raw, off);
-    dispatch_rank_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.k, c.E, nchunks, chunk_cnt, off,
-                                                                 cap, slot_of, row_token, err);
+    if (n <= kPlanMax) {
+        const size_t smem = sizeof(int) * ((size_t)kPlanWarps * c.E + 2 * c.E + 1);
+        dispatch_plan_kernel<<<1, 32 * kPlanWarps, smem, s>>>(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of,
+                                                               row_token, err);
+    } else {
+        const int nchunks = (int)((n + kChunk - 1) / kChunk);
+        const int blocks = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
+        const size_t smem = sizeof(int) * kWarpsPerCta * c.E;
+        dispatch_count_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.E, nchunks, chunk_cnt);
+        dispatch_scan_kernel<<<1, 256, 0, s>>>(chunk_cnt, nchunks, c.E, cap, cnt_raw, off);
+        dispatch_rank_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.k, c.E, nchunks, chunk_cnt, off,
+                                                                     cap, slot_of, row_token, err);
+    }
     const int elt = c.dtype == MOE_F32 ? 4 : 2;
     const int vecs = c.d * elt / 16;
     gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,

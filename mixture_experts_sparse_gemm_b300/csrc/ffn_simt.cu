@@ -169,14 +169,15 @@ cudaError_t run_down(const moe_config &c, const Sizes &z, const void *H, const v
 
 cudaError_t launch_ffn_up_simt(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                const void *packed, const void *x, void *H, void *Hs, cudaStream_t s) {
-    if (c.dtype == MOE_F32) return run_up<float>(c, z, x_perm, off, packed, x, H, Hs, s);
-    return run_up<__nv_bfloat16>(c, z, x_perm, off, packed, x, H, Hs, s);
+    // fp32 only: bf16 weights are packed as tensor-core tile images for the tcgen05 path
+    if (c.dtype != MOE_F32) return cudaErrorNotSupported;
+    return run_up<float>(c, z, x_perm, off, packed, x, H, Hs, s);
 }
 
 cudaError_t launch_ffn_down_simt(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
                                  const int32_t *off, const void *packed, void *Y, cudaStream_t s) {
-    if (c.dtype == MOE_F32) return run_down<float>(c, z, H, Hs, off, packed, Y, s);
-    return run_down<__nv_bfloat16>(c, z, H, Hs, off, packed, Y, s);
+    if (c.dtype != MOE_F32) return cudaErrorNotSupported;
+    return run_down<float>(c, z, H, Hs, off, packed, Y, s);
 }
 
 }  // namespace moe

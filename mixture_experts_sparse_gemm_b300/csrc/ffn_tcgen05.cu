@@ -24,21 +24,22 @@ cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const voi
     const int64_t mtiles = (z.rows_routed + kBM - 1) / kBM + c.E;
     const int64_t mtiles_s = (shared_rows + kBM - 1) / kBM;
 
-    // H = SiLU(X W1) * (X W3)
-    const bool wide1 = (c.f % 128 == 0) && (!shared || fs % 128 == 0);
-    const int bn1 = wide1 ? 256 : 128;
-    CUtensorMap a0, a1, b0, b1;
+    // H = SiLU(X W1) * (X W3); B = packed [W1|W3] tile images, one bulk copy per stage
+    const int bn1 = up_tile_n(c);
+    const bool wide1 = bn1 == 256;
+    CUtensorMap a0, a1;
     bool ok = make_tmap_bf16(&a0, x_perm, rr, c.d, kBM);
     ok = ok && make_tmap_bf16(&a1, shared ? x : x_perm, shared ? (uint64_t)c.T : rr, c.d, kBM);
-    ok = ok && make_tmap_bf16(&b0, pk + L.w13, (uint64_t)c.E * 2 * c.f, c.d, bn1);
-    ok = ok && make_tmap_bf16(&b1, shared ? pk + L.w13s : pk + L.w13, shared ? (uint64_t)2 * fs : (uint64_t)c.E * 2 * c.f,
-                              c.d, bn1);
     if (!ok) return cudaErrorInvalidValue;
+    const CUtensorMap &b0 = a0, &b1 = a1;   // unused: B is not loaded through tensor maps
     TcArgs g1{};
     g1.g = GroupedShape{off, c.E, shared_rows, 2 * c.f / bn1, shared ? 2 * fs / bn1 : 0};
     g1.K0 = c.d;
     g1.K1 = c.d;
     g1.b_rows0 = 2 * c.f;
+    g1.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w13);
+    g1.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w13s);
+    g1.bt_seg0 = (size_t)2 * c.f * c.d * 2;
     g1.C0 = H;
     g1.C1 = Hs;
     g1.ldc0 = c.f;
@@ -60,20 +61,21 @@ cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const v
     const int64_t mtiles = (z.rows_routed + kBM - 1) / kBM + c.E;
     const int64_t mtiles_s = (shared_rows + kBM - 1) / kBM;
 
-    // Y = H W2
-    const int bn2 = (c.d % 256 == 0) ? 256 : 128;
-    CUtensorMap a0, a1, b0, b1;
+    // Y = H W2; B = packed W2 tile images, one bulk copy per stage
+    const int bn2 = down_tile_n(c);
+    CUtensorMap a0, a1;
     bool ok = make_tmap_bf16(&a0, H, rr, c.f, kBM);
     ok = ok && make_tmap_bf16(&a1, shared ? Hs : H, shared ? (uint64_t)c.T : rr, shared ? fs : c.f, kBM);
-    ok = ok && make_tmap_bf16(&b0, pk + L.w2, (uint64_t)c.E * c.d, c.f, bn2);
-    ok = ok && make_tmap_bf16(&b1, shared ? pk + L.w2s : pk + L.w2, shared ? (uint64_t)c.d : (uint64_t)c.E * c.d,
-                              shared ? fs : c.f, bn2);
     if (!ok) return cudaErrorInvalidValue;
+    const CUtensorMap &b0 = a0, &b1 = a1;   // unused: B is not loaded through tensor maps
     TcArgs g2{};
     g2.g = GroupedShape{off, c.E, shared_rows, c.d / bn2, c.d / bn2};
     g2.K0 = c.f;
     g2.K1 = shared ? fs : c.f;
     g2.b_rows0 = c.d;
+    g2.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w2);
+    g2.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w2s);
+    g2.bt_seg0 = (size_t)c.d * c.f * 2;
     g2.C0 = Y;
     g2.C1 = static_cast<__nv_bfloat16 *>(Y) + (size_t)z.rows_routed * c.d;
     g2.ldc0 = c.d;

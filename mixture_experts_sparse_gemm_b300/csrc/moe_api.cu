@@ -178,7 +178,9 @@ int route_launches(const moe_config &c) {
     const int base = (c.dtype == MOE_BF16 && route_tcgen05_supported(c)) ? route_tcgen05_launches(c) : 1;
     return base + (c.mode == MOE_EXPERT_CHOICE ? 1 : 0);
 }
-int dispatch_launches(const moe_config &c) { return c.mode == MOE_EXPERT_CHOICE ? 2 : 4; }
+int dispatch_launches(const moe_config &c) {
+    return c.mode == MOE_EXPERT_CHOICE ? 2 : dispatch_tc_launches((int64_t)c.T * c.k);
+}
 
 }  // namespace
 

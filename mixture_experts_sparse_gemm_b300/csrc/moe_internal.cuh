@@ -30,6 +30,25 @@ struct Sizes {
 };
 Sizes sizes_of(const moe_config &c);
 
+// N width of the tensor-core tiles of the two expert GEMMs (bf16).  The packed
+// bf16 weights are tiled with the same widths, so pack and GEMM must agree.
+inline int up_tile_n(const moe_config &c) {
+    const int fs = c.n_shared > 0 ? c.n_shared * c.f_shared : 0;
+    return (c.f % 128 == 0 && fs % 128 == 0) ? 256 : 128;
+}
+inline int down_tile_n(const moe_config &c) { return (c.d % 256 == 0) ? 256 : 128; }
+
+// Element offset of (row p, column i) of a [N][K] bf16 operand stored as the
+// tensor-core tile images: tiles of BN rows x 64 columns, N-tile major then
+// K-tile, each tile BN rows of 128 bytes with the 16-byte chunks of row r
+// permuted by chunk ^ (r % 8) -- the 128-byte swizzle a TMA load would apply.
+// One tile is then a single contiguous copy that lands in shared memory
+// exactly as the MMA descriptor expects.
+__host__ __device__ inline size_t tiled_offset(int p, int i, int BN, int K) {
+    const int nb = p / BN, r = p % BN, kb = i / 64, ch = (i % 64) / 8, w = i % 8;
+    return (((size_t)nb * (K / 64) + kb) * BN + r) * 64 + (size_t)((ch ^ (r & 7)) * 8 + w);
+}
+
 // Byte offsets inside the packed weight buffer.
 //   w13 : [E][2f][d]      up-projection, K-major, W1/W3 interleaved in groups of kGroup rows
 //   w2  : [E][d][f]       down-projection, K-major
@@ -61,6 +80,7 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);
 size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
+int dispatch_tc_launches(int64_t assignments);
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
                                int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s);
 cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, const int32_t *slot_of,

@@ -41,6 +41,18 @@ __global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __
     }
 }
 
+template <int EPI>
+cudaError_t launch_route_n(int npad, const CUtensorMap &a0, const CUtensorMap &b0, const TcArgs &g, int64_t tiles,
+                           cudaStream_t s) {
+    switch (npad) {
+        case 16: return launch_gemm<16, EPI>(a0, a0, b0, b0, g, tiles, s);
+        case 32: return launch_gemm<32, EPI>(a0, a0, b0, b0, g, tiles, s);
+        case 64: return launch_gemm<64, EPI>(a0, a0, b0, b0, g, tiles, s);
+        case 128: return launch_gemm<128, EPI>(a0, a0, b0, b0, g, tiles, s);
+        default: return launch_gemm<256, EPI>(a0, a0, b0, b0, g, tiles, s);
+    }
+}
+
 }  // namespace
 
 bool route_tcgen05_supported(const moe_config &c) { return c.dtype == MOE_BF16 && c.E <= kMaxE && c.d % 64 == 0; }
@@ -74,12 +86,12 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
                        c.renormalize};
     g.err = err;
     const int64_t tiles = (c.T + kBM - 1) / kBM;
-    switch (npad) {
-        case 16: return launch_gemm<16, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
-        case 32: return launch_gemm<32, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
-        case 64: return launch_gemm<64, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
-        case 128: return launch_gemm<128, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
-        default: return launch_gemm<256, kEpiRoute>(a0, a0, b0, b0, g, tiles, s);
+    const int kmax = (c.mode == MOE_EXPERT_CHOICE || c.k <= 1) ? 1 : (c.k <= 2 ? 2 : (c.k <= 4 ? 4 : 8));
+    switch (kmax) {
+        case 1: return launch_route_n<kEpiRoute + 1>(npad, a0, b0, g, tiles, s);
+        case 2: return launch_route_n<kEpiRoute + 2>(npad, a0, b0, g, tiles, s);
+        case 4: return launch_route_n<kEpiRoute + 4>(npad, a0, b0, g, tiles, s);
+        default: return launch_route_n<kEpiRoute + 8>(npad, a0, b0, g, tiles, s);
     }
 }
 

@@ -39,7 +39,8 @@ constexpr int kBK = 64;
 constexpr int kThreads = 192;
 constexpr int kEpiSwiGLU = 0;
 constexpr int kEpiStore = 1;
-constexpr int kEpiRoute = 2;
+// router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
+constexpr int kEpiRoute = 10;
 
 template <int BN>
 struct TcCfg {
@@ -66,6 +67,11 @@ struct TcArgs {
     GroupedShape g;
     int K0, K1;        // reduction width, routed / shared
     int b_rows0;       // packed B rows per routed segment
+    // B as tensor-core tile images (tiled_offset layout), one bulk copy per stage;
+    // null: B comes through the tensor maps tmB0 / tmB1 instead
+    const uint8_t *Bt0;   // routed segments, bt_seg0 bytes each
+    const uint8_t *Bt1;   // shared segment
+    size_t bt_seg0;
     void *C0;          // routed output rows (bf16)
     void *C1;          // shared output rows (bf16)
     int ldc0, ldc1;    // output row pitch in elements
@@ -73,33 +79,87 @@ struct TcArgs {
     unsigned *err;
 };
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// SiLU(z) = z / (1 + e^-z) with the fast exponential and division (the result is
+// rounded to bf16 right after; for z < -88 the denominator is inf and SiLU -> -0)
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Router epilogue of one token row (all 32 lanes of the warp take part in the
-// TMEM loads; `valid` says whether this lane's row is a token).
-template <int BN>
-__device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid, int T) {
-    const int E = r.E;
-    constexpr int kChunks = BN / 16;
-    const bool softmax = r.gate == MOE_GATE_SOFTMAX;
-    float mx = -FLT_MAX, inv = 1.f;
-    if (softmax) {
-#pragma unroll 1
-        for (int c = 0; c < kChunks; ++c) {
-            uint32_t v[16];
-            tmem_ld16(taddr + c * 16, v);
-            tmem_ld_wait();
+// Keep the best KMAX (key, index, logit) triples in (key desc, index asc) order.
+// Candidates arrive in ascending index order and only a strictly larger key
+// moves up, so a tie keeps the lower index first.
+template <int KMAX>
+__device__ __forceinline__ void topk_insert(float (&tk)[KMAX], int (&ti)[KMAX], float (&tu)[KMAX], float key, int e,
+                                            float u) {
+    if (key > tk[KMAX - 1]) {
+        tk[KMAX - 1] = key;
+        ti[KMAX - 1] = e;
+        tu[KMAX - 1] = u;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int e = c * 16 + i;
-                if (e < E) mx = fmaxf(mx, __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f));
+        for (int j = KMAX - 1; j > 0; --j) {
+            if (tk[j] > tk[j - 1]) {
+                const float a = tk[j], b = tu[j];
+                const int q = ti[j];
+                tk[j] = tk[j - 1];
+                tu[j] = tu[j - 1];
+                ti[j] = ti[j - 1];
+                tk[j - 1] = a;
+                tu[j - 1] = b;
+                ti[j - 1] = q;
             }
         }
+    }
+}
+
+// Router epilogue of one token row (all 32 lanes of the warp take part in the
+// TMEM loads; `valid` says whether this lane's row is a token).
+//   pass 1: u_e = logit + offset.  Softmax: running max, and the top k on u_e
+//           itself -- softmax is increasing in the logit, so its order, ties
+//           included, is the order of the scores, and fp32 logits resolve it
+//           more finely than fp32 scores would.  Sigmoid: key = score + bias.
+//   pass 2: softmax normaliser sum_e exp(u_e - max).
+//   then the k weights (renormalised when asked), or for Expert Choice every
+//   score written expert-major.
+template <int BN, int KMAX>
+__device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid) {
+    const int E = r.E, T = r.T;
+    constexpr int kChunks = BN / 16;
+    const bool softmax = r.gate == MOE_GATE_SOFTMAX;
+    const bool ec = r.mode == MOE_EXPERT_CHOICE;
+    float tk[KMAX], tu[KMAX];
+    int ti[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        tk[j] = -FLT_MAX;
+        tu[j] = 0.f;
+        ti[j] = 0x7fffffff;
+    }
+    float mx = -FLT_MAX;
+#pragma unroll 1
+    for (int c = 0; c < kChunks; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int e = c * 16 + i;
+            if (e < E) {
+                const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
+                if (softmax) {
+                    mx = fmaxf(mx, u);
+                    if (!ec) topk_insert<KMAX>(tk, ti, tu, u, e, u);
+                } else {
+                    const float s = __fdividef(1.f, 1.f + __expf(-u));
+                    topk_insert<KMAX>(tk, ti, tu, s + (r.sel_bias ? r.sel_bias[e] : 0.f), e, u);
+                }
+            }
+        }
+    }
+    float inv = 1.f;
+    if (softmax) {
         float sum = 0.f;
 #pragma unroll 1
         for (int c = 0; c < kChunks; ++c) {
@@ -109,71 +169,41 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int e = c * 16 + i;
-                if (e < E) sum += expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx);
+                if (e < E) sum += __expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx);
             }
         }
         inv = 1.f / sum;
     }
-    float tk[kMaxK], tp[kMaxK];
-    int ti[kMaxK];
-#pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-        tk[j] = -FLT_MAX;
-        tp[j] = 0.f;
-        ti[j] = 0x7fffffff;
-    }
-    const int k = r.k;
-    const bool ec = r.mode == MOE_EXPERT_CHOICE;
+    if (ec) {
 #pragma unroll 1
-    for (int c = 0; c < kChunks; ++c) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c * 16, v);
-        tmem_ld_wait();
+        for (int c = 0; c < kChunks; ++c) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c * 16, v);
+            tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int e = c * 16 + i;
-            if (e >= E) continue;
-            const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
-            const float p = softmax ? expf(u - mx) * inv : 1.f / (1.f + expf(-u));
-            if (ec) {
-                if (valid) r.scores_t[(size_t)e * T + t] = p;
-                continue;
-            }
-            const float key = p + (r.sel_bias ? r.sel_bias[e] : 0.f);
-            // keep the best kMaxK in (key desc, index asc) order; the first k of
-            // them are the top k.  Experts arrive in ascending order and only a
-            // strictly larger key moves up, so a tie keeps the lower index first.
-            if (key > tk[kMaxK - 1]) {
-                tk[kMaxK - 1] = key;
-                ti[kMaxK - 1] = e;
-                tp[kMaxK - 1] = p;
-#pragma unroll
-                for (int j = kMaxK - 1; j > 0; --j) {
-                    if (tk[j] > tk[j - 1]) {
-                        const float a = tk[j], b = tp[j];
-                        const int q = ti[j];
-                        tk[j] = tk[j - 1];
-                        tp[j] = tp[j - 1];
-                        ti[j] = ti[j - 1];
-                        tk[j - 1] = a;
-                        tp[j - 1] = b;
-                        ti[j - 1] = q;
-                    }
-                }
+            for (int i = 0; i < 16; ++i) {
+                const int e = c * 16 + i;
+                if (e < E && valid)
+                    r.scores_t[(size_t)e * T + t] =
+                        __expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx) * inv;
             }
         }
+        return;
     }
-    if (!ec && valid) {
-        float wsum = 0.f;
+    if (!valid) return;
+    const int k = r.k;
+    float p[KMAX], wsum = 0.f;
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-            if (j < k) wsum += tp[j];
+    for (int j = 0; j < KMAX; ++j) {
+        p[j] = softmax ? __expf(tu[j] - mx) * inv : __fdividef(1.f, 1.f + __expf(-tu[j]));
+        if (j < k) wsum += p[j];
+    }
+    const float scale = r.renorm ? 1.f / wsum : 1.f;
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) {
-            if (j < k) {
-                r.topk_idx[(size_t)t * k + j] = ti[j];
-                r.topk_w[(size_t)t * k + j] = r.renorm ? tp[j] / wsum : tp[j];
-            }
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+            r.topk_idx[(size_t)t * k + j] = ti[j];
+            r.topk_w[(size_t)t * k + j] = p[j] * scale;
         }
     }
 }
@@ -245,6 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int arow = seg_row0[s] + mb * kBM;
                 const int brow = (routed ? s * a.b_rows0 : 0) + nb * BN;
                 const int nk = (routed ? a.K0 : a.K1) / kBK;
+                const uint8_t *bt = nullptr;
+                if (a.Bt0)
+                    bt = (routed ? a.Bt0 + (size_t)s * a.bt_seg0 : a.Bt1) + (size_t)nb * nk * C::kBBytes;
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) {
                         ok = false;
@@ -254,7 +287,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
                     mbar_arrive_expect_tx(fb, C::kStageBytes);
                     tma_load_2d(smem_u32(st), mA, kb * kBK, arow, fb);
-                    tma_load_2d(smem_u32(st + C::kABytes), mB, kb * kBK, brow, fb);
+                    if (bt)
+                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)kb * C::kBBytes, C::kBBytes, fb);
+                    else
+                        tma_load_2d(smem_u32(st + C::kABytes), mB, kb * kBK, brow, fb);
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -348,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int rows = min(kBM, seg_rows[s] - mb * kBM);
             const int grow = seg_row0[s] + mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            if constexpr (EPI == kEpiRoute) {
-                route_epilogue<BN>(a.route, taddr, grow, row < rows, a.route.T);
+            if constexpr (EPI > kEpiRoute) {
+                route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows);
             } else {
                 __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? a.C0 : a.C1);
                 const int ldc = routed ? a.ldc0 : a.ldc1;

@@ -151,6 +151,8 @@ DISPATCH_CASES = [
     (1, 4, 2, 0.0, 0.0, 128, "bf16"),
     (300, 8, 2, 0.01, 0.0, 128, "bf16"),     # capacity 0: every assignment dropped
     (500, 8, 2, 1.25, 1.0, 64, "f32"),
+    (40000, 16, 2, 1.1, 1.0, 128, "bf16"),   # > 65536 assignments: the multi-CTA count/scan/rank path
+    (32768, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 65536: the largest single-CTA plan
 ]
 
 
