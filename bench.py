@@ -141,6 +141,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(v, device=None):
+    """Largest value over the ranks of the default process group (v itself alone)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world, tokens_per_rank, steps, max_ms):
+    """Whole-job tokens/s of `world` replicas that each ran `steps` steps of
+    `tokens_per_rank` tokens, the slowest rank taking `max_ms`."""
+    return world * tokens_per_rank * steps / (max_ms * 1e-3)
+
+
 # ------------------------------------------------------------------------------------ work model
 def work_model(wl, off, E_used):
     """Algorithmic bytes and FLOPs per stage launch (bf16 b = 2 or fp32 b = 4).
@@ -236,12 +252,8 @@ def run_gpu(args):
         if ws_n > 1:
             dist.barrier()
 
-    def max_over_ranks(v):
-        if ws_n == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def slowest(v):
+        return max_over_ranks(v, dev)
 
     # ---- device-resident timed region
     clocks = ClockSampler()
@@ -269,7 +281,7 @@ def run_gpu(args):
         bus = None
     clk = clocks.stop(bus, t_lo, t_hi)
     B.moe_check_device_error(stream)
-    total_ms = max_over_ranks(total_ms)
+    total_ms = slowest(total_ms)
 
     # ---- moe_forward (single entry point), device resident: cross-check
     fw_ws = layer.workspace()
@@ -323,7 +335,7 @@ def run_gpu(args):
     e1.record(s_out)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_ms = slowest(e0.elapsed_time(e1))
     B.moe_check_device_error(stream)
 
     # ---- work model and roofline
@@ -363,7 +375,7 @@ def run_gpu(args):
     layer_bytes = sum(model[s]["bytes"] for s in STAGES)
     layer_flops = sum(model[s]["flops"] for s in ("ffn_up", "ffn_down"))
     layer_roof_ms = max(layer_flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (bw * 1e9)) * 1e3
-    value = ws_n * T * K / (total_ms * 1e-3)
+    value = replica_throughput(ws_n, T, K, total_ms)
     x_bytes = T * d * x.element_size()
     out = {
         "metric": METRIC,
@@ -393,7 +405,7 @@ def run_gpu(args):
         "stages": stage_info,
         "forward_ms": round(fwd_ms, 5),
         "roofline": roof,
-        "e2e": {"value": round(ws_n * T * K / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(replica_throughput(ws_n, T, K, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": T * d * y.element_size(),
                 "ms_per_step": round(e2e_ms / K, 5)},
         "gpu_launches": K * B.moe_launch_count(cfg, B.MOE_STAGE_FORWARD),

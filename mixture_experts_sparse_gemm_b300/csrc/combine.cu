@@ -98,14 +98,23 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
 #pragma unroll
             for (int i = 0; i < Vec<T>::N; ++i) acc[i] = 0.f;
             int i = 0;
-            for (; i + 1 < n; i += 2) {   // two rows in flight
-                const uint4 r0 = a.Y[(size_t)s_row[warp][i] * a.vecs + v];
-                const uint4 r1 = a.Y[(size_t)s_row[warp][i + 1] * a.vecs + v];
-                accumulate<T>(acc, r0, s_w[warp][i]);
-                accumulate<T>(acc, r1, s_w[warp][i + 1]);
+            for (; i + 3 < n; i += 4) {   // four rows in flight, accumulated in slot order
+                uint4 r[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) r[q] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) accumulate<T>(acc, r[q], s_w[warp][i + q]);
             }
-            if (i < n) accumulate<T>(acc, a.Y[(size_t)s_row[warp][i] * a.vecs + v], s_w[warp][i]);
-            if (ys) accumulate<T>(acc, ys[v], 1.f);
+            uint4 r[4];
+            const int rem = n - i;
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+                if (q < rem) r[q] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v];
+            const uint4 rs = ys ? ys[v] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int q = 0; q < 3; ++q)
+                if (q < rem) accumulate<T>(acc, r[q], s_w[warp][i + q]);
+            if (ys) accumulate<T>(acc, rs, 1.f);
             a.y[(size_t)t * a.vecs + v] = pack<T>(acc);
         }
         __syncwarp();

@@ -102,11 +102,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
     }
 }
 
-// The same three steps in one CTA of 32 warps, for up to kPlanMax assignments:
-// pass 1 counts per expert (shared-memory atomics), caps and scans them into
-// off[]; pass 2 walks the assignments in rounds of 32 chunks of 256, each round
-// counting per warp, turning the counts into per-warp bases (carried across
-// rounds), and ranking each warp's chunk in order as dispatch_rank_kernel does.
+// The same three steps in one CTA of 32 warps, for up to kPlanMax assignments.
+// Warp w owns one contiguous segment of the assignments (segments in warp order
+// are assignment order).  Pass 1: each warp counts its segment per expert into
+// its own shared-memory counters.
+// Then thread e turns the 32 per-warp counts of expert e into per-warp rank
+// bases and the raw count; warp 0 caps and scans the counts into off[].  Pass 2:
+// each warp re-reads its segment and ranks it in order from its bases; lanes
+// holding the same expert are found with ballots (warp_peers9).
 constexpr int kPlanWarps = 32;
 constexpr int64_t kPlanMax = 65536;
 
@@ -114,15 +117,29 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
     dispatch_plan_kernel(const int32_t *idx, int n, int k, int E, int cap, int32_t *cnt_raw, int32_t *off,
                          int32_t *slot_of, int32_t *row_token, unsigned *err) {
     extern __shared__ int sm[];
-    int *wcnt = sm;                        // [kPlanWarps][E]
-    int *run = wcnt + kPlanWarps * E;      // [E] running rank base per expert
-    int *offs = run + E;                   // [E + 1]
+    int *wcnt = sm;                        // [kPlanWarps][E]: counts, then rank bases
+    int *offs = wcnt + kPlanWarps * E;     // [E + 1]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int e = tid; e < E; e += blockDim.x) run[e] = 0;
+    const int seg = ((n + kPlanWarps - 1) / kPlanWarps + 31) & ~31;
+    const int a0 = warp * seg, a1 = min(n, a0 + seg);
+    int *my = wcnt + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    __syncwarp();
+    for (int a = a0 + lane; a < a1; a += 32) {   // counts: fire-and-forget shared adds
+        const int e = idx[a];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&my[e], 1);
+    }
     __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-        const int e = idx[i];
-        if ((unsigned)e < (unsigned)E) atomicAdd(&run[e], 1);
+    for (int e = tid; e < E; e += blockDim.x) {   // per-warp bases in segment order
+        int s = 0;
+#pragma unroll
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = s;
+            s += c;
+        }
+        offs[e] = s;   // raw count, scanned below
     }
     __syncthreads();
     if (warp == 0) {   // kept counts and their exclusive scan, 32 experts per step
@@ -131,8 +148,9 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
             const int e = e0 + lane;
             int kept = 0;
             if (e < E) {
-                cnt_raw[e] = run[e];
-                kept = (cap < 0) ? run[e] : min(run[e], cap);
+                const int raw = offs[e];
+                cnt_raw[e] = raw;
+                kept = (cap < 0) ? raw : min(raw, cap);
             }
             int incl = kept;
 #pragma unroll
@@ -146,59 +164,39 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
         if (lane == 0) offs[E] = carry;
     }
     __syncthreads();
-    for (int e = tid; e <= E; e += blockDim.x) {
-        off[e] = offs[e];
-        if (e < E) run[e] = 0;
-    }
-    __syncthreads();
-    int *my = wcnt + warp * E;
-    for (int base = 0; base < n; base += kPlanWarps * kChunk) {
-        const int c0 = base + warp * kChunk;
-        for (int e = lane; e < E; e += 32) my[e] = 0;
-        __syncwarp();
-        for (int i = lane; i < kChunk; i += 32) {
-            const int a = c0 + i;
-            if (a < n) {
-                const int e = idx[a];
-                if ((unsigned)e < (unsigned)E) atomicAdd(&my[e], 1);
-            }
+    for (int e = tid; e <= E; e += blockDim.x) off[e] = offs[e];
+    for (int b = a0; b < a1; b += 128) {
+        int ev[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int a = b + q * 32 + lane;
+            ev[q] = (a < a1) ? idx[a] : -1;
         }
-        __syncthreads();
-        for (int e = tid; e < E; e += blockDim.x) {   // per-warp bases, in chunk order
-            int s = run[e];
-            for (int w = 0; w < kPlanWarps; ++w) {
-                const int c = wcnt[w * E + e];
-                wcnt[w * E + e] = s;
-                s += c;
-            }
-            run[e] = s;
-        }
-        __syncthreads();
-        for (int step = 0; step < kChunk / 32; ++step) {
-            const int a = c0 + step * 32 + lane;
-            const int e_in = (a < n) ? idx[a] : -1;
-            const bool valid = (unsigned)e_in < (unsigned)E;
-            if (a < n && !valid) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int a = b + q * 32 + lane;
+            const bool valid = (unsigned)ev[q] < (unsigned)E;
+            if (a < a1 && !valid) {
                 slot_of[a] = -1;
                 atomicOr(err, kErrBadIndex);
             }
-            const int e = valid ? e_in : -1 - lane;
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            const int e = valid ? ev[q] : 0;
+            const unsigned peers = warp_peers9(valid ? (unsigned)e : 511u);   // invalid lanes group apart
             const int rank_in = __popc(peers & ((1u << lane) - 1u));
-            const int b = valid ? my[e] : 0;
+            const int base = valid ? my[e] : 0;
             __syncwarp();
-            if (valid && rank_in == 0) my[e] = b + __popc(peers);
+            if (valid && rank_in == 0) my[e] = base + __popc(peers);
             __syncwarp();
             if (valid) {
-                const int r = b + rank_in;
+                const int r = base + rank_in;
                 const int slot = (cap < 0 || r < cap) ? offs[e] + r : -1;
                 slot_of[a] = slot;
                 if (slot >= 0) row_token[slot] = a / k;
             }
         }
-        __syncthreads();
     }
 }
+
 
 // x_perm[row] = x[row_token[row]] for row < *rows (read on the device).
 __global__ void __launch_bounds__(256)

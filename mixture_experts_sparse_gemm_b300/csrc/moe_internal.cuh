@@ -118,6 +118,20 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
     return __float2bfloat16_rn(v);
 }
 
+// Lanes of the warp holding the same 9-bit key (key < 512), from nine ballots:
+// a lane matches when it agrees on every bit.  Cheaper than __match_any_sync
+// when a warp holds many distinct keys.
+__device__ __forceinline__ unsigned warp_peers9(unsigned key) {
+    unsigned peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 0; b < 9; ++b) {
+        const bool bit = (key >> b) & 1u;
+        const unsigned vote = __ballot_sync(0xffffffffu, bit);
+        peers &= bit ? vote : ~vote;
+    }
+    return peers;
+}
+
 // Tile table of a grouped problem, built once per CTA in shared memory:
 // tile_start[s] = first tile of segment s (tile_start[S] = total tiles).
 // Segment tiles are ordered N-block-major with the M-block fastest, so the

@@ -200,49 +200,70 @@ cudaError_t launch_typed(const RouteArgs &a, cudaStream_t s) {
 // token indices among those with key == K until cap are taken.  The taken tokens
 // are written in ascending token order with a block-wide ordered compaction.
 constexpr int kEcThreads = 1024;
+constexpr int kEcSmemMaxT = 49152;   // the column stays in shared memory up to this many tokens (192 KB)
 
-__device__ __forceinline__ int block_exclusive_scan_flag(bool flag, int *warp_tot, int &block_total) {
+// Exclusive block-wide prefix sum of one int per thread; `total` gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned b = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(b & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[warp] = __popc(b);
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
         const int nw = blockDim.x >> 5;
-        int v = (lane < nw) ? warp_tot[lane] : 0;
-        int incl = v;
+        const int w = (lane < nw) ? warp_tot[lane] : 0;
+        int wi = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+            const int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
         }
-        if (lane < nw) warp_tot[32 + lane] = incl - v;
-        if (lane == 31) warp_tot[64] = incl;
+        if (lane < nw) warp_tot[32 + lane] = wi - w;
+        if (lane == 31) warp_tot[64] = wi;
     }
     __syncthreads();
-    const int r = warp_tot[32 + warp] + in_warp;
-    block_total = warp_tot[64];
+    const int r = warp_tot[32 + warp] + incl - v;
+    total = warp_tot[64];
     __syncthreads();
     return r;
 }
 
 __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scores_t, int T, int cap,
                                                                  int32_t *ec_tok, float *ec_w) {
+    extern __shared__ unsigned s_col[];   // the expert's column, when it fits
     __shared__ unsigned hist[256];
     __shared__ int warp_tot[65];
     __shared__ unsigned s_digit;
     __shared__ int s_remaining;
     const int e = blockIdx.x;
-    const unsigned *col = reinterpret_cast<const unsigned *>(scores_t + (size_t)e * T);
+    const unsigned *g = reinterpret_cast<const unsigned *>(scores_t + (size_t)e * T);
+    const bool in_smem = T <= kEcSmemMaxT;
+    if (in_smem) {
+        for (int t = threadIdx.x; t < T; t += blockDim.x) s_col[t] = g[t];
+        __syncthreads();
+    }
+    const unsigned *col = in_smem ? s_col : g;
 
     unsigned prefix = 0, mask = 0;
     int remaining = cap;
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        for (int t = threadIdx.x; t < T; t += blockDim.x) {
-            const unsigned u = col[t];
-            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        // scores of one expert share a few exponents, so most keys land in a few
+        // bins: aggregate per warp (one atomic per distinct bin) to avoid serialising
+        for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+            const int t = t0 + threadIdx.x;
+            unsigned bin = 256u;   // no bin
+            if (t < T) {
+                const unsigned u = col[t];
+                if ((u & mask) == prefix) bin = (u >> shift) & 255u;
+            }
+            const unsigned peers = warp_peers9(bin);
+            if (bin < 256u && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
         }
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -265,23 +286,31 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scor
         remaining = s_remaining;
         __syncthreads();
     }
-    const unsigned K = prefix;   // remaining = ties at K still to take
-    int eq_base = 0, out_base = 0;
-    for (int base = 0; base < T; base += blockDim.x) {
-        const int t = base + threadIdx.x;
-        const unsigned u = (t < T) ? col[t] : 0u;
-        const bool gt = (t < T) && u > K;
-        const bool eq = (t < T) && u == K;
-        int eq_tot, sel_tot;
-        const int eq_rank = eq_base + block_exclusive_scan_flag(eq, warp_tot, eq_tot);
-        const bool sel = gt || (eq && eq_rank < remaining);
-        const int pos = out_base + block_exclusive_scan_flag(sel, warp_tot, sel_tot);
-        if (sel && pos < cap) {
-            ec_tok[(size_t)e * cap + pos] = t;
-            ec_w[(size_t)e * cap + pos] = __uint_as_float(u);
+    const unsigned K = prefix;   // the cap-th largest key; `remaining` ties at K are taken
+
+    // ordered compaction: thread i owns tokens [i*per, (i+1)*per), so thread order
+    // is token order; ties at K go to the lowest token indices
+    const int per = (T + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int t0 = threadIdx.x * per, t1 = min(T, t0 + per);
+    int gt = 0, eq = 0;
+    for (int t = t0; t < t1; ++t) {
+        const unsigned u = col[t];
+        gt += u > K;
+        eq += u == K;
+    }
+    int tot;
+    const int eq_before = block_exclusive_scan(eq, warp_tot, tot);
+    const int take_eq = max(0, min(eq, remaining - eq_before));
+    const int pos0 = block_exclusive_scan(gt + take_eq, warp_tot, tot);
+    int p = pos0, te = 0;
+    for (int t = t0; t < t1; ++t) {
+        const unsigned u = col[t];
+        const bool sel = (u > K) || (u == K && te++ < take_eq);
+        if (sel && p < cap) {
+            ec_tok[(size_t)e * cap + p] = t;
+            ec_w[(size_t)e * cap + p] = __uint_as_float(u);
+            ++p;
         }
-        eq_base += eq_tot;
-        out_base += sel_tot;
     }
 }
 
@@ -312,7 +341,10 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
 
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
                              cudaStream_t s) {
-    ec_select_kernel<<<c.E, kEcThreads, 0, s>>>(scores_t, c.T, c.ec_capacity, ec_tok, ec_w);
+    const size_t smem = c.T <= kEcSmemMaxT ? sizeof(unsigned) * (size_t)c.T : 0;
+    cudaError_t err = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ec_select_kernel<<<c.E, kEcThreads, smem, s>>>(scores_t, c.T, c.ec_capacity, ec_tok, ec_w);
     return cudaGetLastError();
 }
 

@@ -91,6 +91,9 @@ EC_CASES = {
     "expert_choice_zipf": WORKLOADS["expert_choice_zipf"],
     "ec_small": WORKLOADS["expert_choice_zipf"].with_(T=1000, d=256, E=16, f=128, ec_capacity=100, name="ec_small"),
     "ec_cap_eq_T": WORKLOADS["expert_choice_zipf"].with_(T=77, d=128, E=4, f=64, ec_capacity=77, name="ec_full"),
+    # a column longer than the select kernel keeps in shared memory (49152 tokens)
+    "ec_long_column": WORKLOADS["expert_choice_zipf"].with_(T=50000, d=128, E=4, f=64, ec_capacity=1000,
+                                                            name="ec_long"),
 }
 
 
