@@ -2,9 +2,12 @@
 """MoE-layer forward benchmark on B300.
 
 One step = one pass of the whole layer (route -> capacity dispatch -> grouped
-SwiGLU experts (up, down) -> combine) over one batch of synthetic tokens, every
-stage called through the C ABI on one CUDA stream, with CUDA events between the
-stages.  Default workload: Switch-style top-1 with capacity factor 1.25, bf16,
+SwiGLU experts (up, down) -> combine) over one batch of synthetic tokens: one
+moe_forward call through the C ABI.  The headline value times K such steps; a
+second loop runs the same layer as separate stage calls with CUDA events
+between them for the per-kernel breakdown and roofline; a third runs
+moe_forward end to end from pinned host buffers.
+Default workload: Switch-style top-1 with capacity factor 1.25, bf16,
 T=8192, d=1024, E=64, d_ff=4096 (its 1.61 GB of expert weights stream through
 HBM every step, so the per-step working set is larger than the 126 MB L2).
 
@@ -39,10 +42,9 @@ from workloads import WORKLOADS, make_inputs  # noqa: E402
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s as % of B300 bf16 peak"
 DEFAULT_WORKLOAD = "switch_top1_cap1.25"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-STAGES = ("route", "dispatch", "ffn_up", "ffn_down", "combine")
+STAGES = ("route", "dispatch", "ffn", "combine")
 KERNEL_SOURCES = {   # files whose content defines each stage's kernels (for the ncu traffic record)
-    "ffn_up": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
-    "ffn_down": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
+    "ffn": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
     "route": ["csrc/route.cu", "csrc/route_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
     "dispatch": ["csrc/dispatch.cu"],
     "combine": ["csrc/combine.cu"],
@@ -173,10 +175,10 @@ def work_model(wl, off, E_used):
                   "flops": 2 * T * d * E}
     m["dispatch"] = {"bytes": (T * wl.k * 4 * 3 if wl.mode == "tc" else E * wl.ec_capacity * 4 + T * E * 4) + 2 * A * d * b,
                      "flops": 0}
-    m["ffn_up"] = {"bytes": touched * 2 * d * f * b + A * d * b + A * f * b + (2 * d * fs * b + Ts * d * b + Ts * fs * b),
-                   "flops": 4 * A * d * f + 4 * Ts * d * fs}
-    m["ffn_down"] = {"bytes": touched * d * f * b + A * f * b + A * d * b + (d * fs * b + Ts * fs * b + Ts * d * b),
-                     "flops": 2 * A * d * f + 2 * Ts * d * fs}
+    # grouped experts (up + down): touched weights, x_perm read, H written and read, Y written
+    m["ffn"] = {"bytes": touched * 3 * d * f * b + 2 * A * d * b + 2 * A * f * b
+                         + (3 * d * fs * b + 2 * Ts * d * b + 2 * Ts * fs * b),
+                "flops": 6 * A * d * f + 6 * Ts * d * fs}
     m["combine"] = {"bytes": A * d * b + T * kslots * 8 + T * d * b + Ts * d * b, "flops": 2 * A * d}
     return m, A, touched
 
@@ -220,13 +222,11 @@ def run_gpu(args):
     cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
     slot_of = torch.empty(slots, dtype=torch.int32, device=dev)
     x_perm = torch.empty(rows_routed, d, dtype=dt, device=dev)
-    H = torch.empty(rows_routed, wl.f, dtype=dt, device=dev)
-    fs = wl.n_shared * wl.f_shared
-    Hs = torch.empty(T, fs, dtype=dt, device=dev) if fs else None
     Y = torch.empty(rows_total, d, dtype=dt, device=dev)
     y = torch.empty(T, d, dtype=dt, device=dev)
     ws_route = layer.workspace(B.MOE_STAGE_ROUTE)
     ws_disp = layer.workspace(B.MOE_STAGE_DISPATCH)
+    ws_ffn = layer.workspace(B.MOE_STAGE_GROUPED_FFN)
     x, Wr, lo, sb = inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]
 
     def step(ev=None):
@@ -238,15 +238,12 @@ def run_gpu(args):
         B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream)
         if ev is not None:
             ev[2].record(stream)
-        B.moe_grouped_ffn_up(cfg, x_perm, off, layer.packed, x, H, Hs, stream)
+        B.moe_grouped_ffn(cfg, x_perm, off, layer.packed, x, Y, ws_ffn, stream)
         if ev is not None:
             ev[3].record(stream)
-        B.moe_grouped_ffn_down(cfg, H, Hs, off, layer.packed, Y, stream)
-        if ev is not None:
-            ev[4].record(stream)
         B.moe_combine(cfg, Y, slot_of, gw, y, None, stream)
         if ev is not None:
-            ev[5].record(stream)
+            ev[4].record(stream)
 
     def barrier():
         if ws_n > 1:
@@ -255,23 +252,38 @@ def run_gpu(args):
     def slowest(v):
         return max_over_ranks(v, dev)
 
-    # ---- device-resident timed region
+    # ---- headline timed region: K layer forwards through moe_forward, inputs resident
+    K = args.steps
+    fw_ws = layer.workspace()
     clocks = ClockSampler()
     for _ in range(args.warmup):
+        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
         step()
     torch.cuda.synchronize()
     B.moe_check_device_error(stream)
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     t_lo = time.time()
-    for i in range(K):
-        step(evs[i])
+    e0.record(stream)
+    for _ in range(K):
+        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
+    e1.record(stream)
     torch.cuda.synchronize()
     t_hi = time.time()
     barrier()
-    total_ms = evs[0][0].elapsed_time(evs[K - 1][5])
+    total_ms = slowest(e0.elapsed_time(e1))
+    B.moe_check_device_error(stream)
+
+    # ---- stage breakdown: the same layer as separate C-ABI stage calls, CUDA events
+    # between them on the launching stream (the roofline of each kernel comes from here)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
+    torch.cuda.synchronize()
+    for i in range(K):
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_hi2 = time.time()
+    staged_ms = evs[0][0].elapsed_time(evs[K - 1][len(STAGES)]) / K
     stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)])) for j, s in enumerate(STAGES)}
     bus = None
     try:
@@ -279,22 +291,8 @@ def run_gpu(args):
         bus = f"{bus:02x}:" if isinstance(bus, int) else None
     except Exception:
         bus = None
-    clk = clocks.stop(bus, t_lo, t_hi)
+    clk = clocks.stop(bus, t_lo, t_hi2)
     B.moe_check_device_error(stream)
-    total_ms = slowest(total_ms)
-
-    # ---- moe_forward (single entry point), device resident: cross-check
-    fw_ws = layer.workspace()
-    for _ in range(args.warmup):
-        layer.forward(x, Wr, lo, sb, out=y, stream=stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(K):
-        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    fwd_ms = e0.elapsed_time(e1) / K
 
     # ---- end to end through the C ABI with host buffers (pinned): every step copies its
     # tokens host -> device, runs moe_forward and copies its output device -> host.  The
@@ -369,11 +367,11 @@ def run_gpu(args):
     roof["algorithmic_bytes_per_launch"] = model[dom]["bytes"]
 
     step_ms = total_ms / K
-    ffn_s = (stage_ms["ffn_up"] + stage_ms["ffn_down"]) * 1e-3
-    gemm_flops = model["ffn_up"]["flops"] + model["ffn_down"]["flops"]
+    ffn_s = stage_ms["ffn"] * 1e-3
+    gemm_flops = model["ffn"]["flops"]
     gemm_tflops = gemm_flops / ffn_s / 1e12
     layer_bytes = sum(model[s]["bytes"] for s in STAGES)
-    layer_flops = sum(model[s]["flops"] for s in ("ffn_up", "ffn_down"))
+    layer_flops = model["ffn"]["flops"]
     layer_roof_ms = max(layer_flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (bw * 1e9)) * 1e3
     value = replica_throughput(ws_n, T, K, total_ms)
     x_bytes = T * d * x.element_size()
@@ -403,7 +401,7 @@ def run_gpu(args):
         "layer_roofline": {"ms": round(layer_roof_ms, 5), "frac": round(layer_roof_ms / step_ms, 4),
                            "bytes_per_step": layer_bytes, "flops_per_step": layer_flops},
         "stages": stage_info,
-        "forward_ms": round(fwd_ms, 5),
+        "staged_ms_per_step": round(staged_ms, 5),
         "roofline": roof,
         "e2e": {"value": round(replica_throughput(ws_n, T, K, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": T * d * y.element_size(),

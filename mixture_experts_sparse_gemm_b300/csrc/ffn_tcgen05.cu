@@ -3,87 +3,130 @@
 //
 // Expert FFN with W1, W3 up and W2 down ("lnwmold.com GPT-4 MoE article" §2.2),
 // read as SwiGLU:  H_e = SiLU(X_e W1_e) * (X_e W3_e),  Y_e = H_e W2_e.
-// Up: A = x_perm rows (shared experts: x), B = packed [W1|W3] groups, K = d,
+// Up: A = x_perm rows (shared experts: x), B = packed [W1|W3] tile images, K = d,
 //     256-wide tiles (128 hidden columns) when f % 128 == 0, else 128-wide.
-// Down: A = H rows, B = packed W2, K = f, 256-wide tiles when d % 256 == 0.
+// Down: A = H rows, B = packed W2 tile images, K = f, 256-wide tiles when d % 256 == 0.
+// Fused: both GEMMs in one persistent launch, down tiles after up tiles, each
+//     down tile waiting (on the device) for the up tiles that produce its H rows.
 #include <algorithm>
 
 #include "tc_gemm.cuh"
 
 namespace moe {
+namespace {
+
+struct FfnMaps {
+    CUtensorMap a0, a1;
+};
+
+// Up projection: A = x_perm (routed) / x (shared), B = [W1|W3] images, C = H / Hs.
+bool up_gemm(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off, const void *packed,
+             const void *x, void *H, void *Hs, TcGemm &G, FfnMaps &m) {
+    const PackedLayout L = packed_layout(c);
+    const char *pk = static_cast<const char *>(packed);
+    const bool shared = c.n_shared > 0;
+    const int fs = z.fs_tot;
+    const int bn = up_tile_n(c);
+    const uint64_t rr = (uint64_t)z.rows_routed;
+    bool ok = make_tmap_bf16(&m.a0, x_perm, rr, c.d, kBM);
+    ok = ok && make_tmap_bf16(&m.a1, shared ? x : x_perm, shared ? (uint64_t)c.T : rr, c.d, kBM);
+    G = TcGemm{};
+    G.g = GroupedShape{off, c.E, shared ? c.T : 0, 2 * c.f / bn, shared ? 2 * fs / bn : 0};
+    G.K0 = c.d;
+    G.K1 = c.d;
+    G.b_rows0 = 2 * c.f;
+    G.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w13);
+    G.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w13s);
+    G.bt_seg0 = (size_t)2 * c.f * c.d * 2;
+    G.img_rows = bn;
+    G.C0 = H;
+    G.C1 = Hs;
+    G.ldc0 = c.f;
+    G.ldc1 = fs;
+    return ok;
+}
+
+// Down projection: A = H (routed) / Hs (shared), B = W2 images, C = Y rows.
+bool down_gemm(const moe_config &c, const Sizes &z, const void *H, const void *Hs, const int32_t *off,
+               const void *packed, void *Y, TcGemm &G, FfnMaps &m) {
+    const PackedLayout L = packed_layout(c);
+    const char *pk = static_cast<const char *>(packed);
+    const bool shared = c.n_shared > 0;
+    const int fs = z.fs_tot;
+    const int bn = down_tile_n(c);
+    const uint64_t rr = (uint64_t)z.rows_routed;
+    bool ok = make_tmap_bf16(&m.a0, H, rr, c.f, kBM);
+    ok = ok && make_tmap_bf16(&m.a1, shared ? Hs : H, shared ? (uint64_t)c.T : rr, shared ? fs : c.f, kBM);
+    G = TcGemm{};
+    G.g = GroupedShape{off, c.E, shared ? c.T : 0, c.d / bn, c.d / bn};
+    G.K0 = c.f;
+    G.K1 = shared ? fs : c.f;
+    G.b_rows0 = c.d;
+    G.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w2);
+    G.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w2s);
+    G.bt_seg0 = (size_t)c.d * c.f * 2;
+    G.img_rows = bn;
+    G.C0 = Y;
+    G.C1 = static_cast<__nv_bfloat16 *>(Y) + (size_t)z.rows_routed * c.d;
+    G.ldc0 = c.d;
+    G.ldc1 = c.d;
+    return ok;
+}
+
+// Upper bound on the M tiles of a launch (real count is known on the device only).
+int64_t max_mtiles(const moe_config &c, const Sizes &z) {
+    return (z.rows_routed + kBM - 1) / kBM + c.E + (c.n_shared > 0 ? (c.T + kBM - 1) / kBM : 0);
+}
+
+}  // namespace
+
+size_t ffn_dep_counters(const moe_config &c) { return (size_t)max_mtiles(c, sizes_of(c)) + 1; }
+
+bool ffn_fused_supported(const moe_config &c) { return up_tile_n(c) == 256 && down_tile_n(c) == 256; }
 
 cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                   const void *packed, const void *x, void *H, void *Hs, unsigned *err,
                                   cudaStream_t s) {
-    const PackedLayout L = packed_layout(c);
-    const char *pk = static_cast<const char *>(packed);
-    const bool shared = c.n_shared > 0;
-    const int shared_rows = shared ? c.T : 0;
-    const int fs = z.fs_tot;
-    const uint64_t rr = (uint64_t)z.rows_routed;
-    const int64_t mtiles = (z.rows_routed + kBM - 1) / kBM + c.E;
-    const int64_t mtiles_s = (shared_rows + kBM - 1) / kBM;
-
-    // H = SiLU(X W1) * (X W3); B = packed [W1|W3] tile images, one bulk copy per stage
-    const int bn1 = up_tile_n(c);
-    const bool wide1 = bn1 == 256;
-    CUtensorMap a0, a1;
-    bool ok = make_tmap_bf16(&a0, x_perm, rr, c.d, kBM);
-    ok = ok && make_tmap_bf16(&a1, shared ? x : x_perm, shared ? (uint64_t)c.T : rr, c.d, kBM);
-    if (!ok) return cudaErrorInvalidValue;
-    const CUtensorMap &b0 = a0, &b1 = a1;   // unused: B is not loaded through tensor maps
-    TcArgs g1{};
-    g1.g = GroupedShape{off, c.E, shared_rows, 2 * c.f / bn1, shared ? 2 * fs / bn1 : 0};
-    g1.K0 = c.d;
-    g1.K1 = c.d;
-    g1.b_rows0 = 2 * c.f;
-    g1.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w13);
-    g1.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w13s);
-    g1.bt_seg0 = (size_t)2 * c.f * c.d * 2;
-    g1.C0 = H;
-    g1.C1 = Hs;
-    g1.ldc0 = c.f;
-    g1.ldc1 = fs;
-    g1.err = err;
-    const int64_t tiles1 = mtiles * g1.g.nblk_routed + mtiles_s * g1.g.nblk_shared;
-    return wide1 ? launch_gemm<256, kEpiSwiGLU>(a0, a1, b0, b1, g1, tiles1, s)
-                 : launch_gemm<128, kEpiSwiGLU>(a0, a1, b0, b1, g1, tiles1, s);
+    TcArgs g{};
+    FfnMaps m;
+    if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], m)) return cudaErrorInvalidValue;
+    g.err = err;
+    const int64_t tiles = max_mtiles(c, z) * std::max(g.p[0].g.nblk_routed, g.p[0].g.nblk_shared);
+    return g.p[0].img_rows == 256 ? launch_gemm<256, kEpiSwiGLU>(m.a0, m.a1, m.a0, m.a1, g, tiles, s)
+                                  : launch_gemm<128, kEpiSwiGLU>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
 }
 
 cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
-                                    const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s) {
-    const PackedLayout L = packed_layout(c);
-    const char *pk = static_cast<const char *>(packed);
-    const bool shared = c.n_shared > 0;
-    const int shared_rows = shared ? c.T : 0;
-    const int fs = z.fs_tot;
-    const uint64_t rr = (uint64_t)z.rows_routed;
-    const int64_t mtiles = (z.rows_routed + kBM - 1) / kBM + c.E;
-    const int64_t mtiles_s = (shared_rows + kBM - 1) / kBM;
+                                    const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s,
+                                    const int32_t *row_token, const float *row_gate) {
+    TcArgs g{};
+    FfnMaps m;
+    if (!down_gemm(c, z, H, Hs, off, packed, Y, g.p[0], m)) return cudaErrorInvalidValue;
+    g.err = err;
+    g.gated = row_token != nullptr;
+    g.row_token = row_token;
+    g.row_gate = row_gate;
+    const int64_t tiles = max_mtiles(c, z) * g.p[0].g.nblk_routed;
+    return g.p[0].img_rows == 256 ? launch_gemm<256, kEpiStore>(m.a0, m.a1, m.a0, m.a1, g, tiles, s)
+                                  : launch_gemm<128, kEpiStore>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
+}
 
-    // Y = H W2; B = packed W2 tile images, one bulk copy per stage
-    const int bn2 = down_tile_n(c);
-    CUtensorMap a0, a1;
-    bool ok = make_tmap_bf16(&a0, H, rr, c.f, kBM);
-    ok = ok && make_tmap_bf16(&a1, shared ? Hs : H, shared ? (uint64_t)c.T : rr, shared ? fs : c.f, kBM);
-    if (!ok) return cudaErrorInvalidValue;
-    const CUtensorMap &b0 = a0, &b1 = a1;   // unused: B is not loaded through tensor maps
-    TcArgs g2{};
-    g2.g = GroupedShape{off, c.E, shared_rows, c.d / bn2, c.d / bn2};
-    g2.K0 = c.f;
-    g2.K1 = shared ? fs : c.f;
-    g2.b_rows0 = c.d;
-    g2.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w2);
-    g2.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w2s);
-    g2.bt_seg0 = (size_t)c.d * c.f * 2;
-    g2.C0 = Y;
-    g2.C1 = static_cast<__nv_bfloat16 *>(Y) + (size_t)z.rows_routed * c.d;
-    g2.ldc0 = c.d;
-    g2.ldc1 = c.d;
-    g2.err = err;
-    const int64_t tiles2 = (mtiles + mtiles_s) * (c.d / bn2);
-    return bn2 == 256 ? launch_gemm<256, kEpiStore>(a0, a1, b0, b1, g2, tiles2, s)
-                      : launch_gemm<128, kEpiStore>(a0, a1, b0, b1, g2, tiles2, s);
+cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                                     const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
+                                     unsigned *err, cudaStream_t s, const int32_t *row_token, const float *row_gate) {
+    TcArgs g{};
+    FfnMaps mu, md;
+    if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], mu)) return cudaErrorInvalidValue;
+    if (!down_gemm(c, z, H, Hs, off, packed, Y, g.p[1], md)) return cudaErrorInvalidValue;
+    g.dep = dep;
+    g.err = err;
+    g.gated = row_token != nullptr;
+    g.row_token = row_token;
+    g.row_gate = row_gate;
+    cudaError_t e = cudaMemsetAsync(dep, 0, sizeof(int) * ffn_dep_counters(c), s);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = max_mtiles(c, z) * (g.p[0].g.nblk_routed + g.p[1].g.nblk_routed);
+    return launch_gemm<256, kEpiFfn>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
 }
 
 }  // namespace moe

@@ -97,8 +97,11 @@ DispatchWs dispatch_ws(const moe_config &c) {
     return w;
 }
 
+// the two expert GEMMs run as one persistent launch when both use 256-wide tiles
+bool ffn_fused(const moe_config &c) { return c.dtype == MOE_BF16 && ffn_fused_supported(c); }
+
 struct FfnWs {
-    size_t H, Hs, total;
+    size_t H, Hs, dep, total;
 };
 FfnWs ffn_ws(const moe_config &c) {
     const Sizes z = sizes_of(c);
@@ -106,6 +109,7 @@ FfnWs ffn_ws(const moe_config &c) {
     FfnWs w{};
     w.H = k.take((size_t)z.rows_routed * c.f * z.elt);
     w.Hs = k.take((size_t)(c.n_shared > 0 ? c.T : 0) * z.fs_tot * z.elt);
+    w.dep = k.take(ffn_fused(c) ? sizeof(int) * ffn_dep_counters(c) : 0);
     w.total = k.off;
     return w;
 }
@@ -165,6 +169,9 @@ moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, c
     const Sizes z = sizes_of(c);
     void *H = ws + L.H;
     void *Hs = ws + L.Hs;
+    if (ffn_fused(c))
+        return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, x, H, Hs, Y,
+                                                  reinterpret_cast<int *>(ws + L.dep), err, s));
     cudaError_t e = (c.dtype == MOE_BF16) ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
                                           : launch_ffn_up_simt(c, z, x_perm, off, packed, x, H, Hs, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -180,6 +187,12 @@ int route_launches(const moe_config &c) {
 }
 int dispatch_launches(const moe_config &c) {
     return c.mode == MOE_EXPERT_CHOICE ? 2 : dispatch_tc_launches((int64_t)c.T * c.k);
+}
+
+// moe_forward folds the combine into the down GEMM when every token has one
+// expert and there are no shared experts (the row -> token map is a permutation)
+bool gated_down(const moe_config &c) {
+    return c.dtype == MOE_BF16 && c.mode == MOE_TOKEN_CHOICE && c.k == 1 && c.n_shared == 0;
 }
 
 }  // namespace
@@ -467,9 +480,13 @@ moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *ker
     switch (stage) {
         case MOE_STAGE_ROUTE: *kernels = empty ? 0 : route_launches(c); break;
         case MOE_STAGE_DISPATCH: *kernels = empty ? 0 : dispatch_launches(c); break;
-        case MOE_STAGE_GROUPED_FFN: *kernels = empty ? 0 : 2; break;
+        case MOE_STAGE_GROUPED_FFN: *kernels = empty ? 0 : (ffn_fused(c) ? 1 : 2); break;
         case MOE_STAGE_COMBINE: *kernels = empty ? 0 : 1; break;
-        case MOE_STAGE_FORWARD: *kernels = empty ? 0 : route_launches(c) + dispatch_launches(c) + 2 + 1; break;
+        case MOE_STAGE_FORWARD:
+            *kernels = empty ? 0
+                             : route_launches(c) + dispatch_launches(c) + (ffn_fused(c) ? 1 : 2) +
+                                   (gated_down(c) ? 0 : 1);
+            break;
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
@@ -518,6 +535,22 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, co
     if (st != MOE_OK) return st;
     st = do_dispatch(c, idx, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s);
     if (st != MOE_OK) return st;
+    if (gated_down(c)) {
+        // one expert per token and no shared experts: the down GEMM writes each row
+        // straight to its token's output, scaled by the gate; dropped tokens stay 0
+        const Sizes z = sizes_of(c);
+        const FfnWs F = ffn_ws(c);
+        const int32_t *row_token = reinterpret_cast<const int32_t *>(w + L.dispatch + dispatch_ws(c).row_token);
+        if (cudaMemsetAsync(y, 0, (size_t)c.T * c.d * z.elt, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (ffn_fused(c))
+            return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, x, w + L.ffn + F.H, nullptr, y,
+                                                      reinterpret_cast<int *>(w + L.ffn + F.dep), err, s, row_token,
+                                                      gw));
+        cudaError_t e = launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, w + L.ffn + F.H, nullptr, err, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+        return from_cuda(launch_ffn_down_tcgen05(c, z, w + L.ffn + F.H, nullptr, off, packed, y, err, s, row_token,
+                                                 gw));
+    }
     st = do_ffn(c, x_perm, off, packed, x, Y, w + L.ffn, err, s);
     if (st != MOE_OK) return st;
     return from_cuda(launch_combine(c, sizes_of(c), Y, slot_of, gw, y, s));

@@ -95,8 +95,22 @@ cudaError_t launch_ffn_down_simt(const moe_config &c, const Sizes &z, const void
 cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                   const void *packed, const void *x, void *H, void *Hs, unsigned *err,
                                   cudaStream_t s);
+// With row_token/row_gate (token choice, k == 1, no shared experts) the combine is
+// folded into the epilogue: Y is the layer output y[T][d] and row r is written to
+// y[row_token[r]] scaled by row_gate[row_token[r]]; rows of dropped tokens are
+// not written (the caller zeroes y first).
 cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
-                                    const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s);
+                                    const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s,
+                                    const int32_t *row_token = nullptr, const float *row_gate = nullptr);
+// Both expert GEMMs in one persistent (cooperative) launch: up tiles, then down tiles,
+// each waiting for the up tiles of its rows through `dep` (ffn_dep_counters ints,
+// zeroed here).  Needs 256-wide tiles for both (ffn_fused_supported).
+cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
+                                     const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
+                                     unsigned *err, cudaStream_t s, const int32_t *row_token = nullptr,
+                                     const float *row_gate = nullptr);
+size_t ffn_dep_counters(const moe_config &c);
+bool ffn_fused_supported(const moe_config &c);
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r,
                                  const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
                                  float *topk_w, float *scores_t, void *wr_t, unsigned *err,

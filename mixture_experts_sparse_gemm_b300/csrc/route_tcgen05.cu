@@ -78,10 +78,10 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
     ok = ok && make_tmap_bf16(&b0, wt, (uint64_t)npad, c.d, npad);
     if (!ok) return cudaErrorInvalidValue;
     TcArgs g{};
-    g.g = GroupedShape{seg, 1, 0, 1, 0};
-    g.K0 = c.d;
-    g.K1 = c.d;
-    g.b_rows0 = npad;
+    g.p[0].g = GroupedShape{seg, 1, 0, 1, 0};
+    g.p[0].K0 = c.d;
+    g.p[0].K1 = c.d;
+    g.p[0].b_rows0 = npad;
     g.route = RouteEpi{logit_offset, sel_bias, topk_idx, topk_w, scores_t, c.T, c.E, c.k, c.gate, c.mode,
                        c.renormalize};
     g.err = err;

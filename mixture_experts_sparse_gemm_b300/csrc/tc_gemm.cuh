@@ -37,8 +37,9 @@ using namespace tc;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kThreads = 192;
-constexpr int kEpiSwiGLU = 0;
-constexpr int kEpiStore = 1;
+constexpr int kEpiSwiGLU = 0;   // up projection (+ SwiGLU)
+constexpr int kEpiStore = 1;    // down projection (optionally gated, see TcArgs::gated)
+constexpr int kEpiFfn = 2;      // both: up tiles, then down tiles, in one persistent launch
 // router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
 constexpr int kEpiRoute = 10;
 
@@ -50,7 +51,7 @@ struct TcCfg {
     static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kMiscBytes = 64 + sizeof(int) * (3 * (kMaxE + 2));
+    static constexpr int kMiscBytes = 64 + sizeof(int) * (5 * (kMaxE + 2));
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kMiscBytes;
 };
 
@@ -63,18 +64,33 @@ struct RouteEpi {
     int T, E, k, gate, mode, renorm;
 };
 
-struct TcArgs {
+// One grouped GEMM over the segments: segment s < E is routed expert s (rows
+// off[s]..off[s+1] of A and C), segment E (shared_rows > 0) the merged shared experts.
+struct TcGemm {
     GroupedShape g;
     int K0, K1;        // reduction width, routed / shared
-    int b_rows0;       // packed B rows per routed segment
+    int b_rows0;       // B rows per routed segment (tensor-map B)
     // B as tensor-core tile images (tiled_offset layout), one bulk copy per stage;
     // null: B comes through the tensor maps tmB0 / tmB1 instead
     const uint8_t *Bt0;   // routed segments, bt_seg0 bytes each
     const uint8_t *Bt1;   // shared segment
     size_t bt_seg0;
-    void *C0;          // routed output rows (bf16)
-    void *C1;          // shared output rows (bf16)
-    int ldc0, ldc1;    // output row pitch in elements
+    int img_rows;         // rows of one packed tile image (BN or a multiple: a BN tile is a slice of it)
+    void *C0;             // routed output rows (bf16)
+    void *C1;             // shared output rows (bf16)
+    int ldc0, ldc1;       // output row pitch in elements
+};
+
+struct TcArgs {
+    TcGemm p[2];          // p[1]: the down projection of a kEpiFfn launch
+    // kEpiFfn: dep[mtile_start(s) + mb] counts the finished up tiles of (segment, M
+    // tile); a down tile waits until all of them are done (zeroed before the launch)
+    int *dep;
+    // down projection with the combine of one expert per token folded in: routed row
+    // r is token t = row_token[r] and goes to C0[t] scaled by row_gate[t]
+    int gated;
+    const int32_t *row_token;
+    const float *row_gate;
     RouteEpi route;
     unsigned *err;
 };
@@ -208,12 +224,68 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
     }
 }
 
+// Tile epilogues (all 32 lanes of each epilogue warp run them; `row` is the
+// thread's accumulator row, `rows` the valid rows of the tile).
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, int ldc, int grow, int row, int rows,
+                                           int nb) {
+#pragma unroll 1
+    for (int grp = 0; grp < BN / 128; ++grp) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t g[16], u[16];
+            tmem_ld16(taddr + grp * 128 + c * 16, g);
+            tmem_ld16(taddr + grp * 128 + 64 + c * 16, u);
+            tmem_ld_wait();
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                o[i] = pack_bf16x2(h0, h1);
+            }
+            if (row < rows) {
+                uint4 *dst = reinterpret_cast<uint4 *>(Cp + (size_t)grow * ldc + nb * (BN / 2) + grp * 64 + c * 16);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        }
+    }
+}
+
+template <int BN>
+__device__ __forceinline__ void epi_store(uint32_t taddr, __nv_bfloat16 *Cp, int ldc, size_t orow, float scale, int row,
+                                          int rows, int nb) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
+        tmem_ld_wait();
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            o[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * scale, __uint_as_float(v[2 * i + 1]) * scale);
+        if (row < rows) {
+            uint4 *dst = reinterpret_cast<uint4 *>(Cp + orow * ldc + nb * BN + c * 16);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+    }
+}
+
+// Where a tile lives: phase (GEMM of a kEpiFfn launch), segment, M and N block.
+struct TileAt {
+    int phase, s, mb, nb;
+};
+
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                           const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
                            TcArgs a) {
     using C = TcCfg<BN>;
+    constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
@@ -225,9 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = tempty + 2;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    int *tile_start = reinterpret_cast<int *>(tmem_holder + 16);
-    int *seg_row0 = tile_start + (kMaxE + 2);
+    int *tile_start0 = reinterpret_cast<int *>(tmem_holder + 16);   // tiles of phase 0 per segment
+    int *tile_start1 = tile_start0 + (kMaxE + 2);                   // tiles of phase 1 per segment
+    int *seg_row0 = tile_start1 + (kMaxE + 2);
     int *seg_rows = seg_row0 + (kMaxE + 2);
+    int *mtile_start = seg_rows + (kMaxE + 2);                      // first M tile of each segment
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -245,8 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbarrier_init();
         prefetch_tmap(&tmA0);
         prefetch_tmap(&tmA1);
-        prefetch_tmap(&tmB0);
-        prefetch_tmap(&tmB1);
+        if (a.p[0].Bt0 == nullptr) {
+            prefetch_tmap(&tmB0);
+            prefetch_tmap(&tmB1);
+        }
+        if (kPhases == 2) {
+            prefetch_tmap(&tmA2);
+            prefetch_tmap(&tmA3);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
@@ -256,8 +336,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    const int S = build_tile_table<kBM>(a.g, tile_start, seg_row0, seg_rows);
-    const int total = tile_start[S];
+    const int S = build_tile_table<kBM>(a.p[0].g, tile_start0, seg_row0, seg_rows);
+    const int total0 = tile_start0[S];
+    int total = total0;
+    if (kPhases == 2) {
+        if (threadIdx.x == 0) {
+            int t1 = 0, m = 0;
+            for (int s = 0; s < S; ++s) {
+                const int mblk = (seg_rows[s] + kBM - 1) / kBM;
+                tile_start1[s] = t1;
+                mtile_start[s] = m;
+                t1 += mblk * ((s < a.p[1].g.E) ? a.p[1].g.nblk_routed : a.p[1].g.nblk_shared);
+                m += mblk;
+            }
+            tile_start1[S] = t1;
+            mtile_start[S] = m;
+        }
+        __syncthreads();
+        total += tile_start1[S];
+    }
+    auto locate = [&](int tile) {
+        TileAt t;
+        if (kPhases == 2 && tile >= total0) {
+            t.phase = 1;
+            decode_tile<kBM>(a.p[1].g, tile_start1, seg_rows, S, tile - total0, t.s, t.mb, t.nb);
+        } else {
+            t.phase = 0;
+            decode_tile<kBM>(a.p[0].g, tile_start0, seg_rows, S, tile, t.s, t.mb, t.nb);
+        }
+        return t;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -267,17 +375,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             int issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                int s, mb, nb;
-                decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
-                const bool routed = s < a.g.E;
-                const CUtensorMap *mA = routed ? &tmA0 : &tmA1;
+                const TileAt t = locate(tile);
+                const TcGemm &G = a.p[t.phase];
+                const bool routed = t.s < G.g.E;
+                if (kPhases == 2 && t.phase == 1) {
+                    // H rows of this (segment, M tile) come from the up tiles: wait until all
+                    // of them have published (release/acquire through dep), bounded
+                    const int need = routed ? a.p[0].g.nblk_routed : a.p[0].g.nblk_shared;
+                    const int *cnt = a.dep + mtile_start[t.s] + t.mb;
+                    const uint64_t t0 = globaltimer();
+                    for (uint32_t i = 0;; ++i) {
+                        int v;
+                        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+                        if (v >= need) break;
+                        if ((i & 15u) == 0 && (*abort_flag || globaltimer() - t0 > kWaitLimitNs)) {
+                            if (!*abort_flag) atomicOr(a.err, kErrWaitTimeout);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (!ok) break;
+                    asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> TMA reads
+                }
+                const CUtensorMap *mA = (t.phase == 0) ? (routed ? &tmA0 : &tmA1) : (routed ? &tmA2 : &tmA3);
                 const CUtensorMap *mB = routed ? &tmB0 : &tmB1;
-                const int arow = seg_row0[s] + mb * kBM;
-                const int brow = (routed ? s * a.b_rows0 : 0) + nb * BN;
-                const int nk = (routed ? a.K0 : a.K1) / kBK;
+                const int arow = seg_row0[t.s] + t.mb * kBM;
+                const int brow = (routed ? t.s * G.b_rows0 : 0) + t.nb * BN;
+                const int nk = (routed ? G.K0 : G.K1) / kBK;
                 const uint8_t *bt = nullptr;
-                if (a.Bt0)
-                    bt = (routed ? a.Bt0 + (size_t)s * a.bt_seg0 : a.Bt1) + (size_t)nb * nk * C::kBBytes;
+                size_t img_bytes = 0;
+                if (G.Bt0) {
+                    // rows [nb*BN, nb*BN + BN) of the N dimension are slice `sub` of image `img`;
+                    // image rows are stored consecutively, so a slice is contiguous too
+                    const int per = G.img_rows / BN, img = t.nb / per, sub = t.nb % per;
+                    img_bytes = (size_t)G.img_rows * kBK * 2;
+                    bt = (routed ? G.Bt0 + (size_t)t.s * G.bt_seg0 : G.Bt1) + (size_t)img * nk * img_bytes +
+                         (size_t)sub * C::kBBytes;
+                }
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) {
                         ok = false;
@@ -288,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(fb, C::kStageBytes);
                     tma_load_2d(smem_u32(st), mA, kb * kBK, arow, fb);
                     if (bt)
-                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)kb * C::kBBytes, C::kBBytes, fb);
+                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)kb * img_bytes, C::kBBytes, fb);
                     else
                         tma_load_2d(smem_u32(st + C::kABytes), mB, kb * kBK, brow, fb);
                     ++issued;
@@ -324,9 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-                int s, mb, nb;
-                decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
-                const int nk = ((s < a.g.E) ? a.K0 : a.K1) / kBK;
+                const TileAt t = locate(tile);
+                const TcGemm &G = a.p[t.phase];
+                const int nk = ((t.s < G.g.E) ? G.K0 : G.K1) / kBK;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err)) {
@@ -371,8 +506,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;
         int it = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-            int s, mb, nb;
-            decode_tile<kBM>(a.g, tile_start, seg_rows, S, tile, s, mb, nb);
+            const TileAt t = locate(tile);
+            const TcGemm &G = a.p[t.phase];
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             int ok = 1;
@@ -380,60 +515,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             fence_after();
-            const bool routed = s < a.g.E;
-            const int rows = min(kBM, seg_rows[s] - mb * kBM);
-            const int grow = seg_row0[s] + mb * kBM + row;
+            const bool routed = t.s < G.g.E;
+            const int rows = min(kBM, seg_rows[t.s] - t.mb * kBM);
+            const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI > kEpiRoute) {
                 route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows);
             } else {
-                __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? a.C0 : a.C1);
-                const int ldc = routed ? a.ldc0 : a.ldc1;
-                if constexpr (EPI == kEpiSwiGLU) {
-#pragma unroll 1
-                    for (int grp = 0; grp < BN / 128; ++grp) {
-#pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t g[16], u[16];
-                            tmem_ld16(taddr + grp * 128 + c * 16, g);
-                            tmem_ld16(taddr + grp * 128 + 64 + c * 16, u);
-                            tmem_ld_wait();
-                            uint32_t o[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                                const float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                                o[i] = pack_bf16x2(h0, h1);
-                            }
-                            if (row < rows) {
-                                uint4 *dst = reinterpret_cast<uint4 *>(Cp + (size_t)grow * ldc + nb * (BN / 2) +
-                                                                       grp * 64 + c * 16);
-                                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                            }
-                        }
-                    }
+                __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? G.C0 : G.C1);
+                const int ldc = routed ? G.ldc0 : G.ldc1;
+                const bool up = (EPI == kEpiSwiGLU) || (EPI == kEpiFfn && t.phase == 0);
+                if (up) {
+                    epi_swiglu<BN>(taddr, Cp, ldc, grow, row, rows, t.nb);
                 } else {
-#pragma unroll 1
-                    for (int c = 0; c < BN / 16; ++c) {
-                        uint32_t v[16];
-                        tmem_ld16(taddr + c * 16, v);
-                        tmem_ld_wait();
-                        uint32_t o[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            o[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        if (row < rows) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(Cp + (size_t)grow * ldc + nb * BN + c * 16);
-                            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                        }
+                    size_t orow = (size_t)grow;
+                    float scale = 1.f;
+                    if (a.gated && routed && row < rows) {
+                        const int tok = a.row_token[grow];
+                        orow = (size_t)tok;
+                        scale = a.row_gate[tok];
                     }
+                    epi_store<BN>(taddr, Cp, ldc, orow, scale, row, rows, t.nb);
                 }
             }
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+            if (EPI == kEpiFfn && t.phase == 0 && warp == 2 && lane == 0) {
+                // publish this up tile's H rows to the down tiles (any CTA) that read them:
+                // the phase of tempty[acc] completes once all four epilogue warps have
+                // stored their rows (this warp cannot fall a phase behind: the next one
+                // needs its own arrival), then a GPU-scope release of the counter
+                if (wait_bounded(smem_u32(&tempty[acc]), acc_phase, abort_flag, a.err)) {
+                    __threadfence();
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    int *cnt = a.dep + mtile_start[t.s] + t.mb;
+                    asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
+                }
+            }
         }
     }
 
@@ -445,17 +564,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Persistent launch: one CTA per SM (at most max_tiles).  A kEpiFfn launch has CTAs
+// waiting on other CTAs' up tiles, so it is a cooperative launch (all CTAs resident).
 template <int BN, int EPI>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const TcArgs &args, int64_t max_tiles, cudaStream_t s) {
+                        const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args, int64_t max_tiles,
+                        cudaStream_t s) {
     auto kern = tc_grouped_gemm_kernel<BN, EPI>;
     const size_t smem = TcCfg<BN>::kSmem;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int grid = num_sms();
     if (max_tiles < grid) grid = (int)(max_tiles > 1 ? max_tiles : 1);
-    kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, args);
+    if (EPI == kEpiFfn) {
+        TcArgs targs = args;
+        void *params[] = {const_cast<CUtensorMap *>(&a0), const_cast<CUtensorMap *>(&a1),
+                          const_cast<CUtensorMap *>(&b0), const_cast<CUtensorMap *>(&b1),
+                          const_cast<CUtensorMap *>(&a2), const_cast<CUtensorMap *>(&a3), &targs};
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kThreads), params,
+                                           smem, s);
+    }
+    kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, a2, a3, args);
     return cudaGetLastError();
+}
+
+// Single-GEMM launches pass their A maps again for the unused second phase.
+template <int BN, int EPI>
+cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
+                        const TcArgs &args, int64_t max_tiles, cudaStream_t s) {
+    return launch_gemm<BN, EPI>(a0, a1, b0, b1, a0, a1, args, max_tiles, s);
 }
 
 }  // namespace
