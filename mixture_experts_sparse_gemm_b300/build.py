@@ -37,9 +37,9 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src, extra):
+def _compile(src, extra, force=False):
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    if _stale(obj, [src] + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))):
+    if force or _stale(obj, [src] + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))):
         cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -55,7 +55,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
         return LIB
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), _sources()))
+        objs = list(ex.map(lambda s: _compile(s, extra, force), _sources()))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -76,6 +76,10 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
                               float *topk_w, float *scores_t, unsigned *err, cudaStream_t s);
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
                              cudaStream_t s);
+// scoring + selection from split-K partial logits partial[splits][T][npad] (fp32)
+cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
+                                int32_t *topk_idx, float *topk_w, float *scores_t, const float *partial, int splits,
+                                int npad, cudaStream_t s);
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);

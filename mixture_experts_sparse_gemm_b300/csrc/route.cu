@@ -33,6 +33,96 @@ struct RouteArgs {
     float *scores_t;   // expert choice: [E][T]
 };
 
+constexpr int kPerLane = kMaxE / 32;   // experts per lane, the most a warp holds
+
+// Scores and selection of one token by one warp.  u[i] is the logit (offset
+// included) of expert lane + 32 i, -FLT_MAX past E.  Softmax (max and sum by warp
+// reduction) or sigmoid; Expert Choice writes the scores expert-major; token
+// choice takes k rounds of a warp arg-max on (key desc, index asc) over the keys
+// score + selection bias, so slots come out in descending key order with ties to
+// the lower expert index, and writes indices and (renormalised) weights.
+template <int KPL>
+__device__ __forceinline__ void warp_score_select(const RouteArgs &a, const float (&u)[KPL], int t, int lane) {
+    constexpr int kPerLane = KPL;
+    const int E = a.E;
+    float p[kPerLane];
+    if (a.gate == MOE_GATE_SIGMOID) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) p[i] = 1.f / (1.f + expf(-u[i]));
+    } else {
+        float mx = -FLT_MAX;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) mx = fmaxf(mx, u[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            p[i] = (e < E) ? expf(u[i] - mx) : 0.f;
+            sum += p[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float inv = 1.f / sum;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) p[i] *= inv;
+    }
+
+    if (a.mode == MOE_EXPERT_CHOICE) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) a.scores_t[(size_t)e * a.T + t] = p[i];
+        }
+        return;
+    }
+
+    float key[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = (e < E) ? p[i] + (a.sel_bias ? a.sel_bias[e] : 0.f) : -FLT_MAX;
+    }
+    unsigned chosen = 0;     // bit i: expert lane + 32 i already selected
+    float wsum = 0.f, wj = 0.f;
+    int ij = 0;
+    for (int j = 0; j < a.k; ++j) {
+        float bk = -FLT_MAX, bp = 0.f;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !(chosen >> i & 1u) && key[i] > bk) {   // ascending e: ties keep the lower
+                bk = key[i];
+                bi = e;
+                bp = p[i];
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            const float op = __shfl_xor_sync(0xffffffffu, bp, o);
+            if (ok > bk || (ok == bk && oi < bi)) {
+                bk = ok;
+                bi = oi;
+                bp = op;
+            }
+        }
+        if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
+        wsum += bp;
+        if (lane == j) {
+            ij = bi;
+            wj = bp;
+        }
+    }
+    if (lane < a.k) {
+        a.topk_idx[(size_t)t * a.k + lane] = ij;
+        a.topk_w[(size_t)t * a.k + lane] = a.renorm ? wj / wsum : wj;
+    }
+}
+
 template <typename Tin, int NPT>
 __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
     extern __shared__ float smem[];
@@ -84,90 +174,42 @@ __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
     __syncthreads();
 
     const int warp = tid >> 5, lane = tid & 31;
-    constexpr int kPerLane = kMaxE / 32;
     for (int m = warp; m < kTM; m += kThreads / 32) {
         const int t = t0 + m;
         if (t >= a.T) break;
-        float u[kPerLane], p[kPerLane];
-        float mx = -FLT_MAX;
+        float u[kPerLane];
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) {
             const int e = lane + 32 * i;
             u[i] = (e < E) ? lg[m * E + e] : -FLT_MAX;
-            mx = fmaxf(mx, u[i]);
         }
-        if (a.gate == MOE_GATE_SIGMOID) {
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i) p[i] = 1.f / (1.f + expf(-u[i]));
-        } else {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int e = lane + 32 * i;
-                p[i] = (e < E) ? expf(u[i] - mx) : 0.f;
-                sum += p[i];
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            const float inv = 1.f / sum;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i) p[i] *= inv;
-        }
+        warp_score_select<kPerLane>(a, u, t, lane);
+    }
+}
 
-        if (a.mode == MOE_EXPERT_CHOICE) {
+// Scoring and selection from split-K partial logits of the tensor-core router:
+// one warp per token sums partial[0..splits)[t][e] in split order, adds the logit
+// offset, and runs warp_score_select.
+// KPL = experts per lane (E <= 32 * KPL); the warps loop over tokens.
+template <int KPL>
+__global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const float *__restrict__ partial, int splits,
+                                                           int npad) {
+    const int lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (blockDim.x >> 5);
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
+        float u[KPL];
 #pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E) a.scores_t[(size_t)e * a.T + t] = p[i];
-            }
-            continue;
-        }
-
-        float key[kPerLane];
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
+        for (int i = 0; i < KPL; ++i) {
             const int e = lane + 32 * i;
-            key[i] = (e < E) ? p[i] + (a.sel_bias ? a.sel_bias[e] : 0.f) : -FLT_MAX;
-        }
-        unsigned chosen = 0;     // bit i: expert lane + 32 i already selected
-        float wsum = 0.f, wj = 0.f;
-        int ij = 0;
-        for (int j = 0; j < a.k; ++j) {
-            float bk = -FLT_MAX, bp = 0.f;
-            int bi = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !(chosen >> i & 1u) && key[i] > bk) {   // ascending e: ties keep the lower
-                    bk = key[i];
-                    bi = e;
-                    bp = p[i];
-                }
+            float v = -FLT_MAX;
+            if (e < a.E) {
+                v = 0.f;
+                for (int s = 0; s < splits; ++s) v += partial[((size_t)s * a.T + t) * npad + e];
+                if (a.logit_offset) v += a.logit_offset[e];
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-                if (ok > bk || (ok == bk && oi < bi)) {
-                    bk = ok;
-                    bi = oi;
-                    bp = op;
-                }
-            }
-            if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
-            wsum += bp;
-            if (lane == j) {
-                ij = bi;
-                wj = bp;
-            }
+            u[i] = v;
         }
-        if (lane < a.k) {
-            a.topk_idx[(size_t)t * a.k + lane] = ij;
-            a.topk_w[(size_t)t * a.k + lane] = a.renorm ? wj / wsum : wj;
-        }
+        warp_score_select<KPL>(a, u, t, lane);
     }
 }
 
@@ -201,6 +243,7 @@ cudaError_t launch_typed(const RouteArgs &a, cudaStream_t s) {
 // are written in ascending token order with a block-wide ordered compaction.
 constexpr int kEcThreads = 1024;
 constexpr int kEcSmemMaxT = 49152;   // the column stays in shared memory up to this many tokens (192 KB)
+constexpr int kEcBins = 4096;        // widest radix digit (12 bits)
 
 // Exclusive block-wide prefix sum of one int per thread; `total` gets the sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total) {
@@ -235,7 +278,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
 __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scores_t, int T, int cap,
                                                                  int32_t *ec_tok, float *ec_w) {
     extern __shared__ unsigned s_col[];   // the expert's column, when it fits
-    __shared__ unsigned hist[256];
+    __shared__ unsigned hist[kEcBins];
     __shared__ int warp_tot[65];
     __shared__ unsigned s_digit;
     __shared__ int s_remaining;
@@ -248,41 +291,52 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scor
     }
     const unsigned *col = in_smem ? s_col : g;
 
+    // three digits, high to low: 12 bits (sign, exponent and 3 mantissa bits, so the
+    // scores of one expert -- which share a few exponents -- spread over many bins),
+    // then 10 and 10 bits
+    constexpr int kShift[3] = {20, 10, 0};
+    constexpr int kBits[3] = {12, 10, 10};
     unsigned prefix = 0, mask = 0;
     int remaining = cap;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = kShift[pass];
+        const int nb = 1 << kBits[pass];
+        const unsigned dmask = (unsigned)nb - 1u;
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        // scores of one expert share a few exponents, so most keys land in a few
-        // bins: aggregate per warp (one atomic per distinct bin) to avoid serialising
-        for (int t0 = 0; t0 < T; t0 += blockDim.x) {
-            const int t = t0 + threadIdx.x;
-            unsigned bin = 256u;   // no bin
-            if (t < T) {
-                const unsigned u = col[t];
-                if ((u & mask) == prefix) bin = (u >> shift) & 255u;
-            }
-            const unsigned peers = warp_peers9(bin);
-            if (bin < 256u && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        for (int t = threadIdx.x; t < T; t += blockDim.x) {
+            const unsigned u = col[t];
+            if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & dmask], 1u);
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
-            int cum = 0;
-            unsigned dg = 0;
-            for (int b = 255; b >= 0; --b) {
+        // find the digit holding the `remaining`-th largest key: thread i sums the
+        // bins of digits it owns (digits counted from the top), a block scan gives
+        // the keys above them, and the owner of the crossing walks its bins
+        const int per = (nb + (int)blockDim.x - 1) / (int)blockDim.x;
+        const int b_hi = nb - 1 - (int)threadIdx.x * per;   // this thread's digits: b_hi, b_hi-1, ...
+        int mine = 0;
+        for (int j = 0; j < per; ++j)
+            if (b_hi - j >= 0) mine += (int)hist[b_hi - j];
+        int tot;
+        const int above = block_exclusive_scan(mine, warp_tot, tot);
+        if (above < remaining && above + mine >= remaining) {
+            int cum = above;
+            for (int j = 0; j < per; ++j) {
+                const int b = b_hi - j;
+                if (b < 0) break;
                 const int h = (int)hist[b];
                 if (cum + h >= remaining) {
-                    dg = (unsigned)b;
+                    s_digit = (unsigned)b;
+                    s_remaining = remaining - cum;
                     break;
                 }
                 cum += h;
             }
-            s_digit = dg;
-            s_remaining = remaining - cum;
         }
         __syncthreads();
         prefix |= s_digit << shift;
-        mask |= 255u << shift;
+        mask |= dmask << shift;
         remaining = s_remaining;
         __syncthreads();
     }
@@ -337,6 +391,32 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
     a.scores_t = scores_t;
     if (c.dtype == MOE_F32) return launch_typed<float>(a, s);
     return launch_typed<__nv_bfloat16>(a, s);
+}
+
+cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
+                                int32_t *topk_idx, float *topk_w, float *scores_t, const float *partial, int splits,
+                                int npad, cudaStream_t s) {
+    RouteArgs a{};
+    a.logit_offset = logit_offset;
+    a.sel_bias = sel_bias;
+    a.T = c.T;
+    a.d = c.d;
+    a.E = c.E;
+    a.k = c.k;
+    a.gate = c.gate;
+    a.mode = c.mode;
+    a.renorm = c.renormalize;
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.scores_t = scores_t;
+    int blocks = (c.T + 7) / 8;
+    const int cap = num_sms() * 2;   // warps loop over tokens: the body stays in the instruction cache
+    if (blocks > cap) blocks = cap;
+    if (c.E <= 32) route_select_kernel<1><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
+    else if (c.E <= 64) route_select_kernel<2><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
+    else if (c.E <= 128) route_select_kernel<4><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
+    else route_select_kernel<8><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,

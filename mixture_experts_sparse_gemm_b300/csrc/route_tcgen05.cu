@@ -21,6 +21,27 @@ int padded_n(int E) {
     return n;   // 16, 32, 64, 128 or 256
 }
 
+// K splits of the router GEMM: with few 128-token tiles (T small, d large) the
+// d-reduction is spread over up to 8 CTAs per tile so that ~all 148 SMs of a B300
+// stream x; the partial logits then go through route_select_kernel.  Fixed SM
+// count: workspace sizes are computed without a device query.
+constexpr int kRouteSms = 148;
+int route_splits(const moe_config &c) {
+    const int mtiles = (c.T + kBM - 1) / kBM;
+    // the fused scoring epilogue wins when the tiles already cover half the SMs, or
+    // when each tile is short (d < 2048) and its top-k cheap (E * k-slots < 256)
+    const int kslots = (c.mode == MOE_EXPERT_CHOICE || c.k <= 1) ? 1 : (c.k <= 2 ? 2 : (c.k <= 4 ? 4 : 8));
+    if (mtiles >= kRouteSms / 2) return 1;
+    if (c.d / kBK < 32 && c.E * kslots < 256) return 1;
+    int s = kRouteSms / (mtiles > 0 ? mtiles : 1);
+    s = s < 8 ? s : 8;
+    const int quarter_k = (c.d / kBK) / 4;
+    s = s < quarter_k ? s : quarter_k;
+    return s >= 2 ? s : 1;
+}
+
+size_t wr_t_bytes(const moe_config &c) { return align_up((size_t)padded_n(c.E) * c.d * 2, 256); }
+
 // wr_t[e][i] = W_r[i][e] for e < E, 0 for E <= e < npad; seg = {0, T}
 __global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __nv_bfloat16 *__restrict__ wr_t,
                                         int d, int E, int npad, int32_t *seg, int T) {
@@ -53,15 +74,27 @@ cudaError_t launch_route_n(int npad, const CUtensorMap &a0, const CUtensorMap &b
     }
 }
 
+cudaError_t launch_partial_n(int npad, const CUtensorMap &a0, const CUtensorMap &b0, const TcArgs &g, int64_t tiles,
+                             cudaStream_t s) {
+    switch (npad) {
+        case 16: return launch_gemm<16, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+        case 32: return launch_gemm<32, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+        case 64: return launch_gemm<64, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+        case 128: return launch_gemm<128, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+        default: return launch_gemm<256, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+    }
+}
+
 }  // namespace
 
 bool route_tcgen05_supported(const moe_config &c) { return c.dtype == MOE_BF16 && c.E <= kMaxE && c.d % 64 == 0; }
 
 size_t route_tcgen05_scratch_bytes(const moe_config &c) {
-    return align_up((size_t)padded_n(c.E) * c.d * 2, 256) + 256;
+    const int s = route_splits(c);
+    return wr_t_bytes(c) + 256 + (s > 1 ? sizeof(float) * (size_t)s * c.T * padded_n(c.E) : 0);
 }
 
-int route_tcgen05_launches(const moe_config &) { return 2; }
+int route_tcgen05_launches(const moe_config &c) { return route_splits(c) > 1 ? 3 : 2; }
 
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
                                  const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t, void *wr_t,
@@ -69,7 +102,9 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
     const int npad = padded_n(c.E);
     char *scratch = static_cast<char *>(wr_t);
     __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(scratch);
-    int32_t *seg = reinterpret_cast<int32_t *>(scratch + align_up((size_t)npad * c.d * 2, 256));
+    int32_t *seg = reinterpret_cast<int32_t *>(scratch + wr_t_bytes(c));
+    float *partial = reinterpret_cast<float *>(scratch + wr_t_bytes(c) + 256);
+    const int splits = route_splits(c);
     const dim3 tg((npad + 31) / 32, (c.d + 31) / 32);
     transpose_router_kernel<<<tg, dim3(32, 8), 0, s>>>(static_cast<const __nv_bfloat16 *>(W_r), wt, c.d, c.E, npad,
                                                        seg, c.T);
@@ -86,6 +121,16 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
                        c.renormalize};
     g.err = err;
     const int64_t tiles = (c.T + kBM - 1) / kBM;
+    if (splits > 1) {
+        // split-K partial logits, then warp-per-token scoring and selection
+        g.p[0].g.nblk_routed = splits;
+        g.p[0].ksplit = splits;
+        g.p[0].C0 = partial;
+        g.p[0].ldc0 = c.T;
+        cudaError_t e = launch_partial_n(npad, a0, b0, g, tiles * splits, s);
+        if (e != cudaSuccess) return e;
+        return launch_route_select(c, logit_offset, sel_bias, topk_idx, topk_w, scores_t, partial, splits, npad, s);
+    }
     const int kmax = (c.mode == MOE_EXPERT_CHOICE || c.k <= 1) ? 1 : (c.k <= 2 ? 2 : (c.k <= 4 ? 4 : 8));
     switch (kmax) {
         case 1: return launch_route_n<kEpiRoute + 1>(npad, a0, b0, g, tiles, s);

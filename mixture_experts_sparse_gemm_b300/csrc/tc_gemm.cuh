@@ -40,6 +40,7 @@ constexpr int kThreads = 192;
 constexpr int kEpiSwiGLU = 0;   // up projection (+ SwiGLU)
 constexpr int kEpiStore = 1;    // down projection (optionally gated, see TcArgs::gated)
 constexpr int kEpiFfn = 2;      // both: up tiles, then down tiles, in one persistent launch
+constexpr int kEpiPartial = 3;  // split-K partial sums: fp32 rows of C0[split][rows][BN]
 // router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
 constexpr int kEpiRoute = 10;
 
@@ -79,6 +80,9 @@ struct TcGemm {
     void *C0;             // routed output rows (bf16)
     void *C1;             // shared output rows (bf16)
     int ldc0, ldc1;       // output row pitch in elements
+    // > 1: the K range is split over ksplit tiles (the N-block index is the split;
+    // one N tile of width BN covers all of N), each writing its partial sums
+    int ksplit;
 };
 
 struct TcArgs {
@@ -355,6 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         total += tile_start1[S];
     }
+    // k blocks [kb0, kb0 + nk) of a tile (a K split takes its share of them)
+    auto krange = [&](const TileAt &t, const TcGemm &G, int &kb0, int &nk) {
+        const int all = ((t.s < G.g.E) ? G.K0 : G.K1) / kBK;
+        if (G.ksplit > 1) {
+            const int per = (all + G.ksplit - 1) / G.ksplit;
+            kb0 = t.nb * per;
+            nk = min(all, kb0 + per) - kb0;
+        } else {
+            kb0 = 0;
+            nk = all;
+        }
+    };
     auto locate = [&](int tile) {
         TileAt t;
         if (kPhases == 2 && tile >= total0) {
@@ -401,8 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap *mA = (t.phase == 0) ? (routed ? &tmA0 : &tmA1) : (routed ? &tmA2 : &tmA3);
                 const CUtensorMap *mB = routed ? &tmB0 : &tmB1;
                 const int arow = seg_row0[t.s] + t.mb * kBM;
-                const int brow = (routed ? t.s * G.b_rows0 : 0) + t.nb * BN;
-                const int nk = (routed ? G.K0 : G.K1) / kBK;
+                const int brow = (routed ? t.s * G.b_rows0 : 0) + (G.ksplit > 1 ? 0 : t.nb * BN);
+                int kb0, nk;
+                krange(t, G, kb0, nk);
                 const uint8_t *bt = nullptr;
                 size_t img_bytes = 0;
                 if (G.Bt0) {
@@ -421,11 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_u32(&full[stage]);
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
                     mbar_arrive_expect_tx(fb, C::kStageBytes);
-                    tma_load_2d(smem_u32(st), mA, kb * kBK, arow, fb);
+                    tma_load_2d(smem_u32(st), mA, (kb0 + kb) * kBK, arow, fb);
                     if (bt)
-                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)kb * img_bytes, C::kBBytes, fb);
+                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)(kb0 + kb) * img_bytes, C::kBBytes, fb);
                     else
-                        tma_load_2d(smem_u32(st + C::kABytes), mB, kb * kBK, brow, fb);
+                        tma_load_2d(smem_u32(st + C::kABytes), mB, (kb0 + kb) * kBK, brow, fb);
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -461,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
                 const TileAt t = locate(tile);
                 const TcGemm &G = a.p[t.phase];
-                const int nk = ((t.s < G.g.E) ? G.K0 : G.K1) / kBK;
+                int kb0, nk;
+                krange(t, G, kb0, nk);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err)) {
@@ -521,6 +539,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI > kEpiRoute) {
                 route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows);
+            } else if constexpr (EPI == kEpiPartial) {
+                // fp32 partial sums of K split t.nb: C0[split][row][BN], row stride BN
+                float *P = static_cast<float *>(G.C0) + ((size_t)t.nb * G.ldc0 + grow) * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c * 16, v);
+                    tmem_ld_wait();
+                    if (row < rows) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(P + c * 16);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
+                }
             } else {
                 __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? G.C0 : G.C1);
                 const int ldc = routed ? G.ldc0 : G.ldc1;

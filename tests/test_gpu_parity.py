@@ -59,6 +59,8 @@ SMALL_TC = {
     "sigmoid_top8_e256": WORKLOADS["deepseek_v3"].with_(T=200, d=384, f=128, f_shared=128, name="sig8"),
     "top1_cap": WORKLOADS["switch_top1_cap1.25"].with_(T=1000, d=256, f=128, E=16, name="top1cap"),
     "t1": WORKLOADS["mixtral_T16"].with_(T=1, d=128, f=64, name="t1"),
+    # few token tiles and a long d: the router splits K over CTAs and selects per warp
+    "sigmoid_top8_splitk": WORKLOADS["deepseek_v3"].with_(T=200, d=2048, f=128, f_shared=128, name="sig8_split"),
 }
 ROUTE_CASES = ["tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T4096", "deepseek_v3"] + list(SMALL_TC)
 
@@ -91,6 +93,8 @@ EC_CASES = {
     "expert_choice_zipf": WORKLOADS["expert_choice_zipf"],
     "ec_small": WORKLOADS["expert_choice_zipf"].with_(T=1000, d=256, E=16, f=128, ec_capacity=100, name="ec_small"),
     "ec_cap_eq_T": WORKLOADS["expert_choice_zipf"].with_(T=77, d=128, E=4, f=64, ec_capacity=77, name="ec_full"),
+    # split-K router feeding the expert-major scores
+    "ec_splitk": WORKLOADS["expert_choice_zipf"].with_(T=1000, d=2048, E=16, f=64, ec_capacity=100, name="ec_split"),
     # a column longer than the select kernel keeps in shared memory (49152 tokens)
     "ec_long_column": WORKLOADS["expert_choice_zipf"].with_(T=50000, d=128, E=4, f=64, ec_capacity=1000,
                                                             name="ec_long"),
