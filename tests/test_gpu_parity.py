@@ -213,7 +213,8 @@ def test_dispatch_expert_choice(cuda_device):
 
 FFN_CASES = [
     # T, d, E, f, k, skew, n_shared, f_shared, dtype
-    (700, 256, 8, 384, 2, 1.2, 0, 0, "bf16"),      # f % 128 != 0: 128-wide up tiles; empty experts
+    (700, 256, 8, 320, 2, 1.2, 0, 0, "bf16"),      # f % 128 != 0: 128-wide up tiles; empty experts
+    (700, 256, 8, 384, 2, 1.2, 0, 0, "bf16"),      # skewed segments, 256-wide tiles
     (300, 384, 4, 256, 2, 0.0, 2, 128, "bf16"),    # d % 256 != 0: 128-wide down tiles; shared experts
     (1024, 1024, 8, 512, 1, 0.0, 0, 0, "bf16"),    # several full 128-row tiles per expert
     (129, 128, 3, 64, 1, 0.0, 1, 64, "bf16"),
@@ -254,6 +255,56 @@ def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
     if ns:
         sref = sum(oracle.expert_rows(x, Ws[0][s], Ws[1][s], Ws[2][s], nthreads=NTH) for s in range(ns))
         assert rel_err(Yn[T * k:], sref) <= TOL[dt]
+
+
+# Segment sizes around the 128-row M tile: 1, 15, 16, 17, 111, 112, 113, 127, 128,
+# 129, 240 rows and an empty expert; the shared segment (T = 1029 rows) ends in a
+# 5-row tile.
+EDGE_COUNTS = [1, 15, 16, 17, 111, 112, 113, 127, 128, 129, 240, 0]
+
+
+@pytest.mark.parametrize("d,f", [(256, 256), (384, 128)])
+def test_grouped_ffn_tile_edges(d, f, cuda_device):
+    E, T, ns, fs = len(EDGE_COUNTS), sum(EDGE_COUNTS), 1, 128
+    cfg = B.config(T=T, d=d, E=E, f=f, k=1, n_shared=ns, f_shared=fs, dtype="bf16")
+    g = torch.Generator(device="cpu").manual_seed(d + f)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).to(torch.bfloat16)
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).to(torch.bfloat16)
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).to(torch.bfloat16)
+    Ws = [(torch.randn(ns, d, fs, generator=g) / d ** 0.5).to(torch.bfloat16),
+          (torch.randn(ns, d, fs, generator=g) / d ** 0.5).to(torch.bfloat16),
+          (torch.randn(ns, fs, d, generator=g) / fs ** 0.5).to(torch.bfloat16)]
+    x = random_rows(T, d, seed=11, dtype=torch.bfloat16)
+    order = np.random.default_rng(7).permutation(T)
+    idx = np.repeat(np.arange(E, dtype=np.int32), EDGE_COUNTS)[order].reshape(T, 1)
+    o_off, _, _, o_rows = oracle.dispatch_tc(idx, E, -1)
+    assert np.diff(o_off).tolist() == EDGE_COUNTS
+    x_perm = x[torch.from_numpy(o_rows).long()]
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    off_d, xp_d, x_d = torch.from_numpy(o_off).to(dev), x_perm.to(dev), x.to(dev)
+    Y = _np(layer.grouped_ffn(xp_d, off_d, x_d))
+    # the two GEMMs as separate launches too
+    H = torch.empty(T, f, dtype=torch.bfloat16, device=dev)
+    Hs = torch.empty(T, fs, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty(2 * T, d, dtype=torch.bfloat16, device=dev)
+    B.moe_grouped_ffn_up(cfg, xp_d, off_d, layer.packed, x_d, H, Hs)
+    B.moe_grouped_ffn_down(cfg, H, Hs, off_d, layer.packed, Y2)
+    Y2 = _np(Y2)
+    _check_device_error()
+    ref = np.zeros((2 * T, d))
+    for e in range(E):
+        a, b = int(o_off[e]), int(o_off[e + 1])
+        if b > a:
+            ref[a:b] = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
+    ref[T:] = oracle.expert_rows(x, Ws[0][0], Ws[1][0], Ws[2][0], nthreads=NTH)
+    for got in (Y, Y2):
+        # per segment, so that one short tile going wrong cannot hide behind the others
+        for e in range(E):
+            a, b = int(o_off[e]), int(o_off[e + 1])
+            if b > a:
+                assert rel_err(got[a:b], ref[a:b]) <= TOL["bf16"], (e, b - a)
+        assert rel_err(got[T:], ref[T:]) <= TOL["bf16"]
 
 
 # ------------------------------------------------------------------------------------------ combine
