@@ -294,6 +294,36 @@ def run_gpu(args):
     clk = clocks.stop(bus, t_lo, t_hi2)
     B.moe_check_device_error(stream)
 
+    # ---- load statistics (outside the timed regions): the router with its score sums,
+    # and the statistics kernel, each averaged over a short loop of its own
+    psum = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    frac = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    pmean = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    summary = torch.empty(5, dtype=torch.float64, device=dev)
+    n_ls = 20
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_ls):
+            fn()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        return a0.elapsed_time(a1) / n_ls
+
+    route_plain_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream))
+    route_probs_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream, psum))
+    B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream)
+    stats_ms = timed(lambda: B.moe_load_stats(cfg, idx, cnt, psum, frac, pmean, summary, stream))
+    B.moe_check_device_error(stream)
+    load_stats = {"route_ms": round(route_plain_ms, 5), "route_with_prob_sum_ms": round(route_probs_ms, 5),
+                  "stats_kernel_ms": round(stats_ms, 5),
+                  "lif": round(float(summary[0]), 4), "cv": round(float(summary[1]), 4),
+                  "router_entropy": round(float(summary[2]), 4), "switch_aux": round(float(summary[3]), 4),
+                  "expert_balance": round(float(summary[4]), 4)}
+
     # ---- end to end through the C ABI with host buffers (pinned): every step copies its
     # tokens host -> device, runs moe_forward and copies its output device -> host.  The
     # copies of neighbouring steps overlap the compute on their own streams (double
@@ -402,6 +432,7 @@ def run_gpu(args):
                            "bytes_per_step": layer_bytes, "flops_per_step": layer_flops},
         "stages": stage_info,
         "staged_ms_per_step": round(staged_ms, 5),
+        "load_stats": load_stats,
         "roofline": roof,
         "e2e": {"value": round(replica_throughput(ws_n, T, K, e2e_ms), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": T * d * y.element_size(),

@@ -142,9 +142,13 @@ moe_status moe_pack_weights(const moe_config *cfg, const void *W1, const void *W
  * Expert choice writes topk_idx as ec_tok[E][cap] (int32, ascending token ids; ties
  *   to the lower token index) and topk_w as ec_w[E][cap] = softmax score of that
  *   token for that expert.
+ * prob_sum: [E] fp32 device buffer or NULL.  When given it is overwritten with the
+ *   sum over the T tokens of each expert's router score (softmax probability, or
+ *   sigmoid score without the selection bias), the input of moe_load_stats.  The
+ *   sum is accumulated with atomics, so its last bits vary from run to run.
  */
 moe_status moe_route(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
-                     const float *sel_bias, int32_t *topk_idx, float *topk_w, void *ws,
+                     const float *sel_bias, int32_t *topk_idx, float *topk_w, float *prob_sum, void *ws,
                      size_t ws_bytes, void *stream);
 
 /*
@@ -238,6 +242,24 @@ moe_status moe_combine(const moe_config *cfg, const void *Y, const int32_t *slot
 moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
                        const float *sel_bias, const void *packed, void *y, void *ws, size_t ws_bytes,
                        void *stream);
+
+/*
+ * Load statistics of one routing ("技术日报 2026-04-14" §4.4 diagnostics; §4.2
+ * Switch auxiliary loss and DeepSeek V1 expert-level balance, both without their
+ * alpha).  Inputs (device, read only): topk_idx and cnt_raw as moe_route and
+ * moe_dispatch wrote them, prob_sum as moe_route wrote it.  With
+ *   f_e  = cnt_raw[e] / sum(cnt_raw)   (assignment share before any capacity drop),
+ *   f1_e = share of the T tokens whose slot-0 expert is e (Expert Choice: f_e),
+ *   P_e  = prob_sum[e] / T              (mean router score),
+ * writes token_fraction[e] = f_e and prob_mean[e] = P_e ([E] fp32 each), and
+ * summary (device, 5 doubles) = { E*max f, std(f)/mean(f) (population std),
+ * -sum q ln q with q = P/sum(P), E*sum f1*P, E*sum f*P }.  Balanced routing gives
+ * {1, 0, ln E, 1, 1} for softmax scores.  One kernel on `stream`; T == 0 writes
+ * nothing.
+ */
+moe_status moe_load_stats(const moe_config *cfg, const int32_t *topk_idx, const int32_t *cnt_raw,
+                          const float *prob_sum, float *token_fraction, float *prob_mean, double *summary,
+                          void *stream);
 
 /* Number of CUDA kernels one call of `stage` enqueues for this configuration
  * (memsets not counted; MOE_STAGE_FORWARD: the whole layer).  No CUDA call. */

@@ -7,5 +7,5 @@ points; ``layer`` allocates the buffers a layer needs around them.
 from .binding import (EXPORTS, MoeError, config, config_from_workload, lib, moe_buffer_rows,  # noqa: F401
                       moe_check_device_error, moe_combine, moe_config, moe_dispatch, moe_expert_capacity,
                       moe_forward, moe_grouped_ffn, moe_grouped_ffn_down, moe_grouped_ffn_up,
-                      moe_launch_count, moe_pack_weights, moe_packed_weights_size, moe_route,
+                      moe_launch_count, moe_load_stats, moe_pack_weights, moe_packed_weights_size, moe_route,
                       moe_validate_config, moe_workspace_size, status_string)

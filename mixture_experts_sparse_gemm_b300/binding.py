@@ -24,7 +24,7 @@ MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, M
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
            "moe_workspace_size", "moe_packed_weights_size", "moe_pack_weights", "moe_route", "moe_dispatch",
            "moe_grouped_ffn", "moe_grouped_ffn_up", "moe_grouped_ffn_down", "moe_combine", "moe_forward",
-           "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc")
+           "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc", "moe_load_stats")
 MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS = 65536
 
 
@@ -63,7 +63,7 @@ def lib():
             "moe_workspace_size": [cfgp, ctypes.c_int, szp],
             "moe_packed_weights_size": [cfgp, szp],
             "moe_pack_weights": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
-            "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+            "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_grouped_ffn": [cfgp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_grouped_ffn_up": [cfgp, vp, vp, vp, vp, vp, vp, vp],
@@ -73,6 +73,7 @@ def lib():
             "moe_forward": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_check_device_error": [vp],
             "moe_dispatch_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_load_stats": [cfgp, vp, vp, vp, vp, vp, vp, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -163,9 +164,14 @@ def moe_pack_weights(cfg, W1, W3, W2, W1s, W3s, W2s, packed, stream=None):
                                   _nbytes(packed), _stream(stream)), "moe_pack_weights")
 
 
-def moe_route(cfg, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, ws, stream=None):
+def moe_route(cfg, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, ws, stream=None, prob_sum=None):
     _check(lib().moe_route(ctypes.byref(cfg), _p(x), _p(W_r), _p(logit_offset), _p(sel_bias), _p(topk_idx),
-                           _p(topk_w), _p(ws), _nbytes(ws), _stream(stream)), "moe_route")
+                           _p(topk_w), _p(prob_sum), _p(ws), _nbytes(ws), _stream(stream)), "moe_route")
+
+
+def moe_load_stats(cfg, topk_idx, cnt_raw, prob_sum, token_fraction, prob_mean, summary, stream=None):
+    _check(lib().moe_load_stats(ctypes.byref(cfg), _p(topk_idx), _p(cnt_raw), _p(prob_sum), _p(token_fraction),
+                                _p(prob_mean), _p(summary), _stream(stream)), "moe_load_stats")
 
 
 def moe_dispatch(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, ws, stream=None):

@@ -70,12 +70,13 @@ struct Carver {
 };
 
 struct RouteWs {
-    size_t scores_t, wr_t, total;
+    size_t scores_t, wr_t, psum_rows, total;
 };
 RouteWs route_ws(const moe_config &c) {
     Carver k;
     RouteWs w{};
     w.scores_t = k.take(c.mode == MOE_EXPERT_CHOICE ? sizeof(float) * (size_t)c.E * c.T : 0);
+    w.psum_rows = k.take(sizeof(float) * kPsumRows * (size_t)c.E);   // router score sums, see moe_route
     w.wr_t = k.take(c.dtype == MOE_BF16 && route_tcgen05_supported(c) ? route_tcgen05_scratch_bytes(c) : 0);
     w.total = k.off;
     return w;
@@ -138,16 +139,23 @@ ForwardWs forward_ws(const moe_config &c) {
 }
 
 // ---------------------------------------------------------------- stage bodies (validated input)
+// prob_sum (nullable): the router CTAs add their score sums into kPsumRows rows of
+// the workspace (row = CTA index mod kPsumRows, so few CTAs share an address),
+// then one small kernel sums the rows in order into prob_sum[E].
 moe_status do_route(const moe_config &c, const void *x, const void *W_r, const float *lo, const float *sb,
-                    int32_t *idx, float *w, char *ws, unsigned *err, cudaStream_t s) {
+                    int32_t *idx, float *w, char *ws, unsigned *err, cudaStream_t s, float *prob_sum = nullptr) {
     const RouteWs L = route_ws(c);
     float *scores_t = c.mode == MOE_EXPERT_CHOICE ? reinterpret_cast<float *>(ws + L.scores_t) : nullptr;
+    float *rows = prob_sum ? reinterpret_cast<float *>(ws + L.psum_rows) : nullptr;
     cudaError_t e;
+    if (rows && cudaMemsetAsync(rows, 0, sizeof(float) * kPsumRows * (size_t)c.E, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (c.dtype == MOE_BF16 && route_tcgen05_supported(c))
-        e = launch_route_tcgen05(c, x, W_r, lo, sb, idx, w, scores_t, ws + L.wr_t, err, s);
+        e = launch_route_tcgen05(c, x, W_r, lo, sb, idx, w, scores_t, rows, ws + L.wr_t, err, s);
     else
-        e = launch_route_simt(c, x, W_r, lo, sb, idx, w, scores_t, err, s);
+        e = launch_route_simt(c, x, W_r, lo, sb, idx, w, scores_t, rows, err, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (rows && launch_sum_psum_rows(c, rows, prob_sum, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (c.mode == MOE_EXPERT_CHOICE) return from_cuda(launch_ec_select(c, scores_t, idx, w, s));
     return MOE_OK;
 }
@@ -375,23 +383,28 @@ moe_status moe_pack_weights(const moe_config *cfg, const void *W1, const void *W
 }
 
 moe_status moe_route(const moe_config *cfg, const void *x, const void *W_r, const float *logit_offset,
-                     const float *sel_bias, int32_t *topk_idx, float *topk_w, void *ws, size_t ws_bytes,
-                     void *stream) {
+                     const float *sel_bias, int32_t *topk_idx, float *topk_w, float *prob_sum, void *ws,
+                     size_t ws_bytes, void *stream) {
     moe_status st = moe_validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
     MOE_REQUIRE(x && W_r && topk_idx && topk_w, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(c.mode == MOE_TOKEN_CHOICE || !sel_bias, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(aligned16(x) && aligned16(W_r), MOE_ERR_MISALIGNED);
-    MOE_REQUIRE(aligned4(topk_idx) && aligned4(topk_w) && aligned4(logit_offset) && aligned4(sel_bias),
+    MOE_REQUIRE(aligned4(topk_idx) && aligned4(topk_w) && aligned4(logit_offset) && aligned4(sel_bias) &&
+                    aligned4(prob_sum),
                 MOE_ERR_MISALIGNED);
     st = check_ws(ws, ws_bytes, route_ws(c).total);
     if (st != MOE_OK) return st;
     unsigned *err = nullptr;
     st = device_setup(&err);
-    if (st != MOE_OK || c.T == 0) return st;
-    return do_route(c, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, static_cast<char *>(ws), err,
-                    static_cast<cudaStream_t>(stream));
+    if (st != MOE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (c.T == 0) {   // no tokens: zero score sums
+        if (prob_sum && cudaMemsetAsync(prob_sum, 0, sizeof(float) * c.E, s) != cudaSuccess) return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    return do_route(c, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, static_cast<char *>(ws), err, s, prob_sum);
 }
 
 moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *off,
@@ -490,6 +503,22 @@ moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *ker
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
+}
+
+moe_status moe_load_stats(const moe_config *cfg, const int32_t *topk_idx, const int32_t *cnt_raw,
+                          const float *prob_sum, float *token_fraction, float *prob_mean, double *summary,
+                          void *stream) {
+    moe_status st = moe_validate_config(cfg);
+    if (st != MOE_OK) return st;
+    const moe_config &c = *cfg;
+    MOE_REQUIRE(topk_idx && cnt_raw && prob_sum && token_fraction && prob_mean && summary, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(aligned4(topk_idx) && aligned4(cnt_raw) && aligned4(prob_sum) && aligned4(token_fraction) &&
+                    aligned4(prob_mean) && (reinterpret_cast<uintptr_t>(summary) & 7u) == 0,
+                MOE_ERR_MISALIGNED);
+    st = device_setup(nullptr);
+    if (st != MOE_OK || c.T == 0) return st;
+    return from_cuda(launch_load_stats(c, topk_idx, cnt_raw, prob_sum, token_fraction, prob_mean, summary,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_combine(const moe_config *cfg, const void *Y, const int32_t *slot_of, const float *topk_w, void *y,

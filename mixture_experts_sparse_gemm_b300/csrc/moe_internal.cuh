@@ -12,6 +12,7 @@ namespace moe {
 
 constexpr int kMaxE = 256;     // routed experts
 constexpr int kMaxK = 8;       // experts per token (token choice)
+constexpr int kPsumRows = 64;   // rows of per-CTA router score sums (CTA index mod 64)
 constexpr int kGroup = 64;     // W1/W3 interleave width of the packed up-projection
 
 // bits of the device error word
@@ -73,13 +74,13 @@ struct GroupedShape {
 // ----------------------------------------------------------------------------- launchers
 cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_r,
                               const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
-                              float *topk_w, float *scores_t, unsigned *err, cudaStream_t s);
+                              float *topk_w, float *scores_t, float *psum_rows, unsigned *err, cudaStream_t s);
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
                              cudaStream_t s);
 // scoring + selection from split-K partial logits partial[splits][T][npad] (fp32)
 cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
-                                int32_t *topk_idx, float *topk_w, float *scores_t, const float *partial, int splits,
-                                int npad, cudaStream_t s);
+                                int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
+                                const float *partial, int splits, int npad, cudaStream_t s);
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);
@@ -115,10 +116,19 @@ cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const 
                                      const float *row_gate = nullptr);
 size_t ffn_dep_counters(const moe_config &c);
 bool ffn_fused_supported(const moe_config &c);
+// psum_rows (nullable, [kPsumRows][E], zeroed by the caller): every CTA adds the
+// sum over its tokens of each expert's score (softmax probability or sigmoid
+// score) into row (CTA index mod kPsumRows), for the load statistics
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r,
                                  const float *logit_offset, const float *sel_bias, int32_t *topk_idx,
-                                 float *topk_w, float *scores_t, void *wr_t, unsigned *err,
+                                 float *topk_w, float *scores_t, float *psum_rows, void *wr_t, unsigned *err,
                                  cudaStream_t s);
+// prob_sum[e] = sum over the kPsumRows rows of rows[r][e], in row order
+cudaError_t launch_sum_psum_rows(const moe_config &c, const float *rows, float *prob_sum, cudaStream_t s);
+// load statistics from the routing (one CTA); see moe_load_stats
+cudaError_t launch_load_stats(const moe_config &c, const int32_t *topk_idx, const int32_t *cnt_raw,
+                              const float *prob_sum, float *token_fraction, float *prob_mean, double *summary,
+                              cudaStream_t s);
 size_t route_tcgen05_scratch_bytes(const moe_config &c);
 bool route_tcgen05_supported(const moe_config &c);
 int route_tcgen05_launches(const moe_config &c);

@@ -31,6 +31,7 @@ struct RouteArgs {
     int32_t *topk_idx;
     float *topk_w;
     float *scores_t;   // expert choice: [E][T]
+    float *psum_rows;  // [kPsumRows][E] or null: += each block's sums of the experts' scores
 };
 
 constexpr int kPerLane = kMaxE / 32;   // experts per lane, the most a warp holds
@@ -41,8 +42,11 @@ constexpr int kPerLane = kMaxE / 32;   // experts per lane, the most a warp hold
 // choice takes k rounds of a warp arg-max on (key desc, index asc) over the keys
 // score + selection bias, so slots come out in descending key order with ties to
 // the lower expert index, and writes indices and (renormalised) weights.
+// With a.psum_rows, every score is also added to the lane's running sums pacc
+// (expert lane + 32 i), which the caller flushes once.
 template <int KPL>
-__device__ __forceinline__ void warp_score_select(const RouteArgs &a, const float (&u)[KPL], int t, int lane) {
+__device__ __forceinline__ void warp_score_select(const RouteArgs &a, const float (&u)[KPL], int t, int lane,
+                                                  float (&pacc)[KPL]) {
     constexpr int kPerLane = KPL;
     const int E = a.E;
     float p[kPerLane];
@@ -67,6 +71,11 @@ __device__ __forceinline__ void warp_score_select(const RouteArgs &a, const floa
         const float inv = 1.f / sum;
 #pragma unroll
         for (int i = 0; i < kPerLane; ++i) p[i] *= inv;
+    }
+    if (a.psum_rows) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i)
+            if (lane + 32 * i < E) pacc[i] += p[i];
     }
 
     if (a.mode == MOE_EXPERT_CHOICE) {
@@ -123,6 +132,25 @@ __device__ __forceinline__ void warp_score_select(const RouteArgs &a, const floa
     }
 }
 
+// Adds the warps' running score sums to the block's row of psum_rows: shared-memory
+// sums per block, then one global atomic per expert.  Every thread of the block
+// calls it.
+template <int KPL>
+__device__ __forceinline__ void flush_prob_sum(const RouteArgs &a, const float (&pacc)[KPL], int lane,
+                                               float *sacc) {
+    if (!a.psum_rows) return;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) sacc[e] = 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < a.E && pacc[i] != 0.f) atomicAdd(sacc + e, pacc[i]);
+    }
+    __syncthreads();
+    float *row = a.psum_rows + (size_t)(blockIdx.x % kPsumRows) * a.E;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) atomicAdd(row + e, sacc[e]);
+}
+
 template <typename Tin, int NPT>
 __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
     extern __shared__ float smem[];
@@ -174,6 +202,9 @@ __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
     __syncthreads();
 
     const int warp = tid >> 5, lane = tid & 31;
+    float pacc[kPerLane];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) pacc[i] = 0.f;
     for (int m = warp; m < kTM; m += kThreads / 32) {
         const int t = t0 + m;
         if (t >= a.T) break;
@@ -183,8 +214,10 @@ __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
             const int e = lane + 32 * i;
             u[i] = (e < E) ? lg[m * E + e] : -FLT_MAX;
         }
-        warp_score_select<kPerLane>(a, u, t, lane);
+        warp_score_select<kPerLane>(a, u, t, lane, pacc);
     }
+    __shared__ float sacc[kMaxE];
+    flush_prob_sum<kPerLane>(a, pacc, lane, sacc);
 }
 
 // Scoring and selection from split-K partial logits of the tensor-core router:
@@ -196,6 +229,9 @@ __global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const fl
                                                            int npad) {
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * (blockDim.x >> 5);
+    float pacc[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) pacc[i] = 0.f;
     for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
         float u[KPL];
 #pragma unroll
@@ -209,8 +245,10 @@ __global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const fl
             }
             u[i] = v;
         }
-        warp_score_select<KPL>(a, u, t, lane);
+        warp_score_select<KPL>(a, u, t, lane, pacc);
     }
+    __shared__ float sacc[kMaxE];
+    flush_prob_sum<KPL>(a, pacc, lane, sacc);
 }
 
 template <typename Tin, int NPT>
@@ -372,9 +410,9 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scor
 
 cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
                               const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t,
-                              unsigned *err, cudaStream_t s) {
+                              float *psum_rows, unsigned *err, cudaStream_t s) {
     (void)err;
-    RouteArgs a;
+    RouteArgs a{};
     a.x = x;
     a.Wr = W_r;
     a.logit_offset = logit_offset;
@@ -389,13 +427,14 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
     a.topk_idx = topk_idx;
     a.topk_w = topk_w;
     a.scores_t = scores_t;
+    a.psum_rows = psum_rows;
     if (c.dtype == MOE_F32) return launch_typed<float>(a, s);
     return launch_typed<__nv_bfloat16>(a, s);
 }
 
 cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
-                                int32_t *topk_idx, float *topk_w, float *scores_t, const float *partial, int splits,
-                                int npad, cudaStream_t s) {
+                                int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
+                                const float *partial, int splits, int npad, cudaStream_t s) {
     RouteArgs a{};
     a.logit_offset = logit_offset;
     a.sel_bias = sel_bias;
@@ -409,6 +448,7 @@ cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, 
     a.topk_idx = topk_idx;
     a.topk_w = topk_w;
     a.scores_t = scores_t;
+    a.psum_rows = psum_rows;
     int blocks = (c.T + 7) / 8;
     const int cap = num_sms() * 2;   // warps loop over tokens: the body stays in the instruction cache
     if (blocks > cap) blocks = cap;

@@ -97,8 +97,8 @@ size_t route_tcgen05_scratch_bytes(const moe_config &c) {
 int route_tcgen05_launches(const moe_config &c) { return route_splits(c) > 1 ? 3 : 2; }
 
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
-                                 const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t, void *wr_t,
-                                 unsigned *err, cudaStream_t s) {
+                                 const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t,
+                                 float *psum_rows, void *wr_t, unsigned *err, cudaStream_t s) {
     const int npad = padded_n(c.E);
     char *scratch = static_cast<char *>(wr_t);
     __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(scratch);
@@ -117,7 +117,7 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
     g.p[0].K0 = c.d;
     g.p[0].K1 = c.d;
     g.p[0].b_rows0 = npad;
-    g.route = RouteEpi{logit_offset, sel_bias, topk_idx, topk_w, scores_t, c.T, c.E, c.k, c.gate, c.mode,
+    g.route = RouteEpi{logit_offset, sel_bias, topk_idx, topk_w, scores_t, psum_rows, c.T, c.E, c.k, c.gate, c.mode,
                        c.renormalize};
     g.err = err;
     const int64_t tiles = (c.T + kBM - 1) / kBM;
@@ -129,7 +129,8 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
         g.p[0].ldc0 = c.T;
         cudaError_t e = launch_partial_n(npad, a0, b0, g, tiles * splits, s);
         if (e != cudaSuccess) return e;
-        return launch_route_select(c, logit_offset, sel_bias, topk_idx, topk_w, scores_t, partial, splits, npad, s);
+        return launch_route_select(c, logit_offset, sel_bias, topk_idx, topk_w, scores_t, psum_rows, partial, splits,
+                                   npad, s);
     }
     const int kmax = (c.mode == MOE_EXPERT_CHOICE || c.k <= 1) ? 1 : (c.k <= 2 ? 2 : (c.k <= 4 ? 4 : 8));
     switch (kmax) {

@@ -52,7 +52,7 @@ struct TcCfg {
     static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
     static constexpr int kBarBytes = (2 * kStages + 5) * 8;
-    static constexpr int kMiscBytes = 64 + sizeof(int) * (5 * (kMaxE + 2));
+    static constexpr int kMiscBytes = 64 + sizeof(int) * (6 * (kMaxE + 2));
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kMiscBytes;
 };
 
@@ -62,6 +62,7 @@ struct RouteEpi {
     int32_t *topk_idx;           // [T][k]
     float *topk_w;               // [T][k]
     float *scores_t;             // expert choice: [E][T]
+    float *psum_rows;            // [kPsumRows][E] or null: += each CTA's sums of the experts' scores
     int T, E, k, gate, mode, renorm;
 };
 
@@ -144,7 +145,8 @@ __device__ __forceinline__ void topk_insert(float (&tk)[KMAX], int (&ti)[KMAX], 
 //   then the k weights (renormalised when asked), or for Expert Choice every
 //   score written expert-major.
 template <int BN, int KMAX>
-__device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid) {
+__device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid,
+                                               float *psum_cta) {
     const int E = r.E, T = r.T;
     constexpr int kChunks = BN / 16;
     const bool softmax = r.gate == MOE_GATE_SOFTMAX;
@@ -193,6 +195,29 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
             }
         }
         inv = 1.f / sum;
+    }
+    if (r.psum_rows) {
+        // every expert's score summed over the warp's 32 token rows into the CTA's
+        // shared sums (added to its row of psum_rows once per CTA at the end of the kernel)
+        const int lane = threadIdx.x & 31;
+#pragma unroll 1
+        for (int c = 0; c < kChunks; ++c) {
+            uint32_t v[16];
+            tmem_ld16(taddr + c * 16, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int e = c * 16 + i;
+                float pe = 0.f;
+                if (e < E && valid) {
+                    const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
+                    pe = softmax ? __expf(u - mx) * inv : __fdividef(1.f, 1.f + __expf(-u));
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) pe += __shfl_xor_sync(0xffffffffu, pe, o);
+                if (lane == 0 && e < E) atomicAdd(psum_cta + e, pe);
+            }
+        }
     }
     if (ec) {
 #pragma unroll 1
@@ -306,8 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *seg_row0 = tile_start1 + (kMaxE + 2);
     int *seg_rows = seg_row0 + (kMaxE + 2);
     int *mtile_start = seg_rows + (kMaxE + 2);                      // first M tile of each segment
+    float *psum_cta = reinterpret_cast<float *>(mtile_start + (kMaxE + 2));   // router score sums of this CTA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if constexpr (EPI > kEpiRoute) {
+        for (int e = threadIdx.x; e < kMaxE; e += kThreads) psum_cta[e] = 0.f;   // before the first barrier
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -538,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (EPI > kEpiRoute) {
-                route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows);
+                route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows, psum_cta);
             } else if constexpr (EPI == kEpiPartial) {
                 // fp32 partial sums of K split t.nb: C0[split][row][BN], row stride BN
                 float *P = static_cast<float *>(G.C0) + ((size_t)t.nb * G.ldc0 + grow) * BN;
@@ -589,6 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    if constexpr (EPI > kEpiRoute) {
+        if (a.route.psum_rows) {   // this CTA's router score sums into its row: one atomic per expert
+            float *row = a.route.psum_rows + (size_t)(blockIdx.x % kPsumRows) * a.route.E;
+            for (int e = threadIdx.x; e < a.route.E; e += kThreads) atomicAdd(row + e, psum_cta[e]);
+        }
+    }
     if (warp == 1) {
         __syncwarp();
         fence_after();

@@ -44,11 +44,22 @@ class MoELayer:
         return (c.T, c.E) if c.mode == B.MOE_EXPERT_CHOICE else (c.T, c.k)
 
     # ------------------------------------------------------------------ stages
-    def route(self, x, W_r, logit_offset=None, sel_bias=None, stream=None):
+    def route(self, x, W_r, logit_offset=None, sel_bias=None, stream=None, prob_sum=None):
         idx = torch.empty(self.n_select(), dtype=torch.int32, device=self.device)
         w = torch.empty(self.n_select(), dtype=torch.float32, device=self.device)
-        B.moe_route(self.cfg, x, W_r, logit_offset, sel_bias, idx, w, self.workspace(B.MOE_STAGE_ROUTE), stream)
+        B.moe_route(self.cfg, x, W_r, logit_offset, sel_bias, idx, w, self.workspace(B.MOE_STAGE_ROUTE), stream,
+                    prob_sum)
         return idx, w
+
+    def load_stats(self, topk_idx, cnt_raw, prob_sum, stream=None):
+        """(token_fraction [E], prob_mean [E], summary [5] float64: LIF, CV, router
+        entropy, Switch balance E*sum f1*P, expert balance E*sum f*P)."""
+        E = self.cfg.E
+        frac = torch.empty(E, dtype=torch.float32, device=self.device)
+        pmean = torch.empty(E, dtype=torch.float32, device=self.device)
+        summary = torch.empty(5, dtype=torch.float64, device=self.device)
+        B.moe_load_stats(self.cfg, topk_idx, cnt_raw, prob_sum, frac, pmean, summary, stream)
+        return frac, pmean, summary
 
     def dispatch(self, idx, x, stream=None):
         c = self.cfg

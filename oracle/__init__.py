@@ -193,6 +193,45 @@ def expert_rows(X, W1, W3, W2, scale=None, nthreads=1):
     return out
 
 
+def load_stats(topk_idx, cnt_raw, scores, expert_choice=False):
+    """Load statistics of one routing, from the definitions of "技术日报 2026-04-14"
+    §4.4 (token fraction, LIF, CV, router entropy) and §4.2 (the Switch auxiliary
+    term N * sum_i f_i P_i and the DeepSeek V1 expert-level term sum_i f'_i P_i,
+    both without their alpha).
+
+    topk_idx: [T, k] (token choice) or ec_tok [E, cap]; cnt_raw: [E] assignments per
+    expert before any drop; scores: [T, E] router scores (softmax probability or
+    sigmoid score).  Returns (f [E], P [E], summary [5] = LIF, CV, entropy,
+    switch_aux, expert_balance), all float64:
+      f_i  = cnt_raw[i] / sum(cnt_raw)          (the page's token fraction, ideal 1/E)
+      f1_i = share of tokens whose first choice is i (Switch's argmax p; EC: f_i)
+      P_i  = mean over tokens of scores[:, i]
+      LIF  = E * max_i f_i;  CV = std(f) / mean(f) with the population std
+      entropy = -sum_i q_i ln q_i over q = P / sum(P), q_i = 0 terms omitted
+      switch_aux = E * sum_i f1_i P_i;  expert_balance = sum_i (E f_i) P_i, which is
+      the page's f'_i = N' / (K' T) * count_i with N' = E, K' T = sum(cnt_raw)
+    """
+    cnt = np.asarray(cnt_raw, np.float64)
+    scores = np.asarray(scores, np.float64)
+    T, E = scores.shape
+    f = cnt / cnt.sum()
+    if expert_choice:
+        f1 = f.copy()
+    else:
+        first = np.asarray(topk_idx)[:, 0]
+        f1 = np.zeros(E)
+        for t in range(T):
+            f1[first[t]] += 1.0
+        f1 /= T
+    P = scores.sum(axis=0) / T
+    mean = f.mean()
+    cv = np.sqrt(((f - mean) ** 2).mean()) / mean
+    q = P / P.sum()
+    ent = -sum(qi * np.log(qi) for qi in q if qi > 0.0)
+    summary = np.array([E * f.max(), cv, ent, E * float((f1 * P).sum()), E * float((f * P).sum())])
+    return f, P, summary
+
+
 def combine_tc(Y, slot_of, topk_w, tokens=None, Y_shared=None):
     """Gate-weighted combine, token choice: y[t] = sum over kept slots j (in slot
     order) of topk_w[t, j] * Y[slot_of[t, j]], plus Y_shared[t] when given."""

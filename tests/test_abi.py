@@ -96,9 +96,9 @@ def test_argument_checks_run_before_any_cuda_call():
     c = ctypes.byref(cfg)
     A = 0x10000          # aligned fake device addresses: never dereferenced, the checks fail first
     ws_need = B.moe_workspace_size(cfg, B.MOE_STAGE_DISPATCH)
-    assert L.moe_route(c, None, A, None, None, A, A, A, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
-    assert L.moe_route(c, A + 8, A, None, None, A, A, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
-    assert L.moe_route(c, A, A, None, None, A + 2, A, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_route(c, None, A, None, None, A, A, None, A, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route(c, A + 8, A, None, None, A, A, None, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_route(c, A, A, None, None, A + 2, A, None, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_dispatch(c, A, A, A, A, A, A, A, ws_need - 1, None) == B.MOE_ERR_WORKSPACE
     assert L.moe_dispatch(c, A, A, A, A, A, A, A + 64, ws_need, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_combine(c, A, A, None, A, None, 0, None) == B.MOE_ERR_INVALID_ARG
@@ -106,8 +106,12 @@ def test_argument_checks_run_before_any_cuda_call():
     assert L.moe_forward(None, A, A, None, None, A, A, A, 1 << 40, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_grouped_ffn(c, A, A, A, None, A, A, 0, None) == B.MOE_ERR_WORKSPACE
     ec = B.config(T=64, d=256, E=8, f=128, mode="ec", ec_capacity=8)
-    assert L.moe_route(ctypes.byref(ec), A, A, None, A, A, A, A, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_route(ctypes.byref(ec), A, A, None, A, A, A, None, A, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_pack_weights(c, A, A, A, None, None, None, A, 10, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_route(c, A, A, None, None, A, A, A + 2, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_load_stats(c, A, A, None, A, A, A, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_load_stats(c, A, A, A, A, A, A + 4, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_load_stats(None, A, A, A, A, A, A, None) == B.MOE_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")

@@ -307,6 +307,58 @@ def test_grouped_ffn_tile_edges(d, f, cuda_device):
         assert rel_err(got[T:], ref[T:]) <= TOL["bf16"]
 
 
+# ------------------------------------------------------------------------------------- load statistics
+# The router's score sums (moe_route's prob_sum) and moe_load_stats against the
+# oracle's definitions.  The count-based parts (fractions, LIF, CV) are computed by
+# both sides from the GPU's own routing and counts, the GPU in fp32: bar 1e-5
+# relative.  The score means come from fp32 scores (bf16 inputs, fp32 tensor-core
+# logits, about 1e-6 relative per score) summed in fp32: bar 1e-4 relative.
+STATS_CASES = ["tiny_top2_fp32", "switch_top1_cap1.25", "deepseek_v3", "mixtral_T256", "sigmoid_top8_splitk",
+               "ec_small", "ec_splitk"]
+
+
+@pytest.mark.parametrize("name", STATS_CASES)
+def test_load_stats(name, cuda_device):
+    wl = WORKLOADS[name] if name in WORKLOADS else (SMALL_TC[name] if name in SMALL_TC else EC_CASES[name])
+    dev = cuda_device
+    inp = make_inputs(wl, dev, weights=False)
+    cfg = B.config_from_workload(wl)
+    ec = wl.mode == "ec"
+    sel = (wl.E, wl.ec_capacity) if ec else (wl.T, wl.k)
+    ws = torch.empty(max(1, B.moe_workspace_size(cfg, B.MOE_STAGE_ROUTE)), dtype=torch.uint8, device=dev)
+    idx = torch.empty(sel, dtype=torch.int32, device=dev)
+    w = torch.empty(sel, dtype=torch.float32, device=dev)
+    psum = torch.full((wl.E,), 7.0, dtype=torch.float32, device=dev)   # overwritten, not accumulated into
+    B.moe_route(cfg, inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"], idx, w, ws, prob_sum=psum)
+    rows_routed, _ = B.moe_buffer_rows(cfg)
+    wsd = torch.empty(max(1, B.moe_workspace_size(cfg, B.MOE_STAGE_DISPATCH)), dtype=torch.uint8, device=dev)
+    off = torch.empty(wl.E + 1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
+    slot = torch.empty((wl.T, wl.E) if ec else (wl.T, wl.k), dtype=torch.int32, device=dev)
+    xp = torch.empty(max(1, rows_routed), wl.d, dtype=inp["x"].dtype, device=dev)
+    B.moe_dispatch(cfg, idx, inp["x"], off, cnt, slot, xp, wsd)
+    frac = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    pmean = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    summary = torch.empty(5, dtype=torch.float64, device=dev)
+    B.moe_load_stats(cfg, idx, cnt, psum, frac, pmean, summary)
+    _check_device_error()
+    if ec:
+        scores = oracle.route_ec(inp["x"], inp["W_r"], wl.ec_capacity, inp["logit_offset"], nthreads=NTH,
+                                 want_scores=True)[3]
+    else:
+        scores = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                 wl.renorm, nthreads=NTH, want_scores=True)[3]
+    f, P, s = oracle.load_stats(_np(idx), _np(cnt), scores, expert_choice=ec)
+    gs = summary.cpu().numpy()
+    np.testing.assert_allclose(_np(frac), f, rtol=1e-6, atol=1e-9)
+    np.testing.assert_allclose(_np(pmean), P, rtol=1e-4, atol=1e-7)
+    np.testing.assert_allclose(_np(psum) / wl.T, P, rtol=1e-4, atol=1e-7)
+    np.testing.assert_allclose(gs[:2], s[:2], rtol=1e-5, atol=1e-6)
+    np.testing.assert_allclose(gs[2:], s[2:], rtol=1e-4, atol=0)
+    print(f"{name}: LIF {gs[0]:.3f} CV {gs[1]:.3f} H {gs[2]:.4f} (ln E {np.log(wl.E):.4f}) "
+          f"switch {gs[3]:.4f} balance {gs[4]:.4f}")
+
+
 # ------------------------------------------------------------------------------------------ combine
 
 @pytest.mark.parametrize("T,E,k,C,d,ns,dt", [(1000, 8, 2, 1.0, 256, 0, "bf16"), (4096, 256, 8, 0.0, 7168, 1, "bf16"),

@@ -435,3 +435,66 @@ def test_forward_equals_combine_of_expert_rows():
         Y[off[e]:off[e + 1]] = oracle.expert_rows(x[rows], W1[e], W3[e], W2[e])
     np.testing.assert_allclose(oracle.combine_tc(Y, slot, w), oracle.forward_tc(x, idx, w, slot, W1, W3, W2, np.arange(T)),
                                rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------------ load statistics
+# "技术日报 2026-04-14" §4.4 states the balanced and collapsed values of the
+# diagnostics (token fraction 1/E, LIF = 1 balanced and = E collapsed, CV = 0
+# balanced, entropy largest for the uniform distribution); §4.2 states that the
+# Switch term is optimal at f_i = P_i = 1/N, where N * sum f_i P_i = 1.
+
+def test_load_stats_balanced_routing():
+    E, T, k = 8, 64, 2
+    idx = np.stack([np.arange(T) % E, (np.arange(T) + 3) % E], axis=1)
+    cnt = np.bincount(idx.ravel(), minlength=E)
+    f, P, s = oracle.load_stats(idx, cnt, np.full((T, E), 1.0 / E))
+    assert np.allclose(f, 1.0 / E, rtol=0, atol=1e-15) and np.allclose(P, 1.0 / E, rtol=0, atol=1e-15)
+    assert s[0] == pytest.approx(1.0, abs=1e-14) and s[1] == pytest.approx(0.0, abs=1e-14)
+    assert s[2] == pytest.approx(np.log(E), abs=1e-14)
+    assert s[3] == pytest.approx(1.0, abs=1e-14) and s[4] == pytest.approx(1.0, abs=1e-14)
+
+
+@pytest.mark.parametrize("E", [2, 8, 64, 256])
+def test_load_stats_collapsed_routing(E):
+    T = 50
+    idx = np.zeros((T, 1), np.int64)
+    cnt = np.bincount(idx.ravel(), minlength=E)
+    scores = np.zeros((T, E))
+    scores[:, 0] = 1.0
+    f, P, s = oracle.load_stats(idx, cnt, scores)
+    # f = (1, 0, ..., 0): population std sqrt(E - 1) / E around the mean 1 / E
+    assert s[0] == pytest.approx(E, rel=1e-15)
+    assert s[1] == pytest.approx(np.sqrt(E - 1.0), rel=1e-14)
+    assert s[2] == pytest.approx(0.0, abs=1e-15)
+    assert s[3] == pytest.approx(E, rel=1e-15) and s[4] == pytest.approx(E, rel=1e-15)
+
+
+def test_load_stats_hand_examples():
+    # k = 1, E = 2: f = f1 = (3/4, 1/4), P = (0.6, 0.4)
+    idx = np.array([[0], [0], [0], [1]])
+    scores = np.array([[0.9, 0.1], [0.7, 0.3], [0.5, 0.5], [0.3, 0.7]])
+    f, P, s = oracle.load_stats(idx, np.array([3, 1]), scores)
+    assert np.allclose(f, [0.75, 0.25], rtol=0, atol=1e-15) and np.allclose(P, [0.6, 0.4], rtol=0, atol=1e-15)
+    assert s[0] == pytest.approx(1.5) and s[1] == pytest.approx(0.5)          # std 0.25 / mean 0.5
+    assert s[2] == pytest.approx(-(0.6 * np.log(0.6) + 0.4 * np.log(0.4)), rel=1e-14)
+    assert s[3] == pytest.approx(2 * (0.75 * 0.6 + 0.25 * 0.4)) and s[4] == pytest.approx(1.1)
+    # k = 2, E = 3: first choices all expert 0, assignments (2, 1, 1)
+    idx = np.array([[0, 1], [0, 2]])
+    scores = np.array([[0.5, 0.3, 0.2], [0.6, 0.1, 0.3]])
+    f, P, s = oracle.load_stats(idx, np.array([2, 1, 1]), scores)
+    assert np.allclose(P, [0.55, 0.2, 0.25], rtol=0, atol=1e-15)
+    assert s[3] == pytest.approx(3 * 0.55, rel=1e-14)                          # f1 = (1, 0, 0)
+    assert s[4] == pytest.approx(3 * (0.5 * 0.55 + 0.25 * 0.2 + 0.25 * 0.25), rel=1e-14)
+    assert s[3] != pytest.approx(s[4])
+
+
+def test_load_stats_entropy_matches_scipy():
+    from scipy.stats import entropy
+    rng = np.random.default_rng(5)
+    for E in (4, 64, 256):
+        scores = rng.random((300, E)) ** 3
+        idx = np.argsort(-scores, axis=1, kind="stable")[:, :2]
+        cnt = np.bincount(idx.ravel(), minlength=E)
+        _, P, s = oracle.load_stats(idx, cnt, scores)
+        assert s[2] == pytest.approx(entropy(P), rel=1e-12)   # scipy normalises P, natural log
+        assert s[0] == pytest.approx(E * cnt.max() / cnt.sum(), rel=1e-14)
