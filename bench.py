@@ -164,6 +164,7 @@ def work_model(wl, off, E_used):
     """Algorithmic bytes and FLOPs per stage launch (bf16 b = 2 or fp32 b = 4).
     A = assignments computed; touched = experts with at least one row."""
     b = 4 if wl.dtype == "f32" else 2
+    bw = 1 if wl.dtype == "fp8w" else b   # bytes per stored expert weight (E4M3 codes)
     T, d, E, f = wl.T, wl.d, wl.E, wl.f
     A = int(off[-1])
     touched = int(E_used)
@@ -176,8 +177,11 @@ def work_model(wl, off, E_used):
     m["dispatch"] = {"bytes": (T * wl.k * 4 * 3 if wl.mode == "tc" else E * wl.ec_capacity * 4 + T * E * 4) + 2 * A * d * b,
                      "flops": 0}
     # grouped experts (up + down): touched weights, x_perm read, H written and read, Y written
-    m["ffn"] = {"bytes": touched * 3 * d * f * b + 2 * A * d * b + 2 * A * f * b
-                         + (3 * d * fs * b + 2 * Ts * d * b + 2 * Ts * fs * b),
+    # (FP8 weights: one byte per weight plus one fp32 scale per output channel)
+    sc = 4 * (2 * f + d) if wl.dtype == "fp8w" else 0
+    scs = 4 * (2 * fs + d) if (wl.dtype == "fp8w" and fs) else 0
+    m["ffn"] = {"bytes": touched * (3 * d * f * bw + sc) + 2 * A * d * b + 2 * A * f * b
+                         + (3 * d * fs * bw + scs + 2 * Ts * d * b + 2 * Ts * fs * b),
                 "flops": 6 * A * d * f + 6 * Ts * d * fs}
     m["combine"] = {"bytes": A * d * b + T * kslots * 8 + T * d * b + Ts * d * b, "flops": 2 * A * d}
     return m, A, touched
@@ -204,6 +208,8 @@ def run_gpu(args):
     wl = WORKLOADS[args.workload]
     if args.T:
         wl = wl.with_(T=args.T)
+    if args.fp8_weights:
+        wl = wl.with_(dtype="fp8w")
     if ws_n > 1:   # each replica gets its own batch of tokens
         wl = wl.with_(index=wl.index + 1000 * rank) if rank else wl
     inp = make_inputs(wl, dev)
@@ -416,11 +422,12 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "dtype": {"bf16": "bf16", "f32": "f32", "fp8w": "bf16 (E4M3 expert weights)"}[wl.dtype],
         "data": "synthetic (seeded; random-init expert weights)",
         "config": {"workload": wl.name, "T": T, "d": d, "E": wl.E, "d_ff": wl.f, "k": wl.k, "gate": wl.gate,
                    "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
                    "n_shared": wl.n_shared, "f_shared": wl.f_shared,
+                   "expert_weights": "e4m3 + fp32 scale per output channel" if wl.dtype == "fp8w" else wl.dtype,
                    "assignments_computed": A, "experts_touched": touched,
                    "l2": "inputs larger than L2: the expert weights read per step exceed 126 MB"
                          if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2",
@@ -555,6 +562,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256, help="largest oracle sample per reference step")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds the reference arm aims to take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8-weights", action="store_true",
+                    help="store the expert weights as FP8 E4M3 with per-channel scales (MOE_BF16_FP8W)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

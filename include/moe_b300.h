@@ -34,7 +34,10 @@
  *   - Row-major layouts.  Device buffers must be 16-byte aligned; `ws` and the
  *     packed weight buffer 256-byte aligned (any torch CUDA allocation is).
  *   - dtype MOE_BF16: x, W_r, weights, x_perm, Y and y are bf16 (fp32 accumulate);
- *     dtype MOE_F32: all of those are fp32 (no TF32 anywhere).
+ *     dtype MOE_F32: all of those are fp32 (no TF32 anywhere);
+ *     dtype MOE_BF16_FP8W: as MOE_BF16, except that moe_pack_weights stores the
+ *     expert weights as FP8 E4M3 with one fp32 scale per output channel (the
+ *     grouped FFN streams half the weight bytes; see moe_pack_weights).
  *     Scores and gate weights are always fp32; indices are int32.
  *   - Device-side waits are bounded.  A wait that gives up sets a device error
  *     word; moe_check_device_error reports it as MOE_ERR_TIMEOUT.
@@ -61,7 +64,7 @@ typedef enum {
 
 typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
 typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_mode;
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_BF16_FP8W = 2 } moe_dtype;
 typedef enum {
     MOE_STAGE_ROUTE = 0,
     MOE_STAGE_DISPATCH = 1,
@@ -84,9 +87,10 @@ typedef enum {
  *   ec_capacity: expert choice; tokens each expert takes (1..T).
  *   n_shared, f_shared: always-on shared experts (§3.4), each of hidden width
  *     f_shared; their outputs are added unweighted.
- *   dtype: MOE_BF16 or MOE_F32.
+ *   dtype: MOE_BF16, MOE_F32 or MOE_BF16_FP8W.
  * Build limits: MOE_BF16 needs d % 128 == 0, f % 64 == 0, f_shared % 64 == 0;
- * MOE_F32 needs d % 64 == 0, f % 64 == 0, f_shared % 64 == 0.
+ * MOE_F32 needs d % 64 == 0, f % 64 == 0, f_shared % 64 == 0;
+ * MOE_BF16_FP8W needs d % 256 == 0, f % 128 == 0, n_shared * f_shared % 128 == 0.
  */
 typedef struct moe_config {
     int32_t T, d, E, f, k;
@@ -127,6 +131,18 @@ moe_status moe_packed_weights_size(const moe_config *cfg, size_t *bytes);
  *   W1s, W3s: [n_shared][d][f_shared], W2s: [n_shared][f_shared][d] (NULL when
  *   n_shared == 0).  All in cfg->dtype, device memory, read only.
  *   packed: device buffer of moe_packed_weights_size bytes, written on `stream`.
+ * MOE_BF16_FP8W (weights given in bf16): every output channel of every expert
+ *   matrix (a hidden column of W1 and of W3, a model column of W2) gets the scale
+ *   s = amax / 448 over its K inputs (fp32: amax of |w|, divided by the largest
+ *   E4M3 value), and its weights are stored as the E4M3 code of w / s (fp32
+ *   division, round to nearest even, saturated to +-448; s = 0 for an all-zero
+ *   channel, whose codes are 0).  The GEMMs compute with q * s ("技术日报" §5
+ *   lists FP8 expert weights; this is weight-only quantisation, activations stay
+ *   bf16).  Several shared experts are packed as one merged expert, so the
+ *   scale of a W2 output column covers all shared experts' rows of that column.
+ *   The packed buffer is about half the bf16 one.  The grouped FFN expands the
+ *   codes to bf16 in shared memory; on B300 this mode runs slower than MOE_BF16
+ *   (it saves memory, not time).
  */
 moe_status moe_pack_weights(const moe_config *cfg, const void *W1, const void *W3, const void *W2,
                             const void *W1s, const void *W3s, const void *W2s, void *packed,

@@ -18,7 +18,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_MISALIGNED = 0, 1, 2, 
 MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_GATE_SOFTMAX, MOE_GATE_SIGMOID = 0, 1
 MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_BF16_FP8W = 0, 1, 2
 MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, MOE_STAGE_FORWARD = range(5)
 
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
@@ -121,7 +121,12 @@ def config(T, d, E, f, k=1, gate="softmax", mode="tc", renormalize=True, capacit
     return moe_config(T, d, E, f, k, MOE_GATE_SIGMOID if gate == "sigmoid" else MOE_GATE_SOFTMAX,
                       MOE_EXPERT_CHOICE if mode == "ec" else MOE_TOKEN_CHOICE, int(bool(renormalize)),
                       float(capacity_factor), int(ec_capacity), int(n_shared), int(f_shared),
-                      MOE_F32 if dtype in ("f32", "fp32", "float32") else MOE_BF16)
+                      _DTYPES[dtype])
+
+
+# run dtype names: "fp8w" = bf16 activations with FP8 E4M3 expert weights
+_DTYPES = {"f32": MOE_F32, "fp32": MOE_F32, "float32": MOE_F32, "bf16": MOE_BF16, "bfloat16": MOE_BF16,
+           "fp8w": MOE_BF16_FP8W}
 
 
 def config_from_workload(w, T=None) -> moe_config:

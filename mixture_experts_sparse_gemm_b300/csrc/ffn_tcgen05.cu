@@ -8,6 +8,9 @@
 // Down: A = H rows, B = packed W2 tile images, K = f, 256-wide tiles when d % 256 == 0.
 // Fused: both GEMMs in one persistent launch, down tiles after up tiles, each
 //     down tile waiting (on the device) for the up tiles that produce its H rows.
+// FP8 weights (MOE_BF16_FP8W): the same launches with the W8 kernel, which streams
+//     E4M3 tile images, expands them to bf16 in shared memory and applies the
+//     per-column scales in the epilogue.
 #include <algorithm>
 
 #include "tc_gemm.cuh"
@@ -35,9 +38,14 @@ bool up_gemm(const moe_config &c, const Sizes &z, const void *x_perm, const int3
     G.K0 = c.d;
     G.K1 = c.d;
     G.b_rows0 = 2 * c.f;
+    const size_t wb = fp8_weights(c) ? 1 : 2;   // bytes per stored weight
     G.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w13);
     G.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w13s);
-    G.bt_seg0 = (size_t)2 * c.f * c.d * 2;
+    G.bt_seg0 = (size_t)2 * c.f * c.d * wb;
+    if (fp8_weights(c)) {
+        G.sc0 = reinterpret_cast<const float *>(pk + L.sc13);
+        G.sc1 = reinterpret_cast<const float *>(pk + L.sc13s);
+    }
     G.img_rows = bn;
     G.C0 = H;
     G.C1 = Hs;
@@ -62,9 +70,14 @@ bool down_gemm(const moe_config &c, const Sizes &z, const void *H, const void *H
     G.K0 = c.f;
     G.K1 = shared ? fs : c.f;
     G.b_rows0 = c.d;
+    const size_t wb = fp8_weights(c) ? 1 : 2;
     G.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w2);
     G.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w2s);
-    G.bt_seg0 = (size_t)c.d * c.f * 2;
+    G.bt_seg0 = (size_t)c.d * c.f * wb;
+    if (fp8_weights(c)) {
+        G.sc0 = reinterpret_cast<const float *>(pk + L.sc2);
+        G.sc1 = reinterpret_cast<const float *>(pk + L.sc2s);
+    }
     G.img_rows = bn;
     G.C0 = Y;
     G.C1 = static_cast<__nv_bfloat16 *>(Y) + (size_t)z.rows_routed * c.d;
@@ -92,6 +105,7 @@ cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const voi
     if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], m)) return cudaErrorInvalidValue;
     g.err = err;
     const int64_t tiles = max_mtiles(c, z) * std::max(g.p[0].g.nblk_routed, g.p[0].g.nblk_shared);
+    if (fp8_weights(c)) return launch_gemm<256, kEpiSwiGLU, true>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
     return g.p[0].img_rows == 256 ? launch_gemm<256, kEpiSwiGLU>(m.a0, m.a1, m.a0, m.a1, g, tiles, s)
                                   : launch_gemm<128, kEpiSwiGLU>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
 }
@@ -107,6 +121,7 @@ cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const v
     g.row_token = row_token;
     g.row_gate = row_gate;
     const int64_t tiles = max_mtiles(c, z) * g.p[0].g.nblk_routed;
+    if (fp8_weights(c)) return launch_gemm<256, kEpiStore, true>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
     return g.p[0].img_rows == 256 ? launch_gemm<256, kEpiStore>(m.a0, m.a1, m.a0, m.a1, g, tiles, s)
                                   : launch_gemm<128, kEpiStore>(m.a0, m.a1, m.a0, m.a1, g, tiles, s);
 }
@@ -126,6 +141,7 @@ cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const 
     cudaError_t e = cudaMemsetAsync(dep, 0, sizeof(int) * ffn_dep_counters(c), s);
     if (e != cudaSuccess) return e;
     const int64_t tiles = max_mtiles(c, z) * (g.p[0].g.nblk_routed + g.p[1].g.nblk_routed);
+    if (fp8_weights(c)) return launch_gemm<256, kEpiFfn, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
     return launch_gemm<256, kEpiFfn>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
 }
 

@@ -77,7 +77,7 @@ RouteWs route_ws(const moe_config &c) {
     RouteWs w{};
     w.scores_t = k.take(c.mode == MOE_EXPERT_CHOICE ? sizeof(float) * (size_t)c.E * c.T : 0);
     w.psum_rows = k.take(sizeof(float) * kPsumRows * (size_t)c.E);   // router score sums, see moe_route
-    w.wr_t = k.take(c.dtype == MOE_BF16 && route_tcgen05_supported(c) ? route_tcgen05_scratch_bytes(c) : 0);
+    w.wr_t = k.take(bf16_acts(c) && route_tcgen05_supported(c) ? route_tcgen05_scratch_bytes(c) : 0);
     w.total = k.off;
     return w;
 }
@@ -99,7 +99,7 @@ DispatchWs dispatch_ws(const moe_config &c) {
 }
 
 // the two expert GEMMs run as one persistent launch when both use 256-wide tiles
-bool ffn_fused(const moe_config &c) { return c.dtype == MOE_BF16 && ffn_fused_supported(c); }
+bool ffn_fused(const moe_config &c) { return bf16_acts(c) && ffn_fused_supported(c); }
 
 struct FfnWs {
     size_t H, Hs, dep, total;
@@ -150,7 +150,7 @@ moe_status do_route(const moe_config &c, const void *x, const void *W_r, const f
     cudaError_t e;
     if (rows && cudaMemsetAsync(rows, 0, sizeof(float) * kPsumRows * (size_t)c.E, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (c.dtype == MOE_BF16 && route_tcgen05_supported(c))
+    if (bf16_acts(c) && route_tcgen05_supported(c))
         e = launch_route_tcgen05(c, x, W_r, lo, sb, idx, w, scores_t, rows, ws + L.wr_t, err, s);
     else
         e = launch_route_simt(c, x, W_r, lo, sb, idx, w, scores_t, rows, err, s);
@@ -180,17 +180,17 @@ moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, c
     if (ffn_fused(c))
         return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, x, H, Hs, Y,
                                                   reinterpret_cast<int *>(ws + L.dep), err, s));
-    cudaError_t e = (c.dtype == MOE_BF16) ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
+    cudaError_t e = bf16_acts(c) ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
                                           : launch_ffn_up_simt(c, z, x_perm, off, packed, x, H, Hs, s);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = (c.dtype == MOE_BF16) ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
+    e = bf16_acts(c) ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
                               : launch_ffn_down_simt(c, z, H, Hs, off, packed, Y, s);
     return from_cuda(e);
 }
 
 // kernels enqueued per stage; mirrors the launch sequence of the do_* bodies above
 int route_launches(const moe_config &c) {
-    const int base = (c.dtype == MOE_BF16 && route_tcgen05_supported(c)) ? route_tcgen05_launches(c) : 1;
+    const int base = (bf16_acts(c) && route_tcgen05_supported(c)) ? route_tcgen05_launches(c) : 1;
     return base + (c.mode == MOE_EXPERT_CHOICE ? 1 : 0);
 }
 int dispatch_launches(const moe_config &c) {
@@ -200,7 +200,7 @@ int dispatch_launches(const moe_config &c) {
 // moe_forward folds the combine into the down GEMM when every token has one
 // expert and there are no shared experts (the row -> token map is a permutation)
 bool gated_down(const moe_config &c) {
-    return c.dtype == MOE_BF16 && c.mode == MOE_TOKEN_CHOICE && c.k == 1 && c.n_shared == 0;
+    return bf16_acts(c) && c.mode == MOE_TOKEN_CHOICE && c.k == 1 && c.n_shared == 0;
 }
 
 }  // namespace
@@ -227,10 +227,16 @@ PackedLayout packed_layout(const moe_config &c) {
     const Sizes z = sizes_of(c);
     Carver k;
     PackedLayout L{};
-    L.w13 = k.take((size_t)c.E * 2 * c.f * c.d * z.elt);
-    L.w2 = k.take((size_t)c.E * c.d * c.f * z.elt);
-    L.w13s = k.take((size_t)2 * z.fs_tot * c.d * z.elt);
-    L.w2s = k.take((size_t)c.d * z.fs_tot * z.elt);
+    const size_t we = fp8_weights(c) ? 1 : z.elt;   // bytes per stored weight
+    L.w13 = k.take((size_t)c.E * 2 * c.f * c.d * we);
+    L.w2 = k.take((size_t)c.E * c.d * c.f * we);
+    L.w13s = k.take((size_t)2 * z.fs_tot * c.d * we);
+    L.w2s = k.take((size_t)c.d * z.fs_tot * we);
+    const bool sc = fp8_weights(c);
+    L.sc13 = k.take(sc ? sizeof(float) * (size_t)c.E * 2 * c.f : 0);
+    L.sc2 = k.take(sc ? sizeof(float) * (size_t)c.E * c.d : 0);
+    L.sc13s = k.take(sc ? sizeof(float) * (size_t)2 * z.fs_tot : 0);
+    L.sc2s = k.take(sc ? sizeof(float) * (size_t)c.d : 0);
     L.total = k.off;
     return L;
 }
@@ -292,7 +298,7 @@ moe_status moe_validate_config(const moe_config *cfg) {
     if (c.T < 0 || c.d <= 0 || c.f <= 0 || c.E <= 0) return MOE_ERR_INVALID_ARG;
     if (c.gate != MOE_GATE_SOFTMAX && c.gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c.mode != MOE_TOKEN_CHOICE && c.mode != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
-    if (c.dtype != MOE_F32 && c.dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (c.dtype != MOE_F32 && c.dtype != MOE_BF16 && c.dtype != MOE_BF16_FP8W) return MOE_ERR_INVALID_ARG;
     if (c.n_shared < 0 || (c.n_shared > 0 && c.f_shared <= 0)) return MOE_ERR_INVALID_ARG;
     if (std::isnan(c.capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (c.E > kMaxE) return MOE_ERR_UNSUPPORTED;
@@ -309,6 +315,8 @@ moe_status moe_validate_config(const moe_config *cfg) {
     if (fs > INT32_MAX) return MOE_ERR_UNSUPPORTED;
     if (c.dtype == MOE_BF16) {
         if (c.d % 128 != 0 || c.f % 64 != 0 || fs % 64 != 0) return MOE_ERR_UNSUPPORTED;
+    } else if (c.dtype == MOE_BF16_FP8W) {   // 256-wide tiles for both GEMMs (one fused launch)
+        if (c.d % 256 != 0 || c.f % 128 != 0 || fs % 128 != 0) return MOE_ERR_UNSUPPORTED;
     } else {
         if (c.d % 64 != 0 || c.f % 64 != 0 || fs % 64 != 0) return MOE_ERR_UNSUPPORTED;
     }
@@ -462,7 +470,7 @@ moe_status moe_grouped_ffn_up(const moe_config *cfg, const void *x_perm, const i
     if (st != MOE_OK || c.T == 0) return st;
     const Sizes z = sizes_of(c);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return from_cuda(c.dtype == MOE_BF16 ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
+    return from_cuda(bf16_acts(c) ? launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, H, Hs, err, s)
                                          : launch_ffn_up_simt(c, z, x_perm, off, packed, x, H, Hs, s));
 }
 
@@ -480,7 +488,7 @@ moe_status moe_grouped_ffn_down(const moe_config *cfg, const void *H, const void
     if (st != MOE_OK || c.T == 0) return st;
     const Sizes z = sizes_of(c);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return from_cuda(c.dtype == MOE_BF16 ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
+    return from_cuda(bf16_acts(c) ? launch_ffn_down_tcgen05(c, z, H, Hs, off, packed, Y, err, s)
                                          : launch_ffn_down_simt(c, z, H, Hs, off, packed, Y, s));
 }
 

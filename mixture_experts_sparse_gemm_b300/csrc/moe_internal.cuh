@@ -21,6 +21,11 @@ constexpr unsigned kErrBadIndex = 2u;     // an expert or token id outside its r
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// bf16 activations (MOE_BF16, MOE_BF16_FP8W): the tensor-core paths
+inline bool bf16_acts(const moe_config &c) { return c.dtype == MOE_BF16 || c.dtype == MOE_BF16_FP8W; }
+// expert weights stored as E4M3 codes + per-output-channel fp32 scales
+inline bool fp8_weights(const moe_config &c) { return c.dtype == MOE_BF16_FP8W; }
+
 // ----------------------------------------------------------------------------- sizes
 struct Sizes {
     int64_t rows_routed;   // T*k (token choice) or E*cap (expert choice)
@@ -50,13 +55,23 @@ __host__ __device__ inline size_t tiled_offset(int p, int i, int BN, int K) {
     return (((size_t)nb * (K / 64) + kb) * BN + r) * 64 + (size_t)((ch ^ (r & 7)) * 8 + w);
 }
 
+// Byte offset of (row p, column i) of a [N][K] FP8 operand stored as tile images:
+// BN rows x 64 one-byte columns per tile, N-tile major then K-tile, rows plain
+// (the converter warps of the grouped GEMM expand a tile to the swizzled bf16 layout).
+__host__ __device__ inline size_t tiled_offset8(int p, int i, int BN, int K) {
+    const int nb = p / BN, r = p % BN, kb = i / 64;
+    return (((size_t)nb * (K / 64) + kb) * BN + r) * 64 + (size_t)(i % 64);
+}
+
 // Byte offsets inside the packed weight buffer.
 //   w13 : [E][2f][d]      up-projection, K-major, W1/W3 interleaved in groups of kGroup rows
 //   w2  : [E][d][f]       down-projection, K-major
 //   w13s: [2*fs_tot][d]   shared experts merged along the hidden dimension
 //   w2s : [d][fs_tot]
+//   FP8 weights: the same matrices as E4M3 codes (one byte each), then fp32 scales
+//   sc13: [E][2f] and sc2: [E][d] per output row of w13 / w2, sc13s: [2*fs_tot], sc2s: [d]
 struct PackedLayout {
-    size_t w13, w2, w13s, w2s, total;
+    size_t w13, w2, w13s, w2s, sc13, sc2, sc13s, sc2s, total;
 };
 PackedLayout packed_layout(const moe_config &c);
 

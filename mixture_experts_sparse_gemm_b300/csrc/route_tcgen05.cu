@@ -87,7 +87,7 @@ cudaError_t launch_partial_n(int npad, const CUtensorMap &a0, const CUtensorMap 
 
 }  // namespace
 
-bool route_tcgen05_supported(const moe_config &c) { return c.dtype == MOE_BF16 && c.E <= kMaxE && c.d % 64 == 0; }
+bool route_tcgen05_supported(const moe_config &c) { return bf16_acts(c) && c.E <= kMaxE && c.d % 64 == 0; }
 
 size_t route_tcgen05_scratch_bytes(const moe_config &c) {
     const int s = route_splits(c);

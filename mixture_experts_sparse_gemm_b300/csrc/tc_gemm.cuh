@@ -9,6 +9,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
 //               thread), then the epilogue of the instantiation; it overlaps the
 //               next tile's main loop through the second accumulator
+//   warps 6..13 (W8 only) converters: the FP8 weight tile of a stage -> the bf16
+//               tile of the same stage, which the MMA reads; the per-column
+//               weight scales are applied in the epilogue
 // Tiles never straddle segments: the tile table is built on the device from
 // off[] (segment s < E = routed expert s, segment E = merged shared experts), and
 // a segment's last M tile reads rows past its end (the next segment's rows, or
@@ -25,6 +28,7 @@
 //               Choice, the softmax scores written expert-major.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <float.h>
 
 #include "tc_common.cuh"
@@ -44,14 +48,20 @@ constexpr int kEpiPartial = 3;  // split-K partial sums: fp32 rows of C0[split][
 // router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
 constexpr int kEpiRoute = 10;
 
-template <int BN>
+// W8: B arrives as an FP8 E4M3 tile (BN x 64 bytes) in each stage; eight converter
+// warps expand it into the bf16 tile of the same stage, which the MMA reads.
+// Stage layout: A (bf16) | B (bf16, MMA operand) | B8 (FP8, W8 only).
+template <int BN, bool W8 = false>
 struct TcCfg {
     static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (BN == 256) ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int kBBytes = BN * kBK * 2;      // bf16 B tile, as the MMA reads it
+    static constexpr int kB8Bytes = BN * kBK;         // FP8 B tile, as the copy brings it (W8)
+    static constexpr int kStageBytes = kABytes + kBBytes + (W8 ? kB8Bytes : 0);
+    static constexpr int kStages = W8 ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
+    static constexpr int kConvWarps = W8 ? 8 : 0;
+    static constexpr int kThreadsCta = kThreads + 32 * kConvWarps;
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-    static constexpr int kBarBytes = (2 * kStages + 5) * 8;
+    static constexpr int kBarBytes = (3 * kStages + 5) * 8;
     static constexpr int kMiscBytes = 64 + sizeof(int) * (6 * (kMaxE + 2));
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kMiscBytes;
 };
@@ -84,6 +94,9 @@ struct TcGemm {
     // > 1: the K range is split over ksplit tiles (the N-block index is the split;
     // one N tile of width BN covers all of N), each writing its partial sums
     int ksplit;
+    // FP8 weights (W8 kernels): fp32 scale of every B row (output column), routed
+    // [E][b_rows0] and shared [N]; applied to the accumulator in the epilogue
+    const float *sc0, *sc1;
 };
 
 struct TcArgs {
@@ -255,9 +268,21 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
 
 // Tile epilogues (all 32 lanes of each epilogue warp run them; `row` is the
 // thread's accumulator row, `rows` the valid rows of the tile).
+// sc (FP8 weights, else null): scales of the tile's BN accumulator columns
+__device__ __forceinline__ void scale16(uint32_t (&v)[16], const float *sc) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 f = *reinterpret_cast<const float4 *>(sc + 4 * q);
+        v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) * f.x);
+        v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * f.y);
+        v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * f.z);
+        v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * f.w);
+    }
+}
+
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, int ldc, int grow, int row, int rows,
-                                           int nb) {
+                                           int nb, const float *sc) {
 #pragma unroll 1
     for (int grp = 0; grp < BN / 128; ++grp) {
 #pragma unroll 1
@@ -266,6 +291,10 @@ __device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, in
             tmem_ld16(taddr + grp * 128 + c * 16, g);
             tmem_ld16(taddr + grp * 128 + 64 + c * 16, u);
             tmem_ld_wait();
+            if (sc) {
+                scale16(g, sc + grp * 128 + c * 16);
+                scale16(u, sc + grp * 128 + 64 + c * 16);
+            }
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -284,12 +313,13 @@ __device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, in
 
 template <int BN>
 __device__ __forceinline__ void epi_store(uint32_t taddr, __nv_bfloat16 *Cp, int ldc, size_t orow, float scale, int row,
-                                          int rows, int nb) {
+                                          int rows, int nb, const float *sc) {
 #pragma unroll 1
     for (int c = 0; c < BN / 16; ++c) {
         uint32_t v[16];
         tmem_ld16(taddr + c * 16, v);
         tmem_ld_wait();
+        if (sc) scale16(v, sc + c * 16);
         uint32_t o[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -302,18 +332,44 @@ __device__ __forceinline__ void epi_store(uint32_t taddr, __nv_bfloat16 *Cp, int
     }
 }
 
+// 16 E4M3 codes -> 16 bf16, exactly (every E4M3 value is a bf16 value), without
+// conversion instructions: a code s.eeee.mmm is placed as the bf16 bit pattern
+// s.0000eeee.mmm0000 -- the value 2^(e-127) (1 + m/8), or for e = 0 the bf16
+// subnormal (m/8) 2^-126 -- and one exact bf16 multiply by 2^120 moves the
+// exponent bias from 127 to 7: 2^(e-7) (1 + m/8), resp. (m/8) 2^-6, the E4M3 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t x) {   // x = 0x00bb00aa
+    const uint32_t bits = ((x << 4) & 0x07F007F0u) | ((x << 8) & 0x80008000u);
+    const uint32_t two120 = 0x7B807B80u;   // bf16 2^120, twice
+    const __nv_bfloat162 r = __hmul2(*reinterpret_cast<const __nv_bfloat162 *>(&bits),
+                                     *reinterpret_cast<const __nv_bfloat162 *>(&two120));
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
+
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &v, uint4 &lo, uint4 &hi) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        // bytes 0,1 and 2,3 of the word into the low byte of each 16-bit half
+        o[2 * i] = e4m3x2_to_bf16x2(__byte_perm(w[i], 0u, 0x4140));
+        o[2 * i + 1] = e4m3x2_to_bf16x2(__byte_perm(w[i], 0u, 0x4342));
+    }
+    lo = make_uint4(o[0], o[1], o[2], o[3]);
+    hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // Where a tile lives: phase (GEMM of a kEpiFfn launch), segment, M and N block.
 struct TileAt {
     int phase, s, mb, nb;
 };
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int EPI, bool W8>
+__global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                            const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
                            TcArgs a) {
-    using C = TcCfg<BN>;
+    using C = TcCfg<BN, W8>;
     constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -324,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *tfull = bars + 2 * C::kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *conv = drain + 1;   // W8: the bf16 B tile of stage s written and fenced (converter warps)
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(conv + C::kStages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *tile_start0 = reinterpret_cast<int *>(tmem_holder + 16);   // tiles of phase 0 per segment
     int *tile_start1 = tile_start0 + (kMaxE + 2);                   // tiles of phase 1 per segment
@@ -335,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if constexpr (EPI > kEpiRoute) {
-        for (int e = threadIdx.x; e < kMaxE; e += kThreads) psum_cta[e] = 0.f;   // before the first barrier
+        for (int e = threadIdx.x; e < kMaxE; e += C::kThreadsCta) psum_cta[e] = 0.f;   // before the first barrier
     }
 
     if (threadIdx.x == 0) {
@@ -348,6 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&tempty[i]), 4);
         }
         mbar_init(smem_u32(drain), 1);
+        if (W8)
+            for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&conv[st]), C::kConvWarps);
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tmap(&tmA0);
@@ -451,13 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 krange(t, G, kb0, nk);
                 const uint8_t *bt = nullptr;
                 size_t img_bytes = 0;
+                constexpr int kBCopy = W8 ? C::kB8Bytes : C::kBBytes;   // B bytes per stage
                 if (G.Bt0) {
                     // rows [nb*BN, nb*BN + BN) of the N dimension are slice `sub` of image `img`;
                     // image rows are stored consecutively, so a slice is contiguous too
                     const int per = G.img_rows / BN, img = t.nb / per, sub = t.nb % per;
-                    img_bytes = (size_t)G.img_rows * kBK * 2;
+                    img_bytes = (size_t)G.img_rows * kBK * (W8 ? 1 : 2);
                     bt = (routed ? G.Bt0 + (size_t)t.s * G.bt_seg0 : G.Bt1) + (size_t)img * nk * img_bytes +
-                         (size_t)sub * C::kBBytes;
+                         (size_t)sub * kBCopy;
                 }
                 for (int kb = 0; kb < nk; ++kb) {
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) {
@@ -466,10 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
-                    mbar_arrive_expect_tx(fb, C::kStageBytes);
+                    mbar_arrive_expect_tx(fb, C::kABytes + kBCopy);   // A + B (FP8 for W8)
                     tma_load_2d(smem_u32(st), mA, (kb0 + kb) * kBK, arow, fb);
                     if (bt)
-                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)(kb0 + kb) * img_bytes, C::kBBytes, fb);
+                        bulk_load(smem_u32(st + C::kABytes + (W8 ? C::kBBytes : 0)), bt + (size_t)(kb0 + kb) * img_bytes,
+                                  kBCopy, fb);
                     else
                         tma_load_2d(smem_u32(st + C::kABytes), mB, (kb0 + kb) * kBK, brow, fb);
                     ++issued;
@@ -522,6 +583,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (W8 && !wait_bounded(smem_u32(&conv[stage]), phase, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
                     fence_after();
                     const uint32_t sa = smem_u32(tiles + (size_t)stage * C::kStageBytes);
                     const uint64_t adesc = sdesc_k128(sa);
@@ -545,6 +610,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(smem_u32(drain));
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else if (W8 && warp >= 6) {
+        // ---------------------------------------------------------------- converter (W8)
+        // k block j (stage j % kStages): the FP8 tile -> the stage's bf16 tile in the
+        // 128-byte swizzled K-major layout the MMA descriptor expects.  Thread q of 256
+        // converts the 16-byte chunks q, q + 256, ... (contiguous per warp): chunk c is
+        // row c / 4, bytes 16 (c % 4).. of the row = K elements 16 (c % 4)..+15, which
+        // land in bf16 chunks 2 (c % 4) and 2 (c % 4) + 1, swizzled by row % 8.  Lane 0
+        // polls the barrier; __syncwarp orders the other lanes' reads after it.
+        const int q0 = threadIdx.x - kThreads;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const TileAt t = locate(tile);
+            int kb0, nk;
+            krange(t, a.p[t.phase], kb0, nk);
+            for (int kb = 0; kb < nk; ++kb) {
+                int okw = 1;
+                if (lane == 0) okw = wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err);
+                if (!__shfl_sync(0xffffffffu, okw, 0)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
+                const uint8_t *src = st + C::kABytes + C::kBBytes;
+                uint8_t *dst = st + C::kABytes;
+#pragma unroll
+                for (int c = q0; c < C::kB8Bytes / 16; c += 32 * C::kConvWarps) {
+                    const int r = c >> 2, c8 = c & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + (size_t)c * 16);
+                    uint4 lo, hi;
+                    e4m3x16_to_bf16(v, lo, hi);
+                    uint8_t *row = dst + (size_t)r * 128;
+                    *reinterpret_cast<uint4 *>(row + (((2 * c8) ^ (r & 7)) << 4)) = lo;
+                    *reinterpret_cast<uint4 *>(row + (((2 * c8 + 1) ^ (r & 7)) << 4)) = hi;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // st.shared -> MMA reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&conv[stage]));
+                if (++stage == C::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
         }
     } else {
@@ -586,8 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? G.C0 : G.C1);
                 const int ldc = routed ? G.ldc0 : G.ldc1;
                 const bool up = (EPI == kEpiSwiGLU) || (EPI == kEpiFfn && t.phase == 0);
+                // W8: scales of this tile's BN output columns
+                const float *sc =
+                    W8 ? (routed ? G.sc0 + (size_t)t.s * G.b_rows0 : G.sc1) + (size_t)t.nb * BN : nullptr;
                 if (up) {
-                    epi_swiglu<BN>(taddr, Cp, ldc, grow, row, rows, t.nb);
+                    epi_swiglu<BN>(taddr, Cp, ldc, grow, row, rows, t.nb, sc);
                 } else {
                     size_t orow = (size_t)grow;
                     float scale = 1.f;
@@ -596,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         orow = (size_t)tok;
                         scale = a.row_gate[tok];
                     }
-                    epi_store<BN>(taddr, Cp, ldc, orow, scale, row, rows, t.nb);
+                    epi_store<BN>(taddr, Cp, ldc, orow, scale, row, rows, t.nb, sc);
                 }
             }
             fence_before();
@@ -621,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (EPI > kEpiRoute) {
         if (a.route.psum_rows) {   // this CTA's router score sums into its row: one atomic per expert
             float *row = a.route.psum_rows + (size_t)(blockIdx.x % kPsumRows) * a.route.E;
-            for (int e = threadIdx.x; e < a.route.E; e += kThreads) atomicAdd(row + e, psum_cta[e]);
+            for (int e = threadIdx.x; e < a.route.E; e += C::kThreadsCta) atomicAdd(row + e, psum_cta[e]);
         }
     }
     if (warp == 1) {
@@ -633,12 +746,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Persistent launch: one CTA per SM (at most max_tiles).  A kEpiFfn launch has CTAs
 // waiting on other CTAs' up tiles, so it is a cooperative launch (all CTAs resident).
-template <int BN, int EPI>
+template <int BN, int EPI, bool W8 = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
                         const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args, int64_t max_tiles,
                         cudaStream_t s) {
-    auto kern = tc_grouped_gemm_kernel<BN, EPI>;
-    const size_t smem = TcCfg<BN>::kSmem;
+    auto kern = tc_grouped_gemm_kernel<BN, EPI, W8>;
+    constexpr int kBlock = TcCfg<BN, W8>::kThreadsCta;
+    const size_t smem = TcCfg<BN, W8>::kSmem;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     int grid = num_sms();
@@ -648,18 +762,18 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
         void *params[] = {const_cast<CUtensorMap *>(&a0), const_cast<CUtensorMap *>(&a1),
                           const_cast<CUtensorMap *>(&b0), const_cast<CUtensorMap *>(&b1),
                           const_cast<CUtensorMap *>(&a2), const_cast<CUtensorMap *>(&a3), &targs};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kThreads), params,
+        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kBlock), params,
                                            smem, s);
     }
-    kern<<<grid, kThreads, smem, s>>>(a0, a1, b0, b1, a2, a3, args);
+    kern<<<grid, kBlock, smem, s>>>(a0, a1, b0, b1, a2, a3, args);
     return cudaGetLastError();
 }
 
 // Single-GEMM launches pass their A maps again for the unused second phase.
-template <int BN, int EPI>
+template <int BN, int EPI, bool W8 = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
                         const TcArgs &args, int64_t max_tiles, cudaStream_t s) {
-    return launch_gemm<BN, EPI>(a0, a1, b0, b1, a0, a1, args, max_tiles, s);
+    return launch_gemm<BN, EPI, W8>(a0, a1, b0, b1, a0, a1, args, max_tiles, s);
 }
 
 }  // namespace

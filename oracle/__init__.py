@@ -193,6 +193,57 @@ def expert_rows(X, W1, W3, W2, scale=None, nthreads=1):
     return out
 
 
+# ------------------------------------------------------------------ FP8 (E4M3) expert weights
+E4M3_MAX = 448.0   # largest finite E4M3 value: 1.75 * 2^8
+
+
+def e4m3_round(x):
+    """Round to the nearest FP8 E4M3 value, ties to even, saturating at +-448.
+
+    E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities):
+    normal values (1 + m/8) * 2^(e-7) for e = 1..15, subnormals (m/8) * 2^-6, so the
+    spacing is 2^(E-3) inside the binade [2^E, 2^(E+1)) for E >= -6 and 2^-9 below
+    2^-6.  The value is scaled by its spacing (exact in fp64, a power of two),
+    rounded half to even, scaled back, then clamped to the largest finite value."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    out = np.zeros_like(a)
+    nz = a > 0
+    _, ex = np.frexp(a[nz])                       # a = m * 2^ex, m in [0.5, 1): binade E = ex - 1
+    E = np.maximum(ex.astype(np.float64) - 1.0, -6.0)
+    spacing = np.ldexp(1.0, (E - 3.0).astype(np.int64))
+    out[nz] = np.minimum(np.round(a[nz] / spacing) * spacing, E4M3_MAX)
+    return np.copysign(out, x)
+
+
+def quantize_e4m3_columns(W):
+    """Per-output-channel E4M3 quantisation of W[K][N] (channel = column n, over
+    its K inputs), as moe_pack_weights defines it in fp32: s_n = amax_n / 448,
+    code = E4M3(w / s_n) (fp32 division, then round to nearest even, saturate);
+    s_n = 0 and codes 0 for an all-zero column.  Returns (q [K][N] as the E4M3
+    values in fp64, s [N] fp32)."""
+    W = np.asarray(W, np.float32)
+    amax = np.abs(W).max(axis=0)
+    s = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    q = np.zeros(W.shape, np.float64)
+    nzc = s > 0
+    v = (W[:, nzc] / s[nzc]).astype(np.float32)   # fp32 division, round to nearest
+    q[:, nzc] = e4m3_round(v)
+    return q, s
+
+
+def expert_rows_fp8(x, q1, s1, q3, s3, q2, s2):
+    """SwiGLU expert with E4M3 weights q (values) and per-column fp32 scales s, in
+    fp64: gate = (x q1) * s1, up = (x q3) * s3 per hidden column, h = SiLU(gate) * up,
+    out = (h q2) * s2 per model column -- the expert of "lnwmold.com GPT-4 MoE
+    article" §2.2 with W = q * s, the scale taken out of each column's sum."""
+    x = np.asarray(x, np.float64)
+    g = (x @ np.asarray(q1, np.float64)) * np.asarray(s1, np.float64)
+    u = (x @ np.asarray(q3, np.float64)) * np.asarray(s3, np.float64)
+    h = g / (1.0 + np.exp(-g)) * u
+    return (h @ np.asarray(q2, np.float64)) * np.asarray(s2, np.float64)
+
+
 def load_stats(topk_idx, cnt_raw, scores, expert_choice=False):
     """Load statistics of one routing, from the definitions of "技术日报 2026-04-14"
     §4.4 (token fraction, LIF, CV, router entropy) and §4.2 (the Switch auxiliary

@@ -492,3 +492,239 @@ def test_forward_empty_batch(cuda_device):
     B.moe_forward(cfg, x, torch.zeros(d, E, dtype=torch.bfloat16, device=dev), None, None, layer.packed, y,
                   layer.workspace())
     _check_device_error()
+
+
+# ------------------------------------------------------------------------------------- FP8 expert weights
+# MOE_BF16_FP8W: moe_pack_weights stores every expert matrix as E4M3 codes with one
+# fp32 scale per output channel; the grouped FFN expands the codes to bf16 in
+# shared memory and applies the scales in its epilogue.  Packing is compared bit for
+# bit with the oracle's quantiser; layer outputs against the oracle's fp64 expert
+# with the same codes and scales, within the bf16 bar.
+
+def _e4m3_decode():
+    """Value of every E4M3 code (NaN codes -> nan), from the format's definition."""
+    out = np.empty(256)
+    for code in range(256):
+        sgn = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 7
+        if e == 15 and m == 7:
+            out[code] = np.nan
+        elif e == 0:
+            out[code] = sgn * (m / 8.0) * 2.0 ** -6
+        else:
+            out[code] = sgn * (1 + m / 8.0) * 2.0 ** (e - 7)
+    return out
+
+
+E4M3 = _e4m3_decode()
+
+
+def _packed_offsets(E, d, f, fs):
+    """Byte offsets of the FP8 packed buffer (regions 1024-byte aligned, in order)."""
+    sizes = [("w13", E * 2 * f * d), ("w2", E * d * f), ("w13s", 2 * fs * d), ("w2s", d * fs),
+             ("sc13", 4 * E * 2 * f), ("sc2", 4 * E * d), ("sc13s", 4 * 2 * fs), ("sc2s", 4 * d)]
+    off, o = {}, 0
+    for name, n in sizes:
+        off[name] = o
+        o = (o + n + 1023) // 1024 * 1024
+    return off
+
+
+def _tiled8(p, i, BN, K):
+    nb, r, kb = p // BN, p % BN, i // 64
+    return ((nb * (K // 64) + kb) * BN + r) * 64 + i % 64
+
+
+def _unpack_up(buf, base, scbase, W_rows, d, f, BN=256):
+    """(codes as values [d][f], scales [f]) of W1 (m = 0) or W3 (m = 1) from the
+    packed up image; packed row of hidden column h = (h // 64) * 128 + m * 64 + h % 64."""
+    out = []
+    for m in (0, 1):
+        h = np.arange(f)
+        p = (h // 64) * 128 + m * 64 + h % 64
+        I, H = np.meshgrid(np.arange(d), h, indexing="ij")
+        q = E4M3[buf[base + _tiled8(p[H], I, BN, d)]]
+        s = np.frombuffer(buf[scbase:scbase + 4 * 2 * f].tobytes(), np.float32)[p]
+        out.append((q, s))
+    return out
+
+
+def _unpack_down(buf, base, scbase, d, f, BN=256):
+    n = np.arange(d)
+    Hh, N = np.meshgrid(np.arange(f), n, indexing="ij")
+    q = E4M3[buf[base + _tiled8(N, Hh, BN, f)]]
+    s = np.frombuffer(buf[scbase:scbase + 4 * d].tobytes(), np.float32)
+    return q, s
+
+
+def _fp8_quant(W1, W3, W2):
+    (q1, s1), (q3, s3), (q2, s2) = (oracle.quantize_e4m3_columns(w.float().numpy()) for w in (W1, W3, W2))
+    return q1, s1, q3, s3, q2, s2
+
+
+def _merged_shared(W1s, W3s, W2s):
+    """The shared experts as one expert of hidden width n_shared * f_shared (as
+    packed): W1/W3 concatenated along the hidden columns, W2 along its rows."""
+    return (torch.cat(list(W1s), dim=1), torch.cat(list(W3s), dim=1), torch.cat(list(W2s), dim=0))
+
+
+def test_fp8_packing_is_exact(cuda_device):
+    E, d, f, fs = 3, 256, 256, 128
+    cfg = B.config(T=16, d=d, E=E, f=f, k=1, n_shared=1, f_shared=fs, dtype="fp8w")
+    g = torch.Generator(device="cpu").manual_seed(99)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).bfloat16()
+    W1[1, :, 5] = 0                                     # an all-zero channel: scale 0, codes 0
+    W2[2, :, 17] = 0
+    W1[0, 7, 9] = 3.0e-7                                # tiny weights that land on E4M3 subnormals
+    Ws = [(torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, fs, d, generator=g) / fs ** 0.5).bfloat16()]
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    torch.cuda.synchronize()
+    buf = layer.packed.cpu().numpy()
+    off = _packed_offsets(E, d, f, fs)
+    for e in range(E):
+        got = _unpack_up(buf, off["w13"] + e * 2 * f * d, off["sc13"] + 4 * e * 2 * f, None, d, f)
+        for (gq, gs), W in zip(got, (W1[e], W3[e])):
+            q, s = oracle.quantize_e4m3_columns(W.float().numpy())
+            assert np.array_equal(gs, s) and np.array_equal(gq, q)
+        gq, gs = _unpack_down(buf, off["w2"] + e * d * f, off["sc2"] + 4 * e * d, d, f)
+        q, s = oracle.quantize_e4m3_columns(W2[e].float().numpy())
+        assert np.array_equal(gs, s) and np.array_equal(gq, q)
+    got = _unpack_up(buf, off["w13s"], off["sc13s"], None, d, fs)
+    for (gq, gs), W in zip(got, (Ws[0][0], Ws[1][0])):
+        q, s = oracle.quantize_e4m3_columns(W.float().numpy())
+        assert np.array_equal(gs, s) and np.array_equal(gq, q)
+    gq, gs = _unpack_down(buf, off["w2s"], off["sc2s"], d, fs)
+    q, s = oracle.quantize_e4m3_columns(Ws[2][0].float().numpy())
+    assert np.array_equal(gs, s) and np.array_equal(gq, q)
+
+
+def test_fp8_grouped_ffn_tile_edges(cuda_device):
+    E, d, f, fs = len(EDGE_COUNTS), 256, 256, 128
+    T = sum(EDGE_COUNTS)
+    cfg = B.config(T=T, d=d, E=E, f=f, k=1, n_shared=1, f_shared=fs, dtype="fp8w")
+    g = torch.Generator(device="cpu").manual_seed(5)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).bfloat16()
+    Ws = [(torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, fs, d, generator=g) / fs ** 0.5).bfloat16()]
+    x = random_rows(T, d, seed=12, dtype=torch.bfloat16)
+    idx = np.repeat(np.arange(E, dtype=np.int32), EDGE_COUNTS)[np.random.default_rng(8).permutation(T)]
+    o_off, _, _, o_rows = oracle.dispatch_tc(idx.reshape(T, 1), E, -1)
+    x_perm = x[torch.from_numpy(o_rows).long()]
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    off_d, xp_d, x_d = torch.from_numpy(o_off).to(dev), x_perm.to(dev), x.to(dev)
+    Y = _np(layer.grouped_ffn(xp_d, off_d, x_d))
+    H = torch.empty(T, f, dtype=torch.bfloat16, device=dev)
+    Hs = torch.empty(T, fs, dtype=torch.bfloat16, device=dev)
+    Y2 = torch.empty(2 * T, d, dtype=torch.bfloat16, device=dev)
+    B.moe_grouped_ffn_up(cfg, xp_d, off_d, layer.packed, x_d, H, Hs)
+    B.moe_grouped_ffn_down(cfg, H, Hs, off_d, layer.packed, Y2)
+    Y2 = _np(Y2)
+    _check_device_error()
+    xf = x_perm.float().numpy()
+    ref = np.zeros((2 * T, d))
+    for e in range(E):
+        a, b = int(o_off[e]), int(o_off[e + 1])
+        if b > a:
+            ref[a:b] = oracle.expert_rows_fp8(xf[a:b], *_fp8_quant(W1[e], W3[e], W2[e]))
+    ref[T:] = oracle.expert_rows_fp8(x.float().numpy(), *_fp8_quant(Ws[0][0], Ws[1][0], Ws[2][0]))
+    for got in (Y, Y2):
+        for e in range(E):
+            a, b = int(o_off[e]), int(o_off[e + 1])
+            if b > a:
+                assert rel_err(got[a:b], ref[a:b]) <= TOL["bf16"], (e, b - a)
+        assert rel_err(got[T:], ref[T:]) <= TOL["bf16"]
+
+
+def _fp8_forward_ref(wl, inp, toks):
+    """Oracle layer output for the tokens `toks` with the FP8-quantised experts:
+    oracle routing and capacity dispatch, then per chosen expert the fp64 expert of
+    the codes and scales, weighted, plus the merged shared expert.  One expert's
+    quantised weights at a time."""
+    T, E = wl.T, wl.E
+    x = inp["x"].float().cpu().numpy()
+    oi, ow, gap = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                  wl.renorm, nthreads=NTH)
+    cap = oracle.capacity(wl.capacity_factor, T, wl.k, wl.E)
+    _, _, o_slot, _ = oracle.dispatch_tc(oi, E, cap)
+    y = np.zeros((len(toks), wl.d))
+    pos = {int(t): n for n, t in enumerate(toks)}
+    for e in range(E):
+        rows = [(pos[int(t)], j) for t in toks for j in range(wl.k) if oi[t, j] == e and o_slot[t, j] >= 0]
+        if not rows:
+            continue
+        qs = _fp8_quant(inp["W1"][e].cpu(), inp["W3"][e].cpu(), inp["W2"][e].cpu())
+        n_idx = np.array([r[0] for r in rows])
+        out = oracle.expert_rows_fp8(x[toks[n_idx]], *qs)
+        for (n, j), o in zip(rows, out):
+            y[n] += ow[toks[n], j] * o
+    if wl.n_shared:
+        m1, m3, m2 = _merged_shared(inp["W1s"].cpu(), inp["W3s"].cpu(), inp["W2s"].cpu())
+        y += oracle.expert_rows_fp8(x[toks], *_fp8_quant(m1, m3, m2))
+    return y, oi, o_slot, cap
+
+
+FP8_E2E = {
+    "fp8_switch_drops": WORKLOADS["switch_top1_cap1.25"].with_(T=600, d=256, E=8, f=256, capacity_factor=0.8,
+                                                                logit_offsets="normal_var0.5", dtype="fp8w",
+                                                                name="fp8_switch_drops"),
+    "fp8_sigmoid_shared": WORKLOADS["deepseek_v3"].with_(T=150, d=256, E=32, f=128, f_shared=128, dtype="fp8w",
+                                                          name="fp8_sigmoid_shared"),
+    "fp8_top2": WORKLOADS["mixtral_T256"].with_(T=333, d=512, f=384, dtype="fp8w", name="fp8_top2"),
+    "fp8_switch_full": WORKLOADS["switch_top1_cap1.25"].with_(dtype="fp8w", name="fp8_switch_full"),
+}
+
+
+@pytest.mark.parametrize("name", list(FP8_E2E))
+def test_fp8_forward(name, cuda_device):
+    wl = FP8_E2E[name]
+    inp = make_inputs(wl, cuda_device)
+    cfg, layer = _layer(wl, inp)
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    r_idx, _ = layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    _check_device_error()
+    T = wl.T
+    toks = np.arange(T) if T <= 1000 else _sample_tokens(T, 96, T)
+    ref, oi, o_slot, cap = _fp8_forward_ref(wl, inp, toks)
+    gi = _np(r_idx)
+    _, _, g_slot, _ = oracle.dispatch_tc(gi, wl.E, cap)   # the GPU's own choices, dispatched
+    # tokens routed alike on both sides, with the same slots dropped
+    keep = np.array([(gi[t] == oi[t]).all() and ((g_slot[t] >= 0) == (o_slot[t] >= 0)).all() for t in toks])
+    got = _np(y)[toks]
+    err = rel_err(got[keep], ref[keep])
+    print(f"{name}: {int(keep.sum())} tokens compared, max|err|/max|ref| = {err:.3e}")
+    assert keep.mean() > 0.95 and err <= TOL["bf16"]
+
+
+def test_fp8_subnormal_codes_are_exact(cuda_device):
+    # Down projection of one-hot rows: Y[h, n] = q2[h, n] * s2[n] exactly (one product,
+    # rounded once to bf16).  Most of W2 is tiny next to its column maximum, so its
+    # codes are E4M3 subnormals; a conversion that flushed them would give zeros.
+    d, f = 256, 128
+    cfg = B.config(T=f, d=d, E=1, f=f, k=1, dtype="fp8w")
+    rng = np.random.default_rng(9)
+    W2 = (rng.uniform(4.5e-6, 3.4e-5, (f, d)) * rng.choice([-1.0, 1.0], (f, d))).astype(np.float32)
+    W2[0, :] = 1.0
+    W2t = torch.from_numpy(W2).bfloat16()
+    q, s = oracle.quantize_e4m3_columns(W2t.float().numpy())
+    sub = (q != 0) & (np.abs(q) < 2.0 ** -6)
+    assert sub.sum() > f * d // 2
+    dev = cuda_device
+    W1 = torch.zeros(1, d, f, dtype=torch.bfloat16, device=dev)
+    layer = MoELayer(cfg, W1, W1, W2t.reshape(1, f, d).to(dev))
+    H = torch.eye(f, dtype=torch.bfloat16, device=dev)
+    off = torch.tensor([0, f], dtype=torch.int32, device=dev)
+    Y = torch.empty(f, d, dtype=torch.bfloat16, device=dev)
+    B.moe_grouped_ffn_down(cfg, H, None, off, layer.packed, Y)
+    _check_device_error()
+    ref = q * s.astype(np.float64)
+    got = _np(Y)
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8), np.abs(got - ref).max()

@@ -498,3 +498,96 @@ def test_load_stats_entropy_matches_scipy():
         _, P, s = oracle.load_stats(idx, cnt, scores)
         assert s[2] == pytest.approx(entropy(P), rel=1e-12)   # scipy normalises P, natural log
         assert s[0] == pytest.approx(E * cnt.max() / cnt.sum(), rel=1e-14)
+
+
+# ------------------------------------------------------------------ FP8 E4M3 weights
+def _e4m3_table():
+    """Every finite E4M3 value from the format's definition: sign, 4 exponent bits
+    (bias 7), 3 mantissa bits; exponent 0 is subnormal; S.1111.111 is NaN."""
+    vals = []
+    for code in range(256):
+        sgn = -1.0 if code & 0x80 else 1.0
+        e, m = (code >> 3) & 0xF, code & 7
+        if e == 15 and m == 7:
+            continue
+        vals.append(sgn * (m / 8.0) * 2.0 ** -6 if e == 0 else sgn * (1 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def test_e4m3_round_fixes_every_code_and_the_extremes():
+    t = _e4m3_table()
+    assert np.array_equal(oracle.e4m3_round(t), t)
+    assert t.max() == 448.0 and np.min(t[t > 0]) == 2.0 ** -9
+    assert list(oracle.e4m3_round([500.0, -1e6, 2.0 ** -11, 0.0])) == [448.0, -448.0, 0.0, 0.0]
+
+
+def test_e4m3_round_is_nearest_even():
+    t = np.unique(np.abs(_e4m3_table()))
+    mids = (t[:-1] + t[1:]) / 2                                     # exact ties
+    r = oracle.e4m3_round(mids)
+    lo, hi = t[:-1], t[1:]
+    # the even neighbour: the one whose code's mantissa bit 0 is clear
+    def mant_even(v):
+        v = np.asarray(v)
+        out = np.empty(v.shape, bool)
+        for i, x in enumerate(v):
+            if x < 2.0 ** -6:
+                out[i] = int(round(x / 2.0 ** -9)) % 2 == 0
+            else:
+                e = np.floor(np.log2(x))
+                out[i] = int(round((x / 2.0 ** e - 1) * 8)) % 2 == 0
+        return out
+    want = np.where(mant_even(lo), lo, hi)
+    assert np.array_equal(r, want)
+    # away from ties: the nearest neighbour
+    rng = np.random.default_rng(3)
+    x = rng.uniform(0, 448, 20000) * rng.choice([1, 2.0 ** -8, 2.0 ** -12], 20000)
+    r = oracle.e4m3_round(x)
+    idx = np.clip(np.searchsorted(t, x), 1, len(t) - 1)
+    near = np.where(np.abs(t[idx] - x) < np.abs(t[idx - 1] - x), t[idx], t[idx - 1])
+    tie = np.abs(np.abs(t[idx] - x) - np.abs(t[idx - 1] - x)) == 0
+    assert np.array_equal(r[~tie], near[~tie])
+
+
+def test_e4m3_round_matches_torch_float8():
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.normal(0, 50, 50000), rng.normal(0, 1e-3, 20000), _e4m3_table(),
+                        (_e4m3_table()[:-1] + _e4m3_table()[1:]) / 2])
+    x = x[np.abs(x) <= 448].astype(np.float32)
+    import torch
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(oracle.e4m3_round(x), ref)
+
+
+def test_quantize_e4m3_columns():
+    rng = np.random.default_rng(6)
+    W = rng.normal(0, 0.05, (64, 9)).astype(np.float32)
+    W[:, 3] = 0.0                                                  # an all-zero channel
+    q, s = oracle.quantize_e4m3_columns(W)
+    assert s.dtype == np.float32 and s[3] == 0 and not q[:, 3].any()
+    for n in (0, 1, 2, 4, 8):
+        i = np.argmax(np.abs(W[:, n]))
+        assert abs(q[i, n]) == 448.0                               # the channel's amax maps to the top code
+        assert s[n] == np.float32(np.abs(W[:, n]).max() / np.float32(448))
+    # dequantised weights stay within half an E4M3 step (relative 2^-4) of the input
+    deq = q * s.astype(np.float64)
+    big = np.abs(W) > s.astype(np.float64) * 2.0 ** -6 * 448 / 448
+    assert np.all(np.abs(deq - W)[big] <= np.abs(W)[big] * 2.0 ** -4 + 1e-12)
+
+
+def test_expert_rows_fp8_equals_expert_of_dequantised_weights():
+    rng = np.random.default_rng(7)
+    d, f, n = 32, 48, 5
+    W1, W3 = rng.normal(0, 0.2, (d, f)), rng.normal(0, 0.2, (d, f))
+    W2 = rng.normal(0, 0.2, (f, d))
+    x = rng.normal(0, 1, (n, d))
+    (q1, s1), (q3, s3), (q2, s2) = (oracle.quantize_e4m3_columns(w) for w in (W1, W3, W2))
+    got = oracle.expert_rows_fp8(x, q1, s1, q3, s3, q2, s2)
+    D1, D3, D2 = q1 * s1.astype(float), q3 * s3.astype(float), q2 * s2.astype(float)
+    a = x @ D1
+    ref = ((a / (1 + np.exp(-a))) * (x @ D3)) @ D2
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # and it tracks the unquantised expert to the E4M3 precision
+    a0 = x @ W1
+    full = ((a0 / (1 + np.exp(-a0))) * (x @ W3)) @ W2
+    assert np.abs(got - full).max() <= 0.2 * np.abs(full).max()
