@@ -210,6 +210,8 @@ def run_gpu(args):
         wl = wl.with_(T=args.T)
     if args.fp8_weights:
         wl = wl.with_(dtype="fp8w")
+    if args.affinity_drop:
+        wl = wl.with_(drop_policy="affinity")
     if ws_n > 1:   # each replica gets its own batch of tokens
         wl = wl.with_(index=wl.index + 1000 * rank) if rank else wl
     inp = make_inputs(wl, dev)
@@ -241,7 +243,7 @@ def run_gpu(args):
         B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream)
         if ev is not None:
             ev[1].record(stream)
-        B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream)
+        B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream, gw)
         if ev is not None:
             ev[2].record(stream)
         B.moe_grouped_ffn(cfg, x_perm, off, layer.packed, x, Y, ws_ffn, stream)
@@ -321,7 +323,7 @@ def run_gpu(args):
 
     route_plain_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream))
     route_probs_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream, psum))
-    B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream)
+    B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream, gw)
     stats_ms = timed(lambda: B.moe_load_stats(cfg, idx, cnt, psum, frac, pmean, summary, stream))
     B.moe_check_device_error(stream)
     load_stats = {"route_ms": round(route_plain_ms, 5), "route_with_prob_sum_ms": round(route_probs_ms, 5),
@@ -428,6 +430,7 @@ def run_gpu(args):
                    "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
                    "n_shared": wl.n_shared, "f_shared": wl.f_shared,
                    "expert_weights": "e4m3 + fp32 scale per output channel" if wl.dtype == "fp8w" else wl.dtype,
+                   "drop_policy": wl.drop_policy,
                    "assignments_computed": A, "experts_touched": touched,
                    "l2": "inputs larger than L2: the expert weights read per step exceed 126 MB"
                          if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2",
@@ -562,6 +565,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256, help="largest oracle sample per reference step")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds the reference arm aims to take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--affinity-drop", action="store_true",
+                    help="capacity drop by descending gate weight (DeepSeek-V2) instead of token order")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="store the expert weights as FP8 E4M3 with per-channel scales (MOE_BF16_FP8W)")
     args = ap.parse_args()

@@ -65,6 +65,7 @@ typedef enum {
 typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
 typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_mode;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_BF16_FP8W = 2 } moe_dtype;
+typedef enum { MOE_DROP_TOKEN_ORDER = 0, MOE_DROP_AFFINITY = 1 } moe_drop_policy;
 typedef enum {
     MOE_STAGE_ROUTE = 0,
     MOE_STAGE_DISPATCH = 1,
@@ -88,6 +89,10 @@ typedef enum {
  *   n_shared, f_shared: always-on shared experts (§3.4), each of hidden width
  *     f_shared; their outputs are added unweighted.
  *   dtype: MOE_BF16, MOE_F32 or MOE_BF16_FP8W.
+ *   drop_policy: token choice with a capacity limit; which assignments an
+ *     expert over capacity keeps: MOE_DROP_TOKEN_ORDER the first `cap` in token
+ *     order (§3.2), MOE_DROP_AFFINITY the `cap` with the largest gate weights
+ *     (DeepSeek-V2, "技术日报" §5.2: tokens dropped by descending affinity).
  * Build limits: MOE_BF16 needs d % 128 == 0, f % 64 == 0, f_shared % 64 == 0;
  * MOE_F32 needs d % 64 == 0, f % 64 == 0, f_shared % 64 == 0;
  * MOE_BF16_FP8W needs d % 256 == 0, f % 128 == 0, n_shared * f_shared % 128 == 0.
@@ -101,6 +106,7 @@ typedef struct moe_config {
     int32_t ec_capacity;
     int32_t n_shared, f_shared;
     int32_t dtype;
+    int32_t drop_policy;   /* moe_drop_policy; see moe_dispatch */
 } moe_config;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -176,13 +182,18 @@ moe_status moe_route(const moe_config *cfg, const void *x, const void *W_r, cons
  *     off[E+1]     exclusive prefix sum of the kept counts (off[E] = rows used),
  *     slot_of[T][k] row of the assignment in x_perm, -1 when dropped,
  *     x_perm[rows_routed][d] rows [0, off[E]) = x[token of the row] (rest untouched).
+ * MOE_DROP_AFFINITY (capacity limited): an expert with more than `cap` assignments
+ *   keeps the `cap` with the largest topk_w[T][k] (fp32 gate weights as moe_route
+ *   wrote them), ties to the lower token index; its rows are still in token order.
+ *   The experts of one token must be distinct.  topk_w is read only in that case
+ *   (NULL otherwise).
  * Expert choice: topk_idx is ec_tok[E][cap]; writes off[e] = e*cap, cnt_raw[e] = cap,
  *   slot_of[T][E] (row e*cap + r when expert e took the token as its r-th pick, else
  *   -1) and x_perm[E*cap][d].
  */
-moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *off,
-                        int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
-                        void *stream);
+moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const float *topk_w, const void *x,
+                        int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *ws,
+                        size_t ws_bytes, void *stream);
 
 /*
  * moe_dispatch for callers that cannot allocate device memory.  (The paper has

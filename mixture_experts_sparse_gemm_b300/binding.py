@@ -19,6 +19,7 @@ MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_GATE_SOFTMAX, MOE_GATE_SIGMOID = 0, 1
 MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
 MOE_F32, MOE_BF16, MOE_BF16_FP8W = 0, 1, 2
+MOE_DROP_TOKEN_ORDER, MOE_DROP_AFFINITY = 0, 1
 MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, MOE_STAGE_FORWARD = range(5)
 
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
@@ -39,7 +40,7 @@ class moe_config(ctypes.Structure):
                 ("k", ctypes.c_int32), ("gate", ctypes.c_int32), ("mode", ctypes.c_int32),
                 ("renormalize", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
                 ("ec_capacity", ctypes.c_int32), ("n_shared", ctypes.c_int32), ("f_shared", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("drop_policy", ctypes.c_int32)]
 
 
 _lib = None
@@ -64,7 +65,7 @@ def lib():
             "moe_packed_weights_size": [cfgp, szp],
             "moe_pack_weights": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_route": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
-            "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+            "moe_dispatch": [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_grouped_ffn": [cfgp, vp, vp, vp, vp, vp, vp, sz, vp],
             "moe_grouped_ffn_up": [cfgp, vp, vp, vp, vp, vp, vp, vp],
             "moe_grouped_ffn_down": [cfgp, vp, vp, vp, vp, vp, vp],
@@ -117,11 +118,11 @@ def _check(status, where):
 
 
 def config(T, d, E, f, k=1, gate="softmax", mode="tc", renormalize=True, capacity_factor=0.0, ec_capacity=0,
-           n_shared=0, f_shared=0, dtype="bf16") -> moe_config:
+           n_shared=0, f_shared=0, dtype="bf16", drop_policy="token") -> moe_config:
     return moe_config(T, d, E, f, k, MOE_GATE_SIGMOID if gate == "sigmoid" else MOE_GATE_SOFTMAX,
                       MOE_EXPERT_CHOICE if mode == "ec" else MOE_TOKEN_CHOICE, int(bool(renormalize)),
                       float(capacity_factor), int(ec_capacity), int(n_shared), int(f_shared),
-                      _DTYPES[dtype])
+                      _DTYPES[dtype], MOE_DROP_AFFINITY if drop_policy == "affinity" else MOE_DROP_TOKEN_ORDER)
 
 
 # run dtype names: "fp8w" = bf16 activations with FP8 E4M3 expert weights
@@ -131,7 +132,7 @@ _DTYPES = {"f32": MOE_F32, "fp32": MOE_F32, "float32": MOE_F32, "bf16": MOE_BF16
 
 def config_from_workload(w, T=None) -> moe_config:
     return config(T if T is not None else w.T, w.d, w.E, w.f, w.k if w.mode == "tc" else 0, w.gate, w.mode,
-                  w.renorm, w.capacity_factor, w.ec_capacity, w.n_shared, w.f_shared, w.dtype)
+                  w.renorm, w.capacity_factor, w.ec_capacity, w.n_shared, w.f_shared, w.dtype, w.drop_policy)
 
 
 # ------------------------------------------------------------------ host queries (no CUDA call)
@@ -179,9 +180,10 @@ def moe_load_stats(cfg, topk_idx, cnt_raw, prob_sum, token_fraction, prob_mean, 
                                 _p(prob_mean), _p(summary), _stream(stream)), "moe_load_stats")
 
 
-def moe_dispatch(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, ws, stream=None):
-    _check(lib().moe_dispatch(ctypes.byref(cfg), _p(topk_idx), _p(x), _p(off), _p(cnt_raw), _p(slot_of), _p(x_perm),
-                              _p(ws), _nbytes(ws), _stream(stream)), "moe_dispatch")
+def moe_dispatch(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, ws, stream=None, topk_w=None):
+    """topk_w: the gate weights, read for the affinity-ordered capacity drop only."""
+    _check(lib().moe_dispatch(ctypes.byref(cfg), _p(topk_idx), _p(topk_w), _p(x), _p(off), _p(cnt_raw), _p(slot_of),
+                              _p(x_perm), _p(ws), _nbytes(ws), _stream(stream)), "moe_dispatch")
 
 
 def moe_dispatch_noalloc(cfg, topk_idx, x, off, cnt_raw, slot_of, x_perm, stream=None):

@@ -238,6 +238,58 @@ __global__ void ec_slots_kernel(const int32_t *ec_tok, int T, int E, int cap, in
     }
 }
 
+// ----------------------------------------------------------------------------- affinity-ordered drop
+// DeepSeek-V2 drop ("技术日报 2026-04-14" §5.2: over-capacity tokens dropped by
+// descending affinity): an expert over capacity keeps the `cap` assignments with
+// the largest gate weights, ties to the lower token.  The weights go into a dense
+// S[E][T] (0 where the token did not choose the expert; weights are positive), the
+// column select of the Expert Choice path takes min(cnt_raw[e], cap) per column in
+// ascending token order, and the rows are placed from there.
+
+// S[e][t] = topk_w[t][j] for every assignment (t, j) -> e; cnt_raw[e] += 1
+__global__ void affinity_scatter_kernel(const int32_t *__restrict__ topk_idx, const float *__restrict__ topk_w,
+                                        int64_t n, int k, int T, int E, float *S, int32_t *cnt_raw, unsigned *err) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int e = topk_idx[i];
+        if ((unsigned)e >= (unsigned)E) {
+            atomicOr(err, kErrBadIndex);
+            continue;
+        }
+        S[(size_t)e * T + i / k] = topk_w[i];
+        atomicAdd(&cnt_raw[e], 1);
+    }
+}
+
+// One block per expert: off[e] = sum over e' < e of min(cnt_raw[e'], cap); the kept
+// tokens kept[e][r] (ascending) get rows off[e] + r: row_token, and slot_of of the
+// slot j with topk_idx[t][j] == e.
+__global__ void affinity_rows_kernel(const int32_t *__restrict__ kept, const int32_t *__restrict__ cnt_raw, int cap,
+                                     const int32_t *__restrict__ topk_idx, int k, int E, int32_t *off, int32_t *slot_of,
+                                     int32_t *row_token) {
+    __shared__ int s_off;
+    const int e = blockIdx.x;
+    if (threadIdx.x < 32) {
+        int part = 0;
+        for (int q = threadIdx.x; q < e; q += 32) part += min(cnt_raw[q], cap);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (threadIdx.x == 0) {
+            s_off = part;
+            off[e] = part;
+            if (e == E - 1) off[E] = part + min(cnt_raw[e], cap);
+        }
+    }
+    __syncthreads();
+    const int take = min(cnt_raw[e], cap), base = s_off;
+    for (int r = threadIdx.x; r < take; r += blockDim.x) {
+        const int t = kept[(size_t)e * cap + r];
+        row_token[base + r] = t;
+        for (int j = 0; j < k; ++j)
+            if (topk_idx[(size_t)t * k + j] == e) slot_of[(size_t)t * k + j] = base + r;
+    }
+}
+
 int gather_grid(int64_t rows) {
     const int64_t warps_needed = rows;
     int64_t blocks = (warps_needed + 7) / 8;
@@ -273,6 +325,28 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
         dispatch_rank_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.k, c.E, nchunks, chunk_cnt, off,
                                                                      cap, slot_of, row_token, err);
     }
+    const int elt = c.dtype == MOE_F32 ? 4 : 2;
+    const int vecs = c.d * elt / 16;
+    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,
+                                                      static_cast<uint4 *>(x_perm));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
+                                     const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
+                                     float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
+                                     cudaStream_t s) {
+    const int64_t n = (int64_t)c.T * c.k;
+    cudaError_t ce = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)c.E * c.T, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(cnt_raw, 0, sizeof(int32_t) * c.E, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(slot_of, 0xff, sizeof(int32_t) * (size_t)n, s);
+    if (ce != cudaSuccess) return ce;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > num_sms() * 4) blocks = num_sms() * 4;
+    affinity_scatter_kernel<<<blocks, 256, 0, s>>>(topk_idx, topk_w, n, c.k, c.T, c.E, S, cnt_raw, err);
+    ce = launch_column_select(c, S, cap, cnt_raw, kept, kept_w, s);
+    if (ce != cudaSuccess) return ce;
+    affinity_rows_kernel<<<c.E, 256, 0, s>>>(kept, cnt_raw, cap, topk_idx, c.k, c.E, off, slot_of, row_token);
     const int elt = c.dtype == MOE_F32 ? 4 : 2;
     const int vecs = c.d * elt / 16;
     gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,

@@ -70,6 +70,8 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const int32_t 
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
     if (!topk_idx || !x || !off || !cnt_raw || !slot_of || !x_perm) return MOE_ERR_INVALID_ARG;
+    if (c.mode == MOE_TOKEN_CHOICE && c.drop_policy == MOE_DROP_AFFINITY && c.capacity_factor > 0.f)
+        return MOE_ERR_UNSUPPORTED;   // the affinity order needs the gate weights and a workspace
     const uintptr_t a16 = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x_perm);
     const uintptr_t a4 = reinterpret_cast<uintptr_t>(topk_idx) | reinterpret_cast<uintptr_t>(off) |
                          reinterpret_cast<uintptr_t>(cnt_raw) | reinterpret_cast<uintptr_t>(slot_of);

@@ -82,8 +82,13 @@ RouteWs route_ws(const moe_config &c) {
     return w;
 }
 
+// the affinity-ordered capacity drop applies (token choice, a capacity limit)
+bool affinity_drop(const moe_config &c) {
+    return c.mode == MOE_TOKEN_CHOICE && c.drop_policy == MOE_DROP_AFFINITY && sizes_of(c).cap >= 0;
+}
+
 struct DispatchWs {
-    size_t chunk, row_token, total;
+    size_t chunk, row_token, aff_S, aff_kept, aff_w, total;
 };
 DispatchWs dispatch_ws(const moe_config &c) {
     Carver k;
@@ -93,6 +98,12 @@ DispatchWs dispatch_ws(const moe_config &c) {
         const size_t ints = dispatch_tc_scratch_ints(n, c.E);
         w.chunk = k.take(sizeof(int32_t) * (ints - (size_t)n));
         w.row_token = k.take(sizeof(int32_t) * (size_t)n);
+        if (affinity_drop(c)) {   // dense weights S[E][T], kept tokens and weights [E][cap]
+            const size_t cap = (size_t)sizes_of(c).cap;
+            w.aff_S = k.take(sizeof(float) * (size_t)c.E * c.T);
+            w.aff_kept = k.take(sizeof(int32_t) * (size_t)c.E * cap);
+            w.aff_w = k.take(sizeof(float) * (size_t)c.E * cap);
+        }
     }
     w.total = k.off;
     return w;
@@ -160,12 +171,17 @@ moe_status do_route(const moe_config &c, const void *x, const void *W_r, const f
     return MOE_OK;
 }
 
-moe_status do_dispatch(const moe_config &c, const int32_t *idx, const void *x, int32_t *off, int32_t *cnt_raw,
-                       int32_t *slot_of, void *x_perm, char *ws, unsigned *err, cudaStream_t s) {
+moe_status do_dispatch(const moe_config &c, const int32_t *idx, const float *topk_w, const void *x, int32_t *off,
+                       int32_t *cnt_raw, int32_t *slot_of, void *x_perm, char *ws, unsigned *err, cudaStream_t s) {
     if (c.mode == MOE_EXPERT_CHOICE)
         return from_cuda(launch_dispatch_ec(c, idx, x, off, cnt_raw, slot_of, x_perm, err, s));
     const DispatchWs L = dispatch_ws(c);
     const Sizes z = sizes_of(c);
+    if (affinity_drop(c))
+        return from_cuda(launch_dispatch_affinity(
+            c, z.cap, idx, topk_w, x, off, cnt_raw, slot_of, x_perm, reinterpret_cast<float *>(ws + L.aff_S),
+            reinterpret_cast<int32_t *>(ws + L.aff_kept), reinterpret_cast<float *>(ws + L.aff_w),
+            reinterpret_cast<int32_t *>(ws + L.row_token), err, s));
     return from_cuda(launch_dispatch_tc(c, z.cap, idx, x, off, cnt_raw, slot_of, x_perm,
                                         reinterpret_cast<int32_t *>(ws + L.chunk),
                                         reinterpret_cast<int32_t *>(ws + L.row_token), err, s));
@@ -194,6 +210,7 @@ int route_launches(const moe_config &c) {
     return base + (c.mode == MOE_EXPERT_CHOICE ? 1 : 0);
 }
 int dispatch_launches(const moe_config &c) {
+    if (affinity_drop(c)) return 4;   // scatter, column select, rows, gather
     return c.mode == MOE_EXPERT_CHOICE ? 2 : dispatch_tc_launches((int64_t)c.T * c.k);
 }
 
@@ -299,6 +316,7 @@ moe_status moe_validate_config(const moe_config *cfg) {
     if (c.gate != MOE_GATE_SOFTMAX && c.gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c.mode != MOE_TOKEN_CHOICE && c.mode != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
     if (c.dtype != MOE_F32 && c.dtype != MOE_BF16 && c.dtype != MOE_BF16_FP8W) return MOE_ERR_INVALID_ARG;
+    if (c.drop_policy != MOE_DROP_TOKEN_ORDER && c.drop_policy != MOE_DROP_AFFINITY) return MOE_ERR_INVALID_ARG;
     if (c.n_shared < 0 || (c.n_shared > 0 && c.f_shared <= 0)) return MOE_ERR_INVALID_ARG;
     if (std::isnan(c.capacity_factor)) return MOE_ERR_INVALID_ARG;
     if (c.E > kMaxE) return MOE_ERR_UNSUPPORTED;
@@ -415,14 +433,17 @@ moe_status moe_route(const moe_config *cfg, const void *x, const void *W_r, cons
     return do_route(c, x, W_r, logit_offset, sel_bias, topk_idx, topk_w, static_cast<char *>(ws), err, s, prob_sum);
 }
 
-moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *off,
-                        int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes, void *stream) {
+moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const float *topk_w, const void *x,
+                        int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm, void *ws, size_t ws_bytes,
+                        void *stream) {
     moe_status st = moe_validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
     MOE_REQUIRE(topk_idx && x && off && cnt_raw && slot_of && x_perm, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(topk_w || !affinity_drop(c), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(aligned16(x) && aligned16(x_perm), MOE_ERR_MISALIGNED);
-    MOE_REQUIRE(aligned4(topk_idx) && aligned4(off) && aligned4(cnt_raw) && aligned4(slot_of), MOE_ERR_MISALIGNED);
+    MOE_REQUIRE(aligned4(topk_idx) && aligned4(off) && aligned4(cnt_raw) && aligned4(slot_of) && aligned4(topk_w),
+                MOE_ERR_MISALIGNED);
     st = check_ws(ws, ws_bytes, dispatch_ws(c).total);
     if (st != MOE_OK) return st;
     unsigned *err = nullptr;
@@ -435,7 +456,7 @@ moe_status moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const vo
             return MOE_ERR_CUDA;
         return MOE_OK;
     }
-    return do_dispatch(c, topk_idx, x, off, cnt_raw, slot_of, x_perm, static_cast<char *>(ws), err, s);
+    return do_dispatch(c, topk_idx, topk_w, x, off, cnt_raw, slot_of, x_perm, static_cast<char *>(ws), err, s);
 }
 
 moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int32_t *off, const void *packed,
@@ -570,7 +591,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, co
     void *Y = w + L.Y;
     st = do_route(c, x, W_r, logit_offset, sel_bias, idx, gw, w + L.route, err, s);
     if (st != MOE_OK) return st;
-    st = do_dispatch(c, idx, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s);
+    st = do_dispatch(c, idx, gw, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s);
     if (st != MOE_OK) return st;
     if (gated_down(c)) {
         // one expert per token and no shared experts: the down GEMM writes each row

@@ -92,6 +92,10 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
                               float *topk_w, float *scores_t, float *psum_rows, unsigned *err, cudaStream_t s);
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,
                              cudaStream_t s);
+// per column e of scores_t[E][T]: the min(col_cnt[e], cap) largest (ties to the lower
+// token), ascending token ids -> tok[e][0..), their scores -> w[e][0..)
+cudaError_t launch_column_select(const moe_config &c, const float *scores_t, int cap, const int32_t *col_cnt,
+                                 int32_t *tok, float *w, cudaStream_t s);
 // scoring + selection from split-K partial logits partial[splits][T][npad] (fp32)
 cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
                                 int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
@@ -100,6 +104,13 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);
 size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
+// affinity-ordered capacity drop (token choice): scratch S[E][T] fp32, kept[E][cap]
+// tokens and weights; launches a scatter, the column select, the row placement
+// and the gather (slot_of and cnt_raw zeroed / set here)
+cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
+                                     const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
+                                     float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
+                                     cudaStream_t s);
 int dispatch_tc_launches(int64_t assignments);
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
                                int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s);

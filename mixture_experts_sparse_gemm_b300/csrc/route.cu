@@ -313,14 +313,19 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
     return r;
 }
 
+// col_cnt (nullable): column e takes min(col_cnt[e], cap) tokens instead of cap
+// (the affinity-ordered capacity drop); outputs stay [E][cap].
 __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scores_t, int T, int cap,
-                                                                 int32_t *ec_tok, float *ec_w) {
+                                                                 const int32_t *col_cnt, int32_t *ec_tok,
+                                                                 float *ec_w) {
     extern __shared__ unsigned s_col[];   // the expert's column, when it fits
     __shared__ unsigned hist[kEcBins];
     __shared__ int warp_tot[65];
     __shared__ unsigned s_digit;
     __shared__ int s_remaining;
     const int e = blockIdx.x;
+    const int take = col_cnt ? min(col_cnt[e], cap) : cap;   // tokens this column keeps
+    if (take <= 0) return;                                      // the whole block leaves together
     const unsigned *g = reinterpret_cast<const unsigned *>(scores_t + (size_t)e * T);
     const bool in_smem = T <= kEcSmemMaxT;
     if (in_smem) {
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scor
     constexpr int kShift[3] = {20, 10, 0};
     constexpr int kBits[3] = {12, 10, 10};
     unsigned prefix = 0, mask = 0;
-    int remaining = cap;
+    int remaining = take;
 #pragma unroll 1
     for (int pass = 0; pass < 3; ++pass) {
         const int shift = kShift[pass];
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(kEcThreads) ec_select_kernel(const float *scor
     for (int t = t0; t < t1; ++t) {
         const unsigned u = col[t];
         const bool sel = (u > K) || (u == K && te++ < take_eq);
-        if (sel && p < cap) {
+        if (sel && p < take) {
             ec_tok[(size_t)e * cap + p] = t;
             ec_w[(size_t)e * cap + p] = __uint_as_float(u);
             ++p;
@@ -464,7 +469,16 @@ cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t
     const size_t smem = c.T <= kEcSmemMaxT ? sizeof(unsigned) * (size_t)c.T : 0;
     cudaError_t err = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    ec_select_kernel<<<c.E, kEcThreads, smem, s>>>(scores_t, c.T, c.ec_capacity, ec_tok, ec_w);
+    ec_select_kernel<<<c.E, kEcThreads, smem, s>>>(scores_t, c.T, c.ec_capacity, nullptr, ec_tok, ec_w);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_column_select(const moe_config &c, const float *scores_t, int cap, const int32_t *col_cnt,
+                                 int32_t *tok, float *w, cudaStream_t s) {
+    const size_t smem = c.T <= kEcSmemMaxT ? sizeof(unsigned) * (size_t)c.T : 0;
+    cudaError_t err = cudaFuncSetAttribute(ec_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    ec_select_kernel<<<c.E, kEcThreads, smem, s>>>(scores_t, c.T, cap, col_cnt, tok, w);
     return cudaGetLastError();
 }
 

@@ -61,13 +61,13 @@ class MoELayer:
         B.moe_load_stats(self.cfg, topk_idx, cnt_raw, prob_sum, frac, pmean, summary, stream)
         return frac, pmean, summary
 
-    def dispatch(self, idx, x, stream=None):
+    def dispatch(self, idx, x, stream=None, topk_w=None):
         c = self.cfg
         off = torch.empty(c.E + 1, dtype=torch.int32, device=self.device)
         cnt_raw = torch.empty(c.E, dtype=torch.int32, device=self.device)
         slot_of = torch.empty(self.n_slots(), dtype=torch.int32, device=self.device)
         x_perm = torch.empty(max(self.rows_routed, 1), c.d, dtype=self.dtype, device=self.device)
-        B.moe_dispatch(c, idx, x, off, cnt_raw, slot_of, x_perm, self.workspace(B.MOE_STAGE_DISPATCH), stream)
+        B.moe_dispatch(c, idx, x, off, cnt_raw, slot_of, x_perm, self.workspace(B.MOE_STAGE_DISPATCH), stream, topk_w)
         return off, cnt_raw, slot_of, x_perm
 
     def grouped_ffn(self, x_perm, off, x=None, stream=None):

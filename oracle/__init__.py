@@ -163,6 +163,44 @@ def dispatch_tc(topk_idx, E, cap=-1):
     return off, cnt, slot, row_token[: off[E]].copy()
 
 
+def dispatch_tc_affinity(topk_idx, topk_w, E, cap=-1):
+    """Capacity-limited dispatch with the DeepSeek-V2 drop ("技术日报 2026-04-14" §5.2:
+    over-capacity tokens dropped by descending affinity) -> (off, cnt_raw, slot_of,
+    row_token) as dispatch_tc.  Expert e ranks its assignments (t, j) by weight
+    topk_w[t, j], largest first, ties to the lower token, and keeps the first cap;
+    the kept rows of a segment stay in ascending token order, segments in expert
+    order.  Without a limit (cap < 0) this is dispatch_tc."""
+    idx = np.asarray(topk_idx)
+    w = np.asarray(topk_w, np.float32)
+    if cap < 0:
+        return dispatch_tc(idx, E, cap)
+    T, k = idx.shape
+    cnt = np.zeros(E, np.int32)
+    for t in range(T):
+        for j in range(k):
+            cnt[idx[t, j]] += 1
+    kept = np.zeros((T, k), bool)
+    for e in range(E):
+        cand = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        cand.sort(key=lambda tj: (-float(w[tj]), tj[0]))
+        for t, j in cand[:cap]:
+            kept[t, j] = True
+    off = np.zeros(E + 1, np.int32)
+    for e in range(E):
+        off[e + 1] = off[e] + min(int(cnt[e]), cap)
+    slot = np.full((T, k), -1, np.int32)
+    row_token = np.full(int(off[E]), -1, np.int32)
+    nxt = off[:E].copy()
+    for t in range(T):                               # token order inside each segment
+        for j in range(k):
+            if kept[t, j]:
+                e = idx[t, j]
+                slot[t, j] = nxt[e]
+                row_token[nxt[e]] = t
+                nxt[e] += 1
+    return off, cnt, slot, row_token
+
+
 def swiglu_expert(x_row, W1, W3, W2, scale=1.0):
     """(SiLU(x W1) * (x W3)) W2 for one token, fp64."""
     x_row, W1, W3, W2 = _f32(x_row), _f32(W1), _f32(W3), _f32(W2)

@@ -99,8 +99,17 @@ def test_argument_checks_run_before_any_cuda_call():
     assert L.moe_route(c, None, A, None, None, A, A, None, A, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_route(c, A + 8, A, None, None, A, A, None, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_route(c, A, A, None, None, A + 2, A, None, A, 1 << 20, None) == B.MOE_ERR_MISALIGNED
-    assert L.moe_dispatch(c, A, A, A, A, A, A, A, ws_need - 1, None) == B.MOE_ERR_WORKSPACE
-    assert L.moe_dispatch(c, A, A, A, A, A, A, A + 64, ws_need, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_dispatch(c, A, None, A, A, A, A, A, A, ws_need - 1, None) == B.MOE_ERR_WORKSPACE
+    assert L.moe_dispatch(c, A, None, A, A, A, A, A, A + 64, ws_need, None) == B.MOE_ERR_MISALIGNED
+    aff = B.config(T=64, d=256, E=8, f=128, k=2, capacity_factor=1.0, drop_policy="affinity")
+    ws_aff = B.moe_workspace_size(aff, B.MOE_STAGE_DISPATCH)
+    assert ws_aff > ws_need                                   # dense weights and kept lists
+    assert L.moe_dispatch(ctypes.byref(aff), A, None, A, A, A, A, A, A, ws_aff, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_dispatch(ctypes.byref(aff), A, A + 2, A, A, A, A, A, A, ws_aff, None) == B.MOE_ERR_MISALIGNED
+    assert L.moe_dispatch_noalloc(ctypes.byref(aff), A, A, A, A, A, A, None) == B.MOE_ERR_UNSUPPORTED
+    bad = B.config(T=64, d=256, E=8, f=128, k=2)
+    bad.drop_policy = 7
+    assert B.lib().moe_validate_config(ctypes.byref(bad)) == B.MOE_ERR_INVALID_ARG
     assert L.moe_combine(c, A, A, None, A, None, 0, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_forward(c, A, A, None, None, A + 128, A, A, 1 << 40, None) == B.MOE_ERR_MISALIGNED
     assert L.moe_forward(None, A, A, None, None, A, A, A, 1 << 40, None) == B.MOE_ERR_INVALID_ARG

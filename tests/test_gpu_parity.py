@@ -186,6 +186,68 @@ def test_dispatch_token_choice(T, E, k, C, skew, d, dt, cuda_device):
     assert torch.equal(x_perm[:A], x[torch.from_numpy(o_rows).long().to(cuda_device)])
 
 
+AFFINITY_CASES = [
+    # T, E, k, capacity factor, skew, weight levels (0: continuous), d
+    (8192, 64, 1, 1.25, 1.0, 0, 1024),
+    (1000, 8, 2, 0.8, 1.5, 7, 128),         # seven weight values: many ties at the boundary
+    (4096, 256, 8, 1.0, 0.5, 0, 256),
+    (300, 8, 2, 0.01, 0.0, 0, 128),         # capacity 0: every assignment dropped
+    (500, 16, 2, 20.0, 1.0, 0, 128),        # no expert reaches the limit: token order
+]
+
+
+@pytest.mark.parametrize("T,E,k,C,skew,levels,d", AFFINITY_CASES)
+def test_dispatch_affinity(T, E, k, C, skew, levels, d, cuda_device):
+    cfg = B.config(T=T, d=d, E=E, f=64, k=k, capacity_factor=C, drop_policy="affinity")
+    idx = random_assignment(T, E, k, seed=T + E + 3 * k, skew=skew, device=cuda_device)
+    w = random_weights((T, k), seed=T + 5)
+    if levels:
+        w = torch.floor(w * levels) / levels + 0.05
+    x = random_rows(T, d, seed=T, device=cuda_device)
+    ws = torch.empty(B.moe_workspace_size(cfg, B.MOE_STAGE_DISPATCH), dtype=torch.uint8, device=cuda_device)
+    off = torch.empty(E + 1, dtype=torch.int32, device=cuda_device)
+    cnt = torch.empty(E, dtype=torch.int32, device=cuda_device)
+    slot = torch.empty(T, k, dtype=torch.int32, device=cuda_device)
+    x_perm = torch.empty(T * k, d, dtype=torch.bfloat16, device=cuda_device)
+    B.moe_dispatch(cfg, idx, x, off, cnt, slot, x_perm, ws, topk_w=w.to(cuda_device))
+    _check_device_error()
+    cap = oracle.capacity(C, T, k, E)
+    o_off, o_cnt, o_slot, o_rows = oracle.dispatch_tc_affinity(_np(idx), w.numpy(), E, cap)
+    np.testing.assert_array_equal(_np(off), o_off)
+    np.testing.assert_array_equal(_np(cnt), o_cnt)
+    np.testing.assert_array_equal(_np(slot), o_slot)
+    A = int(o_off[-1])
+    assert torch.equal(x_perm[:A], x[torch.from_numpy(o_rows).long().to(cuda_device)])
+    dropped = int((o_slot < 0).sum())
+    print(f"affinity T={T} E={E} k={k} cap={cap}: {dropped} assignments dropped")
+
+
+def test_forward_affinity_drop(cuda_device):
+    wl = WORKLOADS["switch_top1_cap1.25"].with_(T=600, d=256, E=8, f=256, capacity_factor=0.8,
+                                                logit_offsets="normal_var0.5", drop_policy="affinity",
+                                                name="affinity_drops")
+    inp = make_inputs(wl, cuda_device)
+    cfg, layer = _layer(wl, inp)
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    gi, gw = (_np(t) for t in layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]))
+    _check_device_error()
+    oi, ow, gap = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                  wl.renorm, nthreads=NTH)
+    cap = oracle.capacity(wl.capacity_factor, wl.T, wl.k, wl.E)
+    # the oracle's drop on its own routing and fp64 weights
+    o_off, _, o_slot, _ = oracle.dispatch_tc_affinity(oi, ow, wl.E, cap)
+    # the GPU's drop, recomputed from its own routing and weights: compare tokens routed alike
+    _, _, g_slot, _ = oracle.dispatch_tc_affinity(gi, gw, wl.E, cap)
+    same = (gi == oi).all(axis=1) & ((g_slot >= 0) == (o_slot >= 0)).all(axis=1)
+    assert (o_slot < 0).any() and same.mean() > 0.95
+    toks = np.nonzero(same)[0]
+    ref = oracle.forward_tc_streamed(inp["x"], oi, ow, o_slot, inp["W1"], inp["W3"], inp["W2"], toks,
+                                     nthreads=NTH)
+    err = rel_err(_np(y)[toks], ref)
+    print(f"affinity forward: {len(toks)} tokens, {int((o_slot < 0).sum())} dropped, err {err:.3e}")
+    assert err <= TOL["bf16"]
+
+
 def test_dispatch_expert_choice(cuda_device):
     wl = EC_CASES["ec_small"]
     inp = make_inputs(wl, "cpu", weights=False)

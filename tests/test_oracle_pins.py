@@ -591,3 +591,47 @@ def test_expert_rows_fp8_equals_expert_of_dequantised_weights():
     a0 = x @ W1
     full = ((a0 / (1 + np.exp(-a0))) * (x @ W3)) @ W2
     assert np.abs(got - full).max() <= 0.2 * np.abs(full).max()
+
+
+# ------------------------------------------------------------------ affinity-ordered capacity drop
+def test_affinity_drop_hand_example():
+    # expert 0 gets 4 assignments with cap 2: it keeps the two largest weights (tokens 3
+    # and 1; token 0 and 2 tie below them), rows in token order
+    idx = np.array([[0, 1], [0, 2], [0, 1], [0, 2]])
+    w = np.array([[0.3, 0.7], [0.6, 0.4], [0.3, 0.7], [0.9, 0.1]], np.float32)
+    off, cnt, slot, rows = oracle.dispatch_tc_affinity(idx, w, 3, cap=2)
+    assert list(cnt) == [4, 2, 2] and list(off) == [0, 2, 4, 6]
+    assert list(slot[:, 0]) == [-1, 0, -1, 1]        # tokens 1 and 3 kept by expert 0
+    assert list(rows) == [1, 3, 0, 2, 1, 3]
+    # a tie at the boundary goes to the lower token
+    w2 = w.copy()
+    w2[3, 0] = 0.3
+    off, cnt, slot, rows = oracle.dispatch_tc_affinity(idx, w2, 3, cap=2)
+    assert list(slot[:, 0]) == [0, 1, -1, -1]         # 0.6 (token 1) and the lowest of the 0.3 ties (token 0)
+
+
+@pytest.mark.parametrize("T,E,k,cap,skew", [(300, 8, 2, 60, 1.2), (500, 16, 1, 20, 1.5), (64, 4, 2, 0, 0.0),
+                                            (200, 8, 2, 1000, 1.0)])
+def test_affinity_drop_invariants(T, E, k, cap, skew):
+    from workloads import random_assignment
+    idx = random_assignment(T, E, k, seed=T + E, skew=skew).numpy()
+    rng = np.random.default_rng(T)
+    w = rng.choice(np.linspace(0.05, 0.95, 19), size=(T, k)).astype(np.float32)   # many ties
+    off, cnt, slot, rows = oracle.dispatch_tc_affinity(idx, w, E, cap)
+    t_off, t_cnt, t_slot, _ = oracle.dispatch_tc(idx, E, cap)
+    assert np.array_equal(cnt, t_cnt) and np.array_equal(off, t_off)   # same counts, same segments
+    if cap >= T * k:
+        assert np.array_equal(slot, t_slot)                              # nothing dropped: token order
+    for e in range(E):
+        mine = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e]
+        kept = [(t, j) for t, j in mine if slot[t, j] >= 0]
+        dropped = [(t, j) for t, j in mine if slot[t, j] < 0]
+        assert len(kept) == min(len(mine), cap)
+        # every kept assignment outranks every dropped one: larger weight, or equal and lower token
+        for tk, jk in kept:
+            for td, jd in dropped:
+                assert (w[tk, jk], -tk) > (w[td, jd], -td)
+        # kept rows of the segment in token order
+        rws = sorted(slot[t, j] for t, j in kept)
+        assert rws == list(range(off[e], off[e] + len(kept)))
+        assert [rows[r] for r in rws] == sorted(t for t, _ in kept)
