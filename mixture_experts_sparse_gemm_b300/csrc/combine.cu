@@ -2,10 +2,12 @@
 // y = sum_i G(x)_i E_i(x); §3.4 / §9.1: shared experts added unweighted;
 // "MoE稀疏架构" §4 step 5).
 //
-// One warp per token.  The warp first lists the token's (row, weight) pairs in
-// order -- slots j = 0..k-1 for token choice, experts e ascending for Expert
-// Choice -- then every lane accumulates 16-byte vectors of those Y rows in fp32
-// and writes the token's output row once.
+// One warp per (token, span of the row).  The warp first lists the token's
+// (row, weight) pairs in order -- slots j = 0..k-1 for token choice, experts e
+// ascending for Expert Choice -- then every lane accumulates 16-byte vectors of
+// those Y rows in fp32 (four rows in flight) and writes its part of the token's
+// output row once.  A span is the whole row unless there are fewer tokens than
+// eight warps per SM; then the rows are split so that the work spreads.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -64,8 +66,11 @@ struct CombineArgs {
     const float *w;
     uint4 *y;
     int T, E, k, mode, vecs;
+    int span;              // 16-byte vectors of a row per work item, a multiple of kStepVecs
     int64_t shared_row0;   // first shared row of Y, -1 without shared experts
 };
+
+constexpr int kStepVecs = 32;   // vectors one warp step covers: one per lane
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
@@ -73,7 +78,10 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
     __shared__ float s_w[kWarps][kMaxE];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_tok = (a.mode == MOE_EXPERT_CHOICE) ? a.E : a.k;
-    for (int t = blockIdx.x * kWarps + warp; t < a.T; t += gridDim.x * kWarps) {
+    const int nch = (a.vecs + a.span - 1) / a.span;
+    const int64_t items = (int64_t)a.T * nch;
+    for (int64_t item = (int64_t)blockIdx.x * kWarps + warp; item < items; item += (int64_t)gridDim.x * kWarps) {
+        const int t = (int)(item / nch), c = (int)(item % nch);
         int n = 0;
         for (int j0 = 0; j0 < per_tok; j0 += 32) {
             const int j = j0 + lane;
@@ -93,7 +101,8 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
         }
         __syncwarp();
         const uint4 *ys = a.shared_row0 >= 0 ? a.Y + (size_t)(a.shared_row0 + t) * a.vecs : nullptr;
-        for (int v = lane; v < a.vecs; v += 32) {
+        const int vend = min(a.vecs, (c + 1) * a.span);
+        for (int v = c * a.span + lane; v < vend; v += kStepVecs) {
             float acc[Vec<T>::N];
 #pragma unroll
             for (int i = 0; i < Vec<T>::N; ++i) acc[i] = 0.f;
@@ -110,11 +119,11 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
 #pragma unroll
             for (int q = 0; q < 3; ++q)
                 if (q < rem) r[q] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v];
-            const uint4 rs = ys ? ys[v] : make_uint4(0, 0, 0, 0);
+            r[3] = ys ? ys[v] : make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int q = 0; q < 3; ++q)
                 if (q < rem) accumulate<T>(acc, r[q], s_w[warp][i + q]);
-            if (ys) accumulate<T>(acc, rs, 1.f);
+            if (ys) accumulate<T>(acc, r[3], 1.f);
             a.y[(size_t)t * a.vecs + v] = pack<T>(acc);
         }
         __syncwarp();
@@ -136,12 +145,20 @@ cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, c
     a.mode = c.mode;
     a.vecs = c.d * z.elt / 16;
     a.shared_row0 = (c.n_shared > 0) ? z.rows_routed : -1;
-    int blocks = (c.T + kWarps - 1) / kWarps;
-    const int cap = num_sms() * 8;
+    // one warp per token; with fewer tokens than eight warps per SM the rows are
+    // split into spans so that the work still spreads over the GPU
+    const int64_t target = (int64_t)num_sms() * 8;
+    const int max_ch = (a.vecs + kStepVecs - 1) / kStepVecs;
+    int64_t nch = (target + c.T - 1) / (c.T > 0 ? c.T : 1);
+    nch = nch < 1 ? 1 : (nch > max_ch ? max_ch : nch);
+    a.span = (int)(((a.vecs + nch - 1) / nch + kStepVecs - 1) / kStepVecs * kStepVecs);
+    const int64_t items = (int64_t)c.T * ((a.vecs + a.span - 1) / a.span);
+    int64_t blocks = (items + kWarps - 1) / kWarps;
+    const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (c.dtype == MOE_F32) combine_kernel<float><<<blocks, 32 * kWarps, 0, s>>>(a);
-    else combine_kernel<__nv_bfloat16><<<blocks, 32 * kWarps, 0, s>>>(a);
+    if (c.dtype == MOE_F32) combine_kernel<float><<<(int)blocks, 32 * kWarps, 0, s>>>(a);
+    else combine_kernel<__nv_bfloat16><<<(int)blocks, 32 * kWarps, 0, s>>>(a);
     return cudaGetLastError();
 }
 

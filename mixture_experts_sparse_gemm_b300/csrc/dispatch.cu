@@ -104,32 +104,42 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
 
 // The same three steps in one CTA of 32 warps, for up to kPlanMax assignments.
 // Warp w owns one contiguous segment of the assignments (segments in warp order
-// are assignment order).  Pass 1: each warp counts its segment per expert into
-// its own shared-memory counters.
-// Then thread e turns the 32 per-warp counts of expert e into per-warp rank
-// bases and the raw count; warp 0 caps and scans the counts into off[].  Pass 2:
-// each warp re-reads its segment and ranks it in order from its bases; lanes
-// holding the same expert are found with ballots (warp_peers9).
+// are assignment order) and holds it in registers: lane l keeps assignments
+// a0 + 32 q + l, q < PER, all loaded at once.  Pass 1: each warp counts its
+// segment per expert into its own shared-memory counters.  Then thread e turns
+// the 32 per-warp counts of expert e into per-warp rank bases and the raw count;
+// warp 0 caps and scans the counts into off[].  Pass 2: each warp ranks its
+// segment in order from its bases; lanes holding the same expert are found with
+// ballots (warp_peers9).  row_token is assembled in shared memory and written out
+// in row order at the end.
 constexpr int kPlanWarps = 32;
-constexpr int64_t kPlanMax = 65536;
+constexpr int64_t kPlanMax = 32 * kPlanWarps * 32;   // 32 assignments per lane
 
+size_t plan_smem_bytes(int n, int E) { return sizeof(int) * ((size_t)kPlanWarps * E + E + 1 + (size_t)n); }
+
+template <int PER>
 __global__ void __launch_bounds__(32 * kPlanWarps)
     dispatch_plan_kernel(const int32_t *idx, int n, int k, int E, int cap, int32_t *cnt_raw, int32_t *off,
                          int32_t *slot_of, int32_t *row_token, unsigned *err) {
     extern __shared__ int sm[];
     int *wcnt = sm;                        // [kPlanWarps][E]: counts, then rank bases
     int *offs = wcnt + kPlanWarps * E;     // [E + 1]
+    int *rows_tok = offs + E + 1;          // [n]: token of each kept row
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = ((n + kPlanWarps - 1) / kPlanWarps + 31) & ~31;
+    const int seg = ((n + kPlanWarps - 1) / kPlanWarps + 31) & ~31;   // <= 32 * PER
     const int a0 = warp * seg, a1 = min(n, a0 + seg);
     int *my = wcnt + warp * E;
     for (int e = lane; e < E; e += 32) my[e] = 0;
-    __syncwarp();
-    __syncwarp();
-    for (int a = a0 + lane; a < a1; a += 32) {   // counts: fire-and-forget shared adds
-        const int e = idx[a];
-        if ((unsigned)e < (unsigned)E) atomicAdd(&my[e], 1);
+    int ev[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+        const int a = a0 + q * 32 + lane;
+        ev[q] = (a < a1) ? idx[a] : -1;
     }
+    __syncwarp();
+#pragma unroll
+    for (int q = 0; q < PER; ++q)   // counts: fire-and-forget shared adds
+        if ((unsigned)ev[q] < (unsigned)E) atomicAdd(&my[ev[q]], 1);
     __syncthreads();
     for (int e = tid; e < E; e += blockDim.x) {   // per-warp bases in segment order
         int s = 0;
@@ -165,59 +175,109 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
     }
     __syncthreads();
     for (int e = tid; e <= E; e += blockDim.x) off[e] = offs[e];
-    for (int b = a0; b < a1; b += 128) {
-        int ev[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int a = b + q * 32 + lane;
-            ev[q] = (a < a1) ? idx[a] : -1;
+    for (int q = 0; q < PER; ++q) {
+        if (a0 + q * 32 >= a1) break;   // warp-uniform
+        const int a = a0 + q * 32 + lane;
+        const bool valid = (unsigned)ev[q] < (unsigned)E;
+        if (a < a1 && !valid) {
+            slot_of[a] = -1;
+            atomicOr(err, kErrBadIndex);
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int a = b + q * 32 + lane;
-            const bool valid = (unsigned)ev[q] < (unsigned)E;
-            if (a < a1 && !valid) {
-                slot_of[a] = -1;
-                atomicOr(err, kErrBadIndex);
-            }
-            const int e = valid ? ev[q] : 0;
-            const unsigned peers = warp_peers9(valid ? (unsigned)e : 511u);   // invalid lanes group apart
-            const int rank_in = __popc(peers & ((1u << lane) - 1u));
-            const int base = valid ? my[e] : 0;
-            __syncwarp();
-            if (valid && rank_in == 0) my[e] = base + __popc(peers);
-            __syncwarp();
-            if (valid) {
-                const int r = base + rank_in;
-                const int slot = (cap < 0 || r < cap) ? offs[e] + r : -1;
-                slot_of[a] = slot;
-                if (slot >= 0) row_token[slot] = a / k;
-            }
+        const int e = valid ? ev[q] : 0;
+        const unsigned peers = warp_peers9(valid ? (unsigned)e : 511u);   // invalid lanes group apart
+        const int rank_in = __popc(peers & ((1u << lane) - 1u));
+        const int base = valid ? my[e] : 0;
+        __syncwarp();
+        if (valid && rank_in == 0) my[e] = base + __popc(peers);
+        __syncwarp();
+        if (valid) {
+            const int r = base + rank_in;
+            const int slot = (cap < 0 || r < cap) ? offs[e] + r : -1;
+            slot_of[a] = slot;
+            if (slot >= 0) rows_tok[slot] = a / k;
         }
     }
+    __syncthreads();
+    const int rows = offs[E];
+    for (int r = tid; r < rows; r += blockDim.x) row_token[r] = rows_tok[r];
+}
+
+template <int PER>
+cudaError_t launch_plan(const int32_t *idx, int n, int k, int E, int cap, int32_t *cnt_raw, int32_t *off,
+                        int32_t *slot_of, int32_t *row_token, unsigned *err, cudaStream_t s) {
+    const size_t smem = plan_smem_bytes(n, E);
+    cudaError_t ce = cudaFuncSetAttribute(dispatch_plan_kernel<PER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+    if (ce != cudaSuccess) return ce;
+    dispatch_plan_kernel<PER><<<1, 32 * kPlanWarps, smem, s>>>(idx, n, k, E, cap, cnt_raw, off, slot_of, row_token,
+                                                               err);
+    return cudaGetLastError();
 }
 
 
-// x_perm[row] = x[row_token[row]] for row < *rows (read on the device).
+// x_perm[row] = x[row_token[row]] for row < *rows (read on the device).  One warp
+// per (row, span of the row), four 16-byte vectors per lane in flight; a span is
+// the whole row unless there are fewer rows than 16 warps per SM.
+// With z.slot_of, the same launch zeroes the output rows of dropped tokens and
+// the dependency counters of the fused expert launch (see GatherZero).
 __global__ void __launch_bounds__(256)
-    gather_rows_kernel(const uint4 *__restrict__ x, int vecs, const int32_t *__restrict__ row_token,
-                       const int32_t *__restrict__ rows_dev, int64_t rows_host, uint4 *__restrict__ x_perm) {
+    gather_rows_kernel(const uint4 *__restrict__ x, int vecs, int span, const int32_t *__restrict__ row_token,
+                       const int32_t *__restrict__ rows_dev, int64_t rows_host, uint4 *__restrict__ x_perm,
+                       GatherZero z) {
     const int64_t rows = rows_dev ? (int64_t)*rows_dev : rows_host;
+    const int nch = (vecs + span - 1) / span;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    for (int64_t it = gw; it < rows * nch; it += nwarps) {
+        const int64_t r = it / nch;
+        const int c = (int)(it - r * nch);
         const uint4 *src = x + (size_t)row_token[r] * vecs;
         uint4 *dst = x_perm + (size_t)r * vecs;
-        int v = lane;
-        for (; v + 96 < vecs; v += 128) {
-            const uint4 a0 = src[v], a1 = src[v + 32], a2 = src[v + 64], a3 = src[v + 96];
-            dst[v] = a0;
-            dst[v + 32] = a1;
-            dst[v + 64] = a2;
-            dst[v + 96] = a3;
+        const int vend = min(vecs, (c + 1) * span);
+        for (int v = c * span + lane; v < vend; v += 128) {
+            uint4 t[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (v + 32 * q < vend) t[q] = src[v + 32 * q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (v + 32 * q < vend) dst[v + 32 * q] = t[q];
         }
-        for (; v < vecs; v += 32) dst[v] = src[v];
     }
+    if (z.slot_of) {
+        for (int64_t t0 = gw * 32; t0 < z.T; t0 += nwarps * 32) {   // warp-uniform bound
+            const int64_t t = t0 + lane;
+            unsigned m = __ballot_sync(0xffffffffu, t < z.T && z.slot_of[t] < 0);
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                uint4 *row = z.y + (size_t)(t0 + b) * vecs;
+                for (int v = lane; v < vecs; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (blockIdx.x == 0)
+            for (int i = threadIdx.x; i < z.ndep; i += blockDim.x) z.dep[i] = 0;
+    }
+}
+
+cudaError_t launch_gather(const void *x, int vecs, const int32_t *row_token, const int32_t *rows_dev,
+                          int64_t rows_host, void *x_perm, const GatherZero &z, cudaStream_t s) {
+    constexpr int kSpanStep = 128;   // vectors of one warp step (four per lane)
+    const int64_t target = (int64_t)num_sms() * 16;   // rows split only below 16 warps per SM
+    const int max_ch = (vecs + kSpanStep - 1) / kSpanStep;
+    int64_t nch = rows_host > 0 ? (target + rows_host - 1) / rows_host : 1;
+    nch = nch < 1 ? 1 : (nch > max_ch ? max_ch : nch);
+    const int span = (int)(((vecs + nch - 1) / nch + kSpanStep - 1) / kSpanStep * kSpanStep);
+    const int64_t items = rows_host * ((vecs + span - 1) / span);
+    int64_t blocks = (items + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, span, row_token, rows_dev,
+                                                   rows_host, static_cast<uint4 *>(x_perm), z);
+    return cudaGetLastError();
 }
 
 // Expert choice: off[e] = e*cap, cnt_raw[e] = cap, slot_of[t][e] = e*cap + r.
@@ -290,14 +350,6 @@ __global__ void affinity_rows_kernel(const int32_t *__restrict__ kept, const int
     }
 }
 
-int gather_grid(int64_t rows) {
-    const int64_t warps_needed = rows;
-    int64_t blocks = (warps_needed + 7) / 8;
-    const int64_t cap = (int64_t)num_sms() * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    return (int)blocks;
-}
 
 }  // namespace
 
@@ -310,12 +362,14 @@ size_t dispatch_tc_scratch_ints(int64_t assignments, int E) {
 
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
-                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s) {
+                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s,
+                               const GatherZero &zero) {
     const int64_t n = (int64_t)c.T * c.k;
     if (n <= kPlanMax) {
-        const size_t smem = sizeof(int) * ((size_t)kPlanWarps * c.E + 2 * c.E + 1);
-        dispatch_plan_kernel<<<1, 32 * kPlanWarps, smem, s>>>(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of,
-                                                               row_token, err);
+        const int per = (int)((n + 32 * kPlanWarps - 1) / (32 * kPlanWarps));   // assignments per lane
+        auto plan = per <= 8 ? launch_plan<8> : per <= 16 ? launch_plan<16> : launch_plan<32>;
+        const cudaError_t ce = plan(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, s);
+        if (ce != cudaSuccess) return ce;
     } else {
         const int nchunks = (int)((n + kChunk - 1) / kChunk);
         const int blocks = (nchunks + kWarpsPerCta - 1) / kWarpsPerCta;
@@ -327,15 +381,13 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
     }
     const int elt = c.dtype == MOE_F32 ? 4 : 2;
     const int vecs = c.d * elt / 16;
-    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,
-                                                      static_cast<uint4 *>(x_perm));
-    return cudaGetLastError();
+    return launch_gather(x, vecs, row_token, off + c.E, n, x_perm, zero, s);
 }
 
 cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
                                      const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                      float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, const GatherZero &zero) {
     const int64_t n = (int64_t)c.T * c.k;
     cudaError_t ce = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)c.E * c.T, s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(cnt_raw, 0, sizeof(int32_t) * c.E, s);
@@ -349,9 +401,7 @@ cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int
     affinity_rows_kernel<<<c.E, 256, 0, s>>>(kept, cnt_raw, cap, topk_idx, c.k, c.E, off, slot_of, row_token);
     const int elt = c.dtype == MOE_F32 ? 4 : 2;
     const int vecs = c.d * elt / 16;
-    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, row_token, off + c.E, 0,
-                                                      static_cast<uint4 *>(x_perm));
-    return cudaGetLastError();
+    return launch_gather(x, vecs, row_token, off + c.E, n, x_perm, zero, s);
 }
 
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
@@ -364,9 +414,7 @@ cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const
     ec_slots_kernel<<<blocks, 256, 0, s>>>(ec_tok, c.T, c.E, c.ec_capacity, off, cnt_raw, slot_of, err);
     const int elt = c.dtype == MOE_F32 ? 4 : 2;
     const int vecs = c.d * elt / 16;
-    gather_rows_kernel<<<gather_grid(n), 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, ec_tok, nullptr, n,
-                                                      static_cast<uint4 *>(x_perm));
-    return cudaGetLastError();
+    return launch_gather(x, vecs, ec_tok, nullptr, n, x_perm, GatherZero{}, s);
 }
 
 }  // namespace moe

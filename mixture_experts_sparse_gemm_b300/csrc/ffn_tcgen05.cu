@@ -128,7 +128,8 @@ cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const v
 
 cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                      const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
-                                     unsigned *err, cudaStream_t s, const int32_t *row_token, const float *row_gate) {
+                                     unsigned *err, cudaStream_t s, const int32_t *row_token, const float *row_gate,
+                                     bool dep_zeroed) {
     TcArgs g{};
     FfnMaps mu, md;
     if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], mu)) return cudaErrorInvalidValue;
@@ -138,8 +139,10 @@ cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const 
     g.gated = row_token != nullptr;
     g.row_token = row_token;
     g.row_gate = row_gate;
-    cudaError_t e = cudaMemsetAsync(dep, 0, sizeof(int) * ffn_dep_counters(c), s);
-    if (e != cudaSuccess) return e;
+    if (!dep_zeroed) {
+        const cudaError_t e = cudaMemsetAsync(dep, 0, sizeof(int) * ffn_dep_counters(c), s);
+        if (e != cudaSuccess) return e;
+    }
     const int64_t tiles = max_mtiles(c, z) * (g.p[0].g.nblk_routed + g.p[1].g.nblk_routed);
     if (fp8_weights(c)) return launch_gemm<256, kEpiFfn, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
     return launch_gemm<256, kEpiFfn>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);

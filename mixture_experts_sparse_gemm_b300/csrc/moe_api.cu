@@ -172,7 +172,8 @@ moe_status do_route(const moe_config &c, const void *x, const void *W_r, const f
 }
 
 moe_status do_dispatch(const moe_config &c, const int32_t *idx, const float *topk_w, const void *x, int32_t *off,
-                       int32_t *cnt_raw, int32_t *slot_of, void *x_perm, char *ws, unsigned *err, cudaStream_t s) {
+                       int32_t *cnt_raw, int32_t *slot_of, void *x_perm, char *ws, unsigned *err, cudaStream_t s,
+                       const GatherZero &zero = GatherZero{}) {
     if (c.mode == MOE_EXPERT_CHOICE)
         return from_cuda(launch_dispatch_ec(c, idx, x, off, cnt_raw, slot_of, x_perm, err, s));
     const DispatchWs L = dispatch_ws(c);
@@ -181,10 +182,10 @@ moe_status do_dispatch(const moe_config &c, const int32_t *idx, const float *top
         return from_cuda(launch_dispatch_affinity(
             c, z.cap, idx, topk_w, x, off, cnt_raw, slot_of, x_perm, reinterpret_cast<float *>(ws + L.aff_S),
             reinterpret_cast<int32_t *>(ws + L.aff_kept), reinterpret_cast<float *>(ws + L.aff_w),
-            reinterpret_cast<int32_t *>(ws + L.row_token), err, s));
+            reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero));
     return from_cuda(launch_dispatch_tc(c, z.cap, idx, x, off, cnt_raw, slot_of, x_perm,
                                         reinterpret_cast<int32_t *>(ws + L.chunk),
-                                        reinterpret_cast<int32_t *>(ws + L.row_token), err, s));
+                                        reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero));
 }
 
 moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, const void *packed, const void *x,
@@ -591,24 +592,33 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, co
     void *Y = w + L.Y;
     st = do_route(c, x, W_r, logit_offset, sel_bias, idx, gw, w + L.route, err, s);
     if (st != MOE_OK) return st;
-    st = do_dispatch(c, idx, gw, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s);
-    if (st != MOE_OK) return st;
     if (gated_down(c)) {
-        // one expert per token and no shared experts: the down GEMM writes each row
-        // straight to its token's output, scaled by the gate; dropped tokens stay 0
+        // one expert per token and no shared experts: the down GEMM writes each kept
+        // row straight to its token's output, scaled by the gate; the dispatch gather
+        // zeroes the output rows of dropped tokens (and the fused launch's counters)
         const Sizes z = sizes_of(c);
         const FfnWs F = ffn_ws(c);
         const int32_t *row_token = reinterpret_cast<const int32_t *>(w + L.dispatch + dispatch_ws(c).row_token);
-        if (cudaMemsetAsync(y, 0, (size_t)c.T * c.d * z.elt, s) != cudaSuccess) return MOE_ERR_CUDA;
-        if (ffn_fused(c))
+        const bool fused = ffn_fused(c);
+        GatherZero zero;
+        zero.slot_of = slot_of;
+        zero.T = c.T;
+        zero.y = static_cast<uint4 *>(y);
+        zero.dep = fused ? reinterpret_cast<int *>(w + L.ffn + F.dep) : nullptr;
+        zero.ndep = fused ? (int)ffn_dep_counters(c) : 0;
+        st = do_dispatch(c, idx, gw, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s, zero);
+        if (st != MOE_OK) return st;
+        if (fused)
             return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, x, w + L.ffn + F.H, nullptr, y,
                                                       reinterpret_cast<int *>(w + L.ffn + F.dep), err, s, row_token,
-                                                      gw));
+                                                      gw, /*dep_zeroed=*/true));
         cudaError_t e = launch_ffn_up_tcgen05(c, z, x_perm, off, packed, x, w + L.ffn + F.H, nullptr, err, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
         return from_cuda(launch_ffn_down_tcgen05(c, z, w + L.ffn + F.H, nullptr, off, packed, y, err, s, row_token,
                                                  gw));
     }
+    st = do_dispatch(c, idx, gw, x, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s);
+    if (st != MOE_OK) return st;
     st = do_ffn(c, x_perm, off, packed, x, Y, w + L.ffn, err, s);
     if (st != MOE_OK) return st;
     return from_cuda(launch_combine(c, sizes_of(c), Y, slot_of, gw, y, s));

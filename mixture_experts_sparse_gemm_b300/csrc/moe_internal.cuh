@@ -13,6 +13,7 @@ namespace moe {
 constexpr int kMaxE = 256;     // routed experts
 constexpr int kMaxK = 8;       // experts per token (token choice)
 constexpr int kPsumRows = 64;   // rows of per-CTA router score sums (CTA index mod 64)
+constexpr int kMaxRouteSplits = 8;   // split-K ways of the tensor-core router at most
 constexpr int kGroup = 64;     // W1/W3 interleave width of the packed up-projection
 
 // bits of the device error word
@@ -100,9 +101,21 @@ cudaError_t launch_column_select(const moe_config &c, const float *scores_t, int
 cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
                                 int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
                                 const float *partial, int splits, int npad, cudaStream_t s);
+// Extra work of the dispatch gather in the forward of a layer whose down GEMM
+// writes each kept token's output row itself (one expert per token, no shared
+// experts): zero the output rows of the dropped tokens (slot_of[t] < 0) and the
+// fused expert launch's dependency counters.  slot_of == nullptr: nothing extra.
+struct GatherZero {
+    const int32_t *slot_of = nullptr;   // [T] (k = 1)
+    int64_t T = 0;
+    uint4 *y = nullptr;                 // [T][d] in the activation type
+    int *dep = nullptr;
+    int ndep = 0;
+};
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
-                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s);
+                               int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s,
+                               const GatherZero &zero = GatherZero{});
 size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
 // affinity-ordered capacity drop (token choice): scratch S[E][T] fp32, kept[E][cap]
 // tokens and weights; launches a scatter, the column select, the row placement
@@ -110,7 +123,7 @@ size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
 cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
                                      const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                      float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
-                                     cudaStream_t s);
+                                     cudaStream_t s, const GatherZero &zero = GatherZero{});
 int dispatch_tc_launches(int64_t assignments);
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
                                int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s);
@@ -139,7 +152,7 @@ cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const v
 cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                      const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
                                      unsigned *err, cudaStream_t s, const int32_t *row_token = nullptr,
-                                     const float *row_gate = nullptr);
+                                     const float *row_gate = nullptr, bool dep_zeroed = false);
 size_t ffn_dep_counters(const moe_config &c);
 bool ffn_fused_supported(const moe_config &c);
 // psum_rows (nullable, [kPsumRows][E], zeroed by the caller): every CTA adds the

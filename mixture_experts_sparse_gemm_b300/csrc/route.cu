@@ -233,17 +233,25 @@ __global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const fl
 #pragma unroll
     for (int i = 0; i < KPL; ++i) pacc[i] = 0.f;
     for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
+        // every partial of the token is loaded before the sums (split order kept)
+        float pv[kMaxRouteSplits][KPL];
+#pragma unroll
+        for (int s = 0; s < kMaxRouteSplits; ++s)
+#pragma unroll
+            for (int i = 0; i < KPL; ++i) {
+                const int e = lane + 32 * i;
+                pv[s][i] = (s < splits && e < a.E) ? partial[((size_t)s * a.T + t) * npad + e] : 0.f;
+            }
         float u[KPL];
 #pragma unroll
         for (int i = 0; i < KPL; ++i) {
             const int e = lane + 32 * i;
-            float v = -FLT_MAX;
-            if (e < a.E) {
-                v = 0.f;
-                for (int s = 0; s < splits; ++s) v += partial[((size_t)s * a.T + t) * npad + e];
-                if (a.logit_offset) v += a.logit_offset[e];
-            }
-            u[i] = v;
+            float v = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxRouteSplits; ++s)
+                if (s < splits) v += pv[s][i];
+            if (e < a.E && a.logit_offset) v += a.logit_offset[e];
+            u[i] = (e < a.E) ? v : -FLT_MAX;
         }
         warp_score_select<KPL>(a, u, t, lane, pacc);
     }

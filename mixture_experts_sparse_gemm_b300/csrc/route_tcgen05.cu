@@ -34,7 +34,7 @@ int route_splits(const moe_config &c) {
     if (mtiles >= kRouteSms / 2) return 1;
     if (c.d / kBK < 32 && c.E * kslots < 256) return 1;
     int s = kRouteSms / (mtiles > 0 ? mtiles : 1);
-    s = s < 8 ? s : 8;
+    s = s < kMaxRouteSplits ? s : kMaxRouteSplits;
     const int quarter_k = (c.d / kBK) / 4;
     s = s < quarter_k ? s : quarter_k;
     return s >= 2 ? s : 1;

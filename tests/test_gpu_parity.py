@@ -156,10 +156,14 @@ DISPATCH_CASES = [
     (1000, 8, 2, 1.0, 1.5, 128, "bf16"),
     (257, 16, 3, 0.3, 2.0, 256, "bf16"),
     (1, 4, 2, 0.0, 0.0, 128, "bf16"),
+    (7, 8, 2, 0.0, 0.0, 1152, "bf16"),      # few rows: each split into spans, the last one ragged
     (300, 8, 2, 0.01, 0.0, 128, "bf16"),     # capacity 0: every assignment dropped
     (500, 8, 2, 1.25, 1.0, 64, "f32"),
-    (40000, 16, 2, 1.1, 1.0, 128, "bf16"),   # > 65536 assignments: the multi-CTA count/scan/rank path
-    (32768, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 65536: the largest single-CTA plan
+    (6000, 32, 2, 1.25, 1.0, 128, "bf16"),   # 12000 assignments: 16 per lane in the single-CTA plan
+    (16384, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 32768: the largest single-CTA plan (32 per lane)
+    (16385, 8, 2, 1.0, 1.0, 128, "bf16"),    # 32770: just past it, the multi-CTA count/scan/rank path
+    (40000, 16, 2, 1.1, 1.0, 128, "bf16"),   # 80000: multi-CTA
+    (32768, 256, 2, 1.0, 0.3, 128, "bf16"),  # 65536: multi-CTA with E = 256
 ]
 
 
@@ -228,7 +232,7 @@ def test_forward_affinity_drop(cuda_device):
                                                 name="affinity_drops")
     inp = make_inputs(wl, cuda_device)
     cfg, layer = _layer(wl, inp)
-    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"], out=_nan_out(layer))
     gi, gw = (_np(t) for t in layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]))
     _check_device_error()
     oi, ow, gap = oracle.route_tc(inp["x"], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
@@ -424,7 +428,10 @@ def test_load_stats(name, cuda_device):
 # ------------------------------------------------------------------------------------------ combine
 
 @pytest.mark.parametrize("T,E,k,C,d,ns,dt", [(1000, 8, 2, 1.0, 256, 0, "bf16"), (4096, 256, 8, 0.0, 7168, 1, "bf16"),
-                                             (333, 16, 1, 1.25, 128, 1, "f32")])
+                                             (333, 16, 1, 1.25, 128, 1, "f32"),
+                                             # few tokens: rows split into spans, the last one ragged
+                                             (16, 8, 2, 0.0, 4096, 0, "bf16"), (5, 8, 3, 0.0, 1152, 1, "bf16"),
+                                             (1, 4, 2, 0.0, 576, 1, "f32")])
 def test_combine_token_choice(T, E, k, C, d, ns, dt, cuda_device):
     cfg = B.config(T=T, d=d, E=E, f=64, k=k, capacity_factor=C, n_shared=ns, f_shared=64 if ns else 0, dtype=dt)
     tdt = torch.float32 if dt == "f32" else torch.bfloat16
@@ -490,10 +497,15 @@ E2E_SMALL = {
 }
 
 
+def _nan_out(layer):
+    """Output buffer full of NaN: a row the forward leaves unwritten fails the comparison."""
+    return torch.full((layer.cfg.T, layer.cfg.d), float("nan"), dtype=layer.dtype, device=layer.device)
+
+
 def _run_e2e(wl, n_sample, cuda_device):
     inp = make_inputs(wl, cuda_device)
     cfg, layer = _layer(wl, inp)
-    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"], out=_nan_out(layer))
     r_idx, r_w = layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
     _check_device_error()
     T = wl.T
@@ -750,7 +762,7 @@ def test_fp8_forward(name, cuda_device):
     wl = FP8_E2E[name]
     inp = make_inputs(wl, cuda_device)
     cfg, layer = _layer(wl, inp)
-    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    y = layer.forward(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"], out=_nan_out(layer))
     r_idx, _ = layer.route(inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"])
     _check_device_error()
     T = wl.T
