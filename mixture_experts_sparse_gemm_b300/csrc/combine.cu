@@ -76,6 +76,8 @@ template <typename T>
 __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
     __shared__ int s_row[kWarps][kMaxE];
     __shared__ float s_w[kWarps][kMaxE];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int per_tok = (a.mode == MOE_EXPERT_CHOICE) ? a.E : a.k;
     const int nch = (a.vecs + a.span - 1) / a.span;
@@ -157,9 +159,8 @@ cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, c
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (c.dtype == MOE_F32) combine_kernel<float><<<(int)blocks, 32 * kWarps, 0, s>>>(a);
-    else combine_kernel<__nv_bfloat16><<<(int)blocks, 32 * kWarps, 0, s>>>(a);
-    return cudaGetLastError();
+    auto kern = c.dtype == MOE_F32 ? combine_kernel<float> : combine_kernel<__nv_bfloat16>;
+    return launch_dependent(kern, dim3((unsigned)blocks), dim3(32 * kWarps), 0, s, false, a);
 }
 
 }  // namespace moe

@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
     int *wcnt = sm;                        // [kPlanWarps][E]: counts, then rank bases
     int *offs = wcnt + kPlanWarps * E;     // [E + 1]
     int *rows_tok = offs + E + 1;          // [n]: token of each kept row
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int seg = ((n + kPlanWarps - 1) / kPlanWarps + 31) & ~31;   // <= 32 * PER
     const int a0 = warp * seg, a1 = min(n, a0 + seg);
@@ -210,9 +212,8 @@ cudaError_t launch_plan(const int32_t *idx, int n, int k, int E, int cap, int32_
     cudaError_t ce = cudaFuncSetAttribute(dispatch_plan_kernel<PER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem);
     if (ce != cudaSuccess) return ce;
-    dispatch_plan_kernel<PER><<<1, 32 * kPlanWarps, smem, s>>>(idx, n, k, E, cap, cnt_raw, off, slot_of, row_token,
-                                                               err);
-    return cudaGetLastError();
+    return launch_dependent(dispatch_plan_kernel<PER>, dim3(1), dim3(32 * kPlanWarps), smem, s, false, idx, n, k, E,
+                            cap, cnt_raw, off, slot_of, row_token, err);
 }
 
 
@@ -225,6 +226,8 @@ __global__ void __launch_bounds__(256)
     gather_rows_kernel(const uint4 *__restrict__ x, int vecs, int span, const int32_t *__restrict__ row_token,
                        const int32_t *__restrict__ rows_dev, int64_t rows_host, uint4 *__restrict__ x_perm,
                        GatherZero z) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t rows = rows_dev ? (int64_t)*rows_dev : rows_host;
     const int nch = (vecs + span - 1) / span;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -275,9 +278,9 @@ cudaError_t launch_gather(const void *x, int vecs, const int32_t *row_token, con
     const int64_t cap = (int64_t)num_sms() * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), vecs, span, row_token, rows_dev,
-                                                   rows_host, static_cast<uint4 *>(x_perm), z);
-    return cudaGetLastError();
+    return launch_dependent(gather_rows_kernel, dim3((unsigned)blocks), dim3(256), 0, s, false,
+                            static_cast<const uint4 *>(x), vecs, span, row_token, rows_dev, rows_host,
+                            static_cast<uint4 *>(x_perm), z);
 }
 
 // Expert choice: off[e] = e*cap, cnt_raw[e] = cap, slot_of[t][e] = e*cap + r.

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_b300.h"
 
 namespace moe {
@@ -175,6 +177,42 @@ int route_tcgen05_launches(const moe_config &c);
 int num_sms();
 // architecture check and device error word of the current device (set up once per device)
 moe_status device_ready(unsigned **err_word);
+
+// ----------------------------------------------------------------------------- dependent launches
+// Kernels after the first of a library call are launched with programmatic stream
+// serialisation: such a grid may start while its predecessor on the stream is
+// still running, once every CTA of the predecessor has executed pdl_trigger() (or
+// exited).  Each of these kernels calls pdl_wait() -- which returns when the
+// predecessor grid has completed and its memory writes are visible -- before its
+// first access to global memory; only shared-memory and TMEM setup come earlier.
+// Without the launch attribute both instructions do nothing.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch with programmatic stream serialisation (and optionally as a cooperative
+// launch).  The kernel must follow the pdl_wait() rule above.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             bool cooperative, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ----------------------------------------------------------------------------- device helpers
 __device__ __forceinline__ float to_f32(float v) { return v; }

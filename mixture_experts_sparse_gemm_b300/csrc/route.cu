@@ -227,6 +227,8 @@ __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
 template <int KPL>
 __global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const float *__restrict__ partial, int splits,
                                                            int npad) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int nwarps = gridDim.x * (blockDim.x >> 5);
     float pacc[KPL];
@@ -465,11 +467,9 @@ cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, 
     int blocks = (c.T + 7) / 8;
     const int cap = num_sms() * 2;   // warps loop over tokens: the body stays in the instruction cache
     if (blocks > cap) blocks = cap;
-    if (c.E <= 32) route_select_kernel<1><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
-    else if (c.E <= 64) route_select_kernel<2><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
-    else if (c.E <= 128) route_select_kernel<4><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
-    else route_select_kernel<8><<<blocks, 256, 0, s>>>(a, partial, splits, npad);
-    return cudaGetLastError();
+    auto kern = c.E <= 32 ? route_select_kernel<1> : c.E <= 64 ? route_select_kernel<2>
+              : c.E <= 128 ? route_select_kernel<4> : route_select_kernel<8>;
+    return launch_dependent(kern, dim3(blocks), dim3(256), 0, s, false, a, partial, splits, npad);
 }
 
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,

@@ -46,6 +46,7 @@ size_t wr_t_bytes(const moe_config &c) { return align_up((size_t)padded_n(c.E) *
 __global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __nv_bfloat16 *__restrict__ wr_t,
                                         int d, int E, int npad, int32_t *seg, int T) {
     __shared__ __nv_bfloat16 tile[32][34];
+    pdl_trigger();   // the router GEMM may start its setup; it waits for this grid before reading
     const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
     for (int ii = threadIdx.y; ii < 32; ii += blockDim.y) {
         const int i = i0 + ii, e = e0 + threadIdx.x;

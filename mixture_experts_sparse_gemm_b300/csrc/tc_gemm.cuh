@@ -427,6 +427,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
     }
     __syncthreads();
     fence_after();
+    pdl_wait();      // the previous kernel's outputs (segment offsets, A rows) are visible from here on
+    pdl_trigger();
     const uint32_t tmem_base = *tmem_holder;
     const int S = build_tile_table<kBM>(a.p[0].g, tile_start0, seg_row0, seg_rows);
     const int total0 = tile_start0[S];
@@ -746,6 +748,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
 
 // Persistent launch: one CTA per SM (at most max_tiles).  A kEpiFfn launch has CTAs
 // waiting on other CTAs' up tiles, so it is a cooperative launch (all CTAs resident).
+// Every CTA waits for the previous kernel on the stream before its first global
+// access, so the launch is a dependent one and its setup overlaps that kernel.
 template <int BN, int EPI, bool W8 = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
                         const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args, int64_t max_tiles,
@@ -757,16 +761,20 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
     if (err != cudaSuccess) return err;
     int grid = num_sms();
     if (max_tiles < grid) grid = (int)(max_tiles > 1 ? max_tiles : 1);
-    if (EPI == kEpiFfn) {
+    // always a dependent launch (the kernel waits for its predecessor before reading
+    // global memory); a kEpiFfn launch is also cooperative
+    err = launch_dependent(kern, dim3(grid), dim3(kBlock), smem, s, EPI == kEpiFfn, a0, a1, b0, b1, a2, a3, args);
+    if (err != cudaSuccess && EPI == kEpiFfn) {
+        // a runtime that refuses the two attributes together: plain cooperative launch
+        (void)cudaGetLastError();
         TcArgs targs = args;
         void *params[] = {const_cast<CUtensorMap *>(&a0), const_cast<CUtensorMap *>(&a1),
                           const_cast<CUtensorMap *>(&b0), const_cast<CUtensorMap *>(&b1),
                           const_cast<CUtensorMap *>(&a2), const_cast<CUtensorMap *>(&a3), &targs};
-        return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kBlock), params,
-                                           smem, s);
+        err = cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), dim3(grid), dim3(kBlock), params,
+                                          smem, s);
     }
-    kern<<<grid, kBlock, smem, s>>>(a0, a1, b0, b1, a2, a3, args);
-    return cudaGetLastError();
+    return err;
 }
 
 // Single-GEMM launches pass their A maps again for the unused second phase.
