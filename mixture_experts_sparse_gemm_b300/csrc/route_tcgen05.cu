@@ -8,8 +8,12 @@
 // §9.1) weights; for Expert Choice (§3.3) it writes the softmax scores
 // expert-major for the column selection.  The logits never reach HBM.
 //
-// W_r arrives as [d][E] (the pages' x W_r); the MMA wants it K-major, so a small
-// transpose writes W_r^T [Npad][d] (zero rows E..Npad-1) into the workspace.
+// W_r arrives as [d][E] (the pages' x W_r).  When its rows are whole 16-byte units
+// (E a multiple of 8) the MMA reads it in place as an MN-major B operand: TMA boxes
+// of [64 d rows][64 experts], columns past E zero-filled, N = E rounded up to 64..256.
+// Otherwise a small transpose writes W_r^T [Npad][d] (zero rows E..Npad-1) into the
+// workspace for the K-major path.  The token rows are the tile table's one
+// unrouted segment [0, T), so no segment table is needed in device memory.
 #include "tc_gemm.cuh"
 
 namespace moe {
@@ -40,11 +44,20 @@ int route_splits(const moe_config &c) {
     return s >= 2 ? s : 1;
 }
 
-size_t wr_t_bytes(const moe_config &c) { return align_up((size_t)padded_n(c.E) * c.d * 2, 256); }
+// W_r read in place (MN-major B): its rows of E bf16 are 16-byte multiples
+bool wr_in_place(const moe_config &c) { return c.E % 8 == 0; }
+// N of the router GEMM: the MN-major boxes are 64 experts wide
+int route_n(const moe_config &c) {
+    const int n = padded_n(c.E);
+    return wr_in_place(c) && n < 64 ? 64 : n;
+}
+size_t wr_t_bytes(const moe_config &c) {
+    return wr_in_place(c) ? 0 : align_up((size_t)route_n(c) * c.d * 2, 256);
+}
 
-// wr_t[e][i] = W_r[i][e] for e < E, 0 for E <= e < npad; seg = {0, T}
+// wr_t[e][i] = W_r[i][e] for e < E, 0 for E <= e < npad
 __global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __nv_bfloat16 *__restrict__ wr_t,
-                                        int d, int E, int npad, int32_t *seg, int T) {
+                                        int d, int E, int npad) {
     __shared__ __nv_bfloat16 tile[32][34];
     pdl_trigger();   // the router GEMM may start its setup; it waits for this grid before reading
     const int e0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
@@ -56,10 +69,6 @@ __global__ void transpose_router_kernel(const __nv_bfloat16 *__restrict__ Wr, __
     for (int ee = threadIdx.y; ee < 32; ee += blockDim.y) {
         const int e = e0 + ee, i = i0 + threadIdx.x;
         if (e < npad && i < d) wr_t[(size_t)e * d + i] = tile[threadIdx.x][ee];
-    }
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) {
-        seg[0] = 0;
-        seg[1] = T;
     }
 }
 
@@ -92,29 +101,34 @@ bool route_tcgen05_supported(const moe_config &c) { return bf16_acts(c) && c.E <
 
 size_t route_tcgen05_scratch_bytes(const moe_config &c) {
     const int s = route_splits(c);
-    return wr_t_bytes(c) + 256 + (s > 1 ? sizeof(float) * (size_t)s * c.T * padded_n(c.E) : 0);
+    return wr_t_bytes(c) + (s > 1 ? sizeof(float) * (size_t)s * c.T * route_n(c) : 0);
 }
 
-int route_tcgen05_launches(const moe_config &c) { return route_splits(c) > 1 ? 3 : 2; }
+int route_tcgen05_launches(const moe_config &c) { return (wr_in_place(c) ? 0 : 1) + (route_splits(c) > 1 ? 2 : 1); }
 
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
                                  const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t,
                                  float *psum_rows, void *wr_t, unsigned *err, cudaStream_t s) {
-    const int npad = padded_n(c.E);
+    const int npad = route_n(c);
     char *scratch = static_cast<char *>(wr_t);
-    __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(scratch);
-    int32_t *seg = reinterpret_cast<int32_t *>(scratch + wr_t_bytes(c));
-    float *partial = reinterpret_cast<float *>(scratch + wr_t_bytes(c) + 256);
+    float *partial = reinterpret_cast<float *>(scratch + wr_t_bytes(c));
     const int splits = route_splits(c);
-    const dim3 tg((npad + 31) / 32, (c.d + 31) / 32);
-    transpose_router_kernel<<<tg, dim3(32, 8), 0, s>>>(static_cast<const __nv_bfloat16 *>(W_r), wt, c.d, c.E, npad,
-                                                       seg, c.T);
     CUtensorMap a0, b0;
     bool ok = make_tmap_bf16(&a0, x, (uint64_t)c.T, c.d, kBM);
-    ok = ok && make_tmap_bf16(&b0, wt, (uint64_t)npad, c.d, npad);
-    if (!ok) return cudaErrorInvalidValue;
     TcArgs g{};
-    g.p[0].g = GroupedShape{seg, 1, 0, 1, 0};
+    if (wr_in_place(c)) {
+        // [d][E] row-major, boxes of 64 d rows x 64 experts (past E: zero fill)
+        ok = ok && make_tmap_bf16(&b0, W_r, (uint64_t)c.d, c.E, 64);
+        g.p[0].b_mn = 1;
+    } else {
+        __nv_bfloat16 *wt = reinterpret_cast<__nv_bfloat16 *>(scratch);
+        const dim3 tg((npad + 31) / 32, (c.d + 31) / 32);
+        transpose_router_kernel<<<tg, dim3(32, 8), 0, s>>>(static_cast<const __nv_bfloat16 *>(W_r), wt, c.d, c.E,
+                                                           npad);
+        ok = ok && make_tmap_bf16(&b0, wt, (uint64_t)npad, c.d, npad);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    g.p[0].g = GroupedShape{nullptr, 0, c.T, 1, 1};   // one unrouted segment: the T token rows
     g.p[0].K0 = c.d;
     g.p[0].K1 = c.d;
     g.p[0].b_rows0 = npad;
@@ -124,7 +138,7 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
     const int64_t tiles = (c.T + kBM - 1) / kBM;
     if (splits > 1) {
         // split-K partial logits, then warp-per-token scoring and selection
-        g.p[0].g.nblk_routed = splits;
+        g.p[0].g.nblk_shared = splits;
         g.p[0].ksplit = splits;
         g.p[0].C0 = partial;
         g.p[0].ldc0 = c.T;

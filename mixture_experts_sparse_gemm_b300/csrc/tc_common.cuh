@@ -153,12 +153,29 @@ __device__ __forceinline__ uint64_t sdesc_k128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor of an MN-major operand: rows of 128 bytes (64
+// bf16 along M/N) one per K index, 128-byte swizzled as TMA writes a [64 K][64 MN]
+// box; 8-row groups (8 K) are 1024 bytes apart (stride byte offset) and successive
+// 64-wide MN chunks `lbo` bytes apart (leading byte offset).  A K step of 16 moves
+// the start address by 16 rows = 2048 bytes.
+__device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A/B, fp32 D, both K-major:
 // D format [4,6) = 1 (f32), A format [7,10) = 1 (bf16), B format [10,13) = 1,
 // N >> 3 at [17,23), M >> 4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// bit 16 of the instruction descriptor: B is MN-major ("transpose B")
+constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 }  // namespace tc
 

@@ -97,6 +97,9 @@ struct TcGemm {
     // FP8 weights (W8 kernels): fp32 scale of every B row (output column), routed
     // [E][b_rows0] and shared [N]; applied to the accumulator in the epilogue
     const float *sc0, *sc1;
+    // B given MN-major through tmB0 / tmB1: a row-major [K][N] matrix read in place,
+    // each stage BN / 64 boxes of [64 K rows][64 N] (BN >= 64; router launches only)
+    int b_mn;
 };
 
 struct TcArgs {
@@ -371,6 +374,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                            TcArgs a) {
     using C = TcCfg<BN, W8>;
     constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
+    constexpr bool kRouter = EPI >= kEpiPartial;   // router launches may read B (W_r) MN-major
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
@@ -533,6 +537,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     if (bt)
                         bulk_load(smem_u32(st + C::kABytes + (W8 ? C::kBBytes : 0)), bt + (size_t)(kb0 + kb) * img_bytes,
                                   kBCopy, fb);
+                    else if (kRouter && BN >= 64 && G.b_mn)
+                        for (int j = 0; j < BN / 64; ++j)   // 64-wide N chunks, 8 KB apart
+                            tma_load_2d(smem_u32(st + C::kABytes + j * 8192), mB,
+                                        (G.ksplit > 1 ? 0 : t.nb * BN) + 64 * j, (kb0 + kb) * kBK, fb);
                     else
                         tma_load_2d(smem_u32(st + C::kABytes), mB, (kb0 + kb) * kBK, brow, fb);
                     ++issued;
@@ -592,13 +600,15 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     fence_after();
                     const uint32_t sa = smem_u32(tiles + (size_t)stage * C::kStageBytes);
                     const uint64_t adesc = sdesc_k128(sa);
-                    const uint64_t bdesc = sdesc_k128(sa + C::kABytes);
+                    const bool bmn = kRouter && G.b_mn != 0;
+                    const uint64_t bdesc = bmn ? sdesc_mn128(sa + C::kABytes, 8192) : sdesc_k128(sa + C::kABytes);
+                    // K step of 16: 32 bytes inside the K-major swizzle atom, or 16 rows of
+                    // the MN-major tile (encoded >> 4)
+                    const uint64_t bstep = bmn ? (2048 >> 4) : 2;
+                    const uint32_t idesc = bmn ? (kIdesc | kIdescBMajorMN) : kIdesc;
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // advance 16 bf16 = 32 bytes inside the swizzle atom (encoded >> 4)
-                        mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), kIdesc,
-                                 (kb | kk) != 0);
-                    }
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc, (kb | kk) != 0);
                     mma_commit(smem_u32(&empty[stage]));
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -683,8 +693,9 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             } else if constexpr (EPI == kEpiPartial) {
                 // fp32 partial sums of K split t.nb: C0[split][row][BN], row stride BN
                 float *P = static_cast<float *>(G.C0) + ((size_t)t.nb * G.ldc0 + grow) * BN;
+                const int nchunk = min(BN / 16, (a.route.E + 15) / 16);   // chunks holding experts
 #pragma unroll 1
-                for (int c = 0; c < BN / 16; ++c) {
+                for (int c = 0; c < nchunk; ++c) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c * 16, v);
                     tmem_ld_wait();

@@ -61,6 +61,13 @@ SMALL_TC = {
     "t1": WORKLOADS["mixtral_T16"].with_(T=1, d=128, f=64, name="t1"),
     # few token tiles and a long d: the router splits K over CTAs and selects per warp
     "sigmoid_top8_splitk": WORKLOADS["deepseek_v3"].with_(T=200, d=2048, f=128, f_shared=128, name="sig8_split"),
+    # W_r read in place by the tensor-core router: two 64-expert chunks (E = 128), and
+    # E = 24 (a multiple of 8, not of 64: the chunk past E is zero-filled); E = 12 is
+    # not a multiple of 8 and takes the transposed copy of W_r
+    "sigmoid_top4_e128": WORKLOADS["deepseek_v3"].with_(T=300, d=256, E=128, k=4, f=128, f_shared=128,
+                                                         name="sig4_e128"),
+    "top2_e24": WORKLOADS["mixtral_T256"].with_(T=500, d=256, E=24, f=128, name="top2_e24"),
+    "top2_e12": WORKLOADS["mixtral_T256"].with_(T=500, d=256, E=12, f=128, name="top2_e12"),
 }
 ROUTE_CASES = ["tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T4096", "deepseek_v3"] + list(SMALL_TC)
 
