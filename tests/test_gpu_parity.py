@@ -561,6 +561,37 @@ def test_forward_small_all_tokens(name, cuda_device):
     _run_e2e(E2E_SMALL[name], None, cuda_device)
 
 
+BACK_TO_BACK = dict(E2E_SMALL, split_router_shared=WORKLOADS["deepseek_v3"].with_(
+    T=200, d=2048, E=32, f=128, f_shared=128, name="b2b_split"))
+
+
+@pytest.mark.parametrize("name", list(BACK_TO_BACK))
+def test_forward_back_to_back(name, cuda_device):
+    """Forwards queued back to back on one stream with no host synchronisation, their
+    input rewritten by a torch kernel in between (every kernel after the first of a
+    call starts before its predecessor ends and waits on the device): each output
+    equals the same forward run on its own, bit for bit."""
+    wl = BACK_TO_BACK[name]
+    inp = make_inputs(wl, cuda_device)
+    cfg, layer = _layer(wl, inp)
+    args = (inp["W_r"], inp["logit_offset"], inp["sel_bias"])
+    xs = [inp["x"], random_rows(wl.T, wl.d, seed=7, dtype=inp["x"].dtype, device=cuda_device), inp["x"] * 0.5]
+    ref = []
+    for x in xs:
+        y = layer.forward(x, *args, out=_nan_out(layer))
+        _check_device_error()
+        ref.append(y.clone())
+    xbuf = torch.empty_like(inp["x"])
+    outs = []
+    for _ in range(2):
+        for x in xs:
+            xbuf.copy_(x)
+            outs.append(layer.forward(xbuf, *args, out=_nan_out(layer)))
+    _check_device_error()
+    for i, y in enumerate(outs):
+        assert torch.equal(y, ref[i % len(xs)]), f"forward {i} differs from its isolated run"
+
+
 def test_forward_empty_batch(cuda_device):
     wl = WORKLOADS["mixtral_T16"].with_(T=0, d=128, f=64)
     cfg = B.config_from_workload(wl)
