@@ -1,7 +1,7 @@
 // Persistent grouped GEMM on the 5th-generation tensor cores (bf16 in, fp32
 // accumulate in TMEM), shared by the expert GEMMs and the router.
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM, 6 warps (15 with FP8 weights):
 //   warp 0      TMA producer: 128x64 A tile + BNx64 B tile per stage, 128-byte
 //               swizzle, into a STAGES-deep shared-memory ring (full/empty mbarriers)
 //   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16)
@@ -9,9 +9,11 @@
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
 //               thread), then the epilogue of the instantiation; it overlaps the
 //               next tile's main loop through the second accumulator
-//   warps 6..13 (W8 only) converters: the FP8 weight tile of a stage -> the bf16
-//               tile of the same stage, which the MMA reads; the per-column
-//               weight scales are applied in the epilogue
+//   warps 6..13 (W8 only) converters: an FP8 weight tile of the FP8 ring -> one
+//               of two bf16 B buffers, which the MMA reads; the per-column weight
+//               scales are applied in the epilogue
+//   warp 14     (W8 only) FP8 producer: the weight tiles into their own ring,
+//               ahead of the MMA (warp 0 then brings only A, into its own ring)
 // Tiles never straddle segments: the tile table is built on the device from
 // off[] (segment s < E = routed expert s, segment E = merged shared experts), and
 // a segment's last M tile reads rows past its end (the next segment's rows, or
@@ -48,22 +50,29 @@ constexpr int kEpiPartial = 3;  // split-K partial sums: fp32 rows of C0[split][
 // router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
 constexpr int kEpiRoute = 10;
 
-// W8: B arrives as an FP8 E4M3 tile (BN x 64 bytes) in each stage; eight converter
-// warps expand it into the bf16 tile of the same stage, which the MMA reads.
-// Stage layout: A (bf16) | B (bf16, MMA operand) | B8 (FP8, W8 only).
+// W8: B arrives as FP8 E4M3 tiles (BN x 64 bytes) in a ring of its own (6 slots),
+// brought by an FP8 producer warp and released by eight converter warps as soon as
+// they have expanded a tile into one of two bf16 B buffers, which the MMA reads
+// and releases.  A has its own ring (3 stages).  The weights thus run up to eight
+// k blocks ahead of the MMA, as many weight bytes in flight as the bf16 kernel has.
+// Shared memory: stages (bf16: A | B; W8: A) | W8: bf16 B buffers | W8: FP8 slots.
 template <int BN, bool W8 = false>
 struct TcCfg {
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = BN * kBK * 2;      // bf16 B tile, as the MMA reads it
     static constexpr int kB8Bytes = BN * kBK;         // FP8 B tile, as the copy brings it (W8)
-    static constexpr int kStageBytes = kABytes + kBBytes + (W8 ? kB8Bytes : 0);
+    static constexpr int kStageBytes = kABytes + (W8 ? 0 : kBBytes);
     static constexpr int kStages = W8 ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
-    static constexpr int kConvWarps = W8 ? 8 : 0;
-    static constexpr int kThreadsCta = kThreads + 32 * kConvWarps;
+    static constexpr int kBBufs = W8 ? 3 : 0;         // bf16 B buffers (W8)
+    static constexpr int kB8Stages = W8 ? 4 : 0;      // FP8 ring slots
+    static constexpr int kConvWarps = W8 ? 12 : 0;
+    static constexpr int kB8Warp = kThreads / 32 + kConvWarps;   // W8: warp of the FP8 copies
+    static constexpr int kThreadsCta = kThreads + 32 * kConvWarps + (W8 ? 32 : 0);
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
-    static constexpr int kBarBytes = (3 * kStages + 5) * 8;
+    static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kBBufs + 2 * kB8Stages) * 8;
     static constexpr int kMiscBytes = 64 + sizeof(int) * (6 * (kMaxE + 2));
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes + kMiscBytes;
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kBBufs * kBBytes +
+                                    (size_t)kB8Stages * kB8Bytes + kBarBytes + kMiscBytes;
 };
 
 struct RouteEpi {
@@ -378,14 +387,19 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + (size_t)C::kStages * C::kStageBytes);
+    uint8_t *bbuf = tiles + (size_t)C::kStages * C::kStageBytes;   // W8: bf16 B buffers
+    uint8_t *b8ring = bbuf + (size_t)C::kBBufs * C::kBBytes;        // W8: FP8 B slots
+    uint64_t *bars = reinterpret_cast<uint64_t *>(b8ring + (size_t)C::kB8Stages * C::kB8Bytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + C::kStages;
     uint64_t *tfull = bars + 2 * C::kStages;
     uint64_t *tempty = tfull + 2;
     uint64_t *drain = tempty + 2;
-    uint64_t *conv = drain + 1;   // W8: the bf16 B tile of stage s written and fenced (converter warps)
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(conv + C::kStages);
+    uint64_t *conv = drain + 1;                 // W8: bf16 B buffer written and fenced (converter warps)
+    uint64_t *bempty = conv + C::kBBufs;        // W8: bf16 B buffer read by the MMA
+    uint64_t *f8full = bempty + C::kBBufs;      // W8: FP8 slot landed
+    uint64_t *f8empty = f8full + C::kB8Stages;  // W8: FP8 slot expanded by all converter warps
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(f8empty + C::kB8Stages);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *tile_start0 = reinterpret_cast<int *>(tmem_holder + 16);   // tiles of phase 0 per segment
     int *tile_start1 = tile_start0 + (kMaxE + 2);                   // tiles of phase 1 per segment
@@ -409,8 +423,16 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             mbar_init(smem_u32(&tempty[i]), 4);
         }
         mbar_init(smem_u32(drain), 1);
-        if (W8)
-            for (int st = 0; st < C::kStages; ++st) mbar_init(smem_u32(&conv[st]), C::kConvWarps);
+        if (W8) {
+            for (int b = 0; b < C::kBBufs; ++b) {
+                mbar_init(smem_u32(&conv[b]), C::kConvWarps);
+                mbar_init(smem_u32(&bempty[b]), 1);
+            }
+            for (int f = 0; f < C::kB8Stages; ++f) {
+                mbar_init(smem_u32(&f8full[f]), 1);
+                mbar_init(smem_u32(&f8empty[f]), C::kConvWarps);
+            }
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
         prefetch_tmap(&tmA0);
@@ -532,11 +554,12 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
-                    mbar_arrive_expect_tx(fb, C::kABytes + kBCopy);   // A + B (FP8 for W8)
+                    mbar_arrive_expect_tx(fb, C::kABytes + (W8 ? 0 : kBCopy));   // A + B (W8: A only)
                     tma_load_2d(smem_u32(st), mA, (kb0 + kb) * kBK, arow, fb);
-                    if (bt)
-                        bulk_load(smem_u32(st + C::kABytes + (W8 ? C::kBBytes : 0)), bt + (size_t)(kb0 + kb) * img_bytes,
-                                  kBCopy, fb);
+                    if (W8)
+                        ;   // the FP8 B tiles come through their own ring (B8 producer warp)
+                    else if (bt)
+                        bulk_load(smem_u32(st + C::kABytes), bt + (size_t)(kb0 + kb) * img_bytes, kBCopy, fb);
                     else if (kRouter && BN >= 64 && G.b_mn)
                         for (int j = 0; j < BN / 64; ++j)   // 64-wide N chunks, 8 KB apart
                             tma_load_2d(smem_u32(st + C::kABytes + j * 8192), mB,
@@ -573,6 +596,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
             int stage = 0;
             uint32_t phase = 0;
+            int bb = 0;           // W8: bf16 B buffer
+            uint32_t bph = 0;
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
@@ -593,15 +618,18 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                         ok = false;
                         break;
                     }
-                    if (W8 && !wait_bounded(smem_u32(&conv[stage]), phase, abort_flag, a.err)) {
-                        ok = false;
-                        break;
+                    if constexpr (W8) {
+                        if (!wait_bounded(smem_u32(&conv[bb]), bph, abort_flag, a.err)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     fence_after();
                     const uint32_t sa = smem_u32(tiles + (size_t)stage * C::kStageBytes);
                     const uint64_t adesc = sdesc_k128(sa);
                     const bool bmn = kRouter && G.b_mn != 0;
-                    const uint64_t bdesc = bmn ? sdesc_mn128(sa + C::kABytes, 8192) : sdesc_k128(sa + C::kABytes);
+                    const uint32_t sb = W8 ? smem_u32(bbuf + (size_t)bb * C::kBBytes) : sa + C::kABytes;
+                    const uint64_t bdesc = bmn ? sdesc_mn128(sb, 8192) : sdesc_k128(sb);
                     // K step of 16: 32 bytes inside the K-major swizzle atom, or 16 rows of
                     // the MN-major tile (encoded >> 4)
                     const uint64_t bstep = bmn ? (2048 >> 4) : 2;
@@ -610,6 +638,13 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     for (int kk = 0; kk < kBK / 16; ++kk)
                         mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc, (kb | kk) != 0);
                     mma_commit(smem_u32(&empty[stage]));
+                    if constexpr (W8) {
+                        mma_commit(smem_u32(&bempty[bb]));
+                        if (++bb == C::kBBufs) {
+                            bb = 0;
+                            bph ^= 1u;
+                        }
+                    }
                     if (++stage == C::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -624,17 +659,68 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {
             }
         }
-    } else if (W8 && warp >= 6) {
+    } else if (W8 && warp == C::kB8Warp) {
+        // ---------------------------------------------------------------- FP8 B producer (W8)
+        // The weight tiles of every k block, in the walk's order, into the FP8 ring;
+        // a slot is refilled once all converter warps have expanded it.
+        if (lane == 0) {
+            int f = 0;
+            uint32_t fph = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileAt t = locate(tile);
+                const TcGemm &G = a.p[t.phase];
+                const bool routed = t.s < G.g.E;
+                int kb0, nk;
+                krange(t, G, kb0, nk);
+                // rows [nb*BN, nb*BN + BN) of the N dimension are slice `sub` of image `img`
+                const int per = G.img_rows / BN, img = t.nb / per, sub = t.nb % per;
+                const size_t img_bytes = (size_t)G.img_rows * kBK;
+                const uint8_t *bt = (routed ? G.Bt0 + (size_t)t.s * G.bt_seg0 : G.Bt1) + (size_t)img * nk * img_bytes +
+                                    (size_t)sub * C::kB8Bytes;
+                for (int kb = 0; kb < nk; ++kb) {
+                    if (!wait_bounded(smem_u32(&f8empty[f]), fph ^ 1u, abort_flag, a.err)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&f8full[f]);
+                    mbar_arrive_expect_tx(fb, C::kB8Bytes);
+                    bulk_load(smem_u32(b8ring + (size_t)f * C::kB8Bytes), bt + (size_t)(kb0 + kb) * img_bytes,
+                              C::kB8Bytes, fb);
+                    ++issued;
+                    if (++f == C::kB8Stages) {
+                        f = 0;
+                        fph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // leave no copy in flight: wait (bounded) for the last slots issued
+                const int n = issued < C::kB8Stages ? issued : C::kB8Stages;
+                for (int i = 0; i < n; ++i) {
+                    if (--f < 0) {
+                        f = C::kB8Stages - 1;
+                        fph ^= 1u;
+                    }
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(smem_u32(&f8full[f]), fph) && globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (W8 && warp >= kThreads / 32) {
         // ---------------------------------------------------------------- converter (W8)
-        // k block j (stage j % kStages): the FP8 tile -> the stage's bf16 tile in the
-        // 128-byte swizzled K-major layout the MMA descriptor expects.  Thread q of 256
-        // converts the 16-byte chunks q, q + 256, ... (contiguous per warp): chunk c is
-        // row c / 4, bytes 16 (c % 4).. of the row = K elements 16 (c % 4)..+15, which
-        // land in bf16 chunks 2 (c % 4) and 2 (c % 4) + 1, swizzled by row % 8.  Lane 0
-        // polls the barrier; __syncwarp orders the other lanes' reads after it.
+        // k block j: FP8 slot j % kB8Stages -> bf16 B buffer j % kBBufs, once the MMA
+        // has released that buffer, in the 128-byte swizzled K-major layout the
+        // MMA descriptor expects.  Thread q of 256 converts the 16-byte chunks q,
+        // q + 256, ... (contiguous per warp): chunk c is row c / 4, bytes 16 (c % 4).. of
+        // the row = K elements 16 (c % 4)..+15, which land in bf16 chunks 2 (c % 4) and
+        // 2 (c % 4) + 1, swizzled by row % 8.  Lane 0 polls the barriers; __syncwarp
+        // orders the other lanes' accesses after it.
         const int q0 = threadIdx.x - kThreads;
-        int stage = 0;
-        uint32_t phase = 0;
+        int bb = 0, f = 0;
+        uint32_t bph = 0, fph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             const TileAt t = locate(tile);
@@ -642,14 +728,15 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             krange(t, a.p[t.phase], kb0, nk);
             for (int kb = 0; kb < nk; ++kb) {
                 int okw = 1;
-                if (lane == 0) okw = wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err);
+                if (lane == 0)
+                    okw = wait_bounded(smem_u32(&f8full[f]), fph, abort_flag, a.err) &&
+                          wait_bounded(smem_u32(&bempty[bb]), bph ^ 1u, abort_flag, a.err);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) {
                     ok = false;
                     break;
                 }
-                uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
-                const uint8_t *src = st + C::kABytes + C::kBBytes;
-                uint8_t *dst = st + C::kABytes;
+                const uint8_t *src = b8ring + (size_t)f * C::kB8Bytes;
+                uint8_t *dst = bbuf + (size_t)bb * C::kBBytes;
 #pragma unroll
                 for (int c = q0; c < C::kB8Bytes / 16; c += 32 * C::kConvWarps) {
                     const int r = c >> 2, c8 = c & 3;
@@ -662,10 +749,17 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // st.shared -> MMA reads
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&conv[stage]));
-                if (++stage == C::kStages) {
-                    stage = 0;
-                    phase ^= 1u;
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&f8empty[f]));   // the FP8 slot has been read
+                    mbar_arrive(smem_u32(&conv[bb]));
+                }
+                if (++f == C::kB8Stages) {
+                    f = 0;
+                    fph ^= 1u;
+                }
+                if (++bb == C::kBBufs) {
+                    bb = 0;
+                    bph ^= 1u;
                 }
             }
         }
