@@ -144,7 +144,7 @@ cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const voi
 // With row_token/row_gate (token choice, k == 1, no shared experts) the combine is
 // folded into the epilogue: Y is the layer output y[T][d] and row r is written to
 // y[row_token[r]] scaled by row_gate[row_token[r]]; rows of dropped tokens are
-// not written (the caller zeroes y first).
+// not written (the caller zeroes them: moe_forward's dispatch gather does).
 cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
                                     const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s,
                                     const int32_t *row_token = nullptr, const float *row_gate = nullptr);
