@@ -28,11 +28,11 @@
  *     from moe_workspace_size for the same stage).
  *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream).  No call synchronises the host, so a sequence of
- *     calls can be captured in a CUDA graph.  Inside a call, every kernel after
- *     the first is a programmatic dependent launch: it may start its setup while
- *     its predecessor finishes, and it waits for that kernel on the device before
- *     touching memory.  The first kernel of a call is an ordinary launch, so the
- *     usual stream order holds against the caller's own work.
+ *     calls can be captured in a CUDA graph.  The kernels are programmatic
+ *     dependent launches: one may start its setup while the previous kernel on
+ *     the stream finishes, but it waits on the device for that kernel to complete
+ *     before touching memory, so stream order holds against the caller's own work
+ *     as well.
  *   - Arguments are checked before anything is launched.  A rejected call returns
  *     a non-zero moe_status and has no side effect.
  *   - Row-major layouts.  Device buffers must be 16-byte aligned; `ws` and the

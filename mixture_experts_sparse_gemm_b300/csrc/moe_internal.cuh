@@ -179,9 +179,10 @@ int num_sms();
 moe_status device_ready(unsigned **err_word);
 
 // ----------------------------------------------------------------------------- dependent launches
-// Kernels after the first of a library call are launched with programmatic stream
-// serialisation: such a grid may start while its predecessor on the stream is
-// still running, once every CTA of the predecessor has executed pdl_trigger() (or
+// The hot kernels (tensor-core GEMMs, split-K select, dispatch plan, gather,
+// combine) are launched with programmatic stream serialisation: such a grid may
+// start while its predecessor on the stream -- ours or the caller's -- is still
+// running, once every CTA of the predecessor has executed pdl_trigger() (or
 // exited).  Each of these kernels calls pdl_wait() -- which returns when the
 // predecessor grid has completed and its memory writes are visible -- before its
 // first access to global memory; only shared-memory and TMEM setup come earlier.
