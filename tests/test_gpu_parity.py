@@ -590,6 +590,29 @@ def test_forward_back_to_back(name, cuda_device):
     _check_device_error()
     for i, y in enumerate(outs):
         assert torch.equal(y, ref[i % len(xs)]), f"forward {i} differs from its isolated run"
+    # inputs uploaded from pinned host memory on a side stream, the forward ordered
+    # after the upload by an event (the end-to-end loop of bench.py), double-buffered
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    hosts = [x.cpu().pin_memory() for x in xs]
+    bufs = [torch.empty_like(inp["x"]) for _ in range(2)]
+    done = [None, None]
+    outs = []
+    for i in range(2 * len(xs)):
+        b = i & 1
+        with torch.cuda.stream(side):
+            if done[b] is not None:
+                side.wait_event(done[b])              # the forward two steps back has read bufs[b]
+            bufs[b].copy_(hosts[i % len(xs)], non_blocking=True)
+            up = torch.cuda.Event()
+            up.record(side)
+        main.wait_event(up)
+        outs.append(layer.forward(bufs[b], *args, out=_nan_out(layer)))
+        done[b] = torch.cuda.Event()
+        done[b].record(main)
+    _check_device_error()
+    for i, y in enumerate(outs):
+        assert torch.equal(y, ref[i % len(xs)]), f"uploaded forward {i} differs from its isolated run"
 
 
 def test_forward_empty_batch(cuda_device):
