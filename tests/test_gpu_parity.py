@@ -501,6 +501,11 @@ E2E_SMALL = {
                                                                   name="small_switch_drops"),
     "small_ec": EC_CASES["ec_small"],
     "small_fp32_shared": WORKLOADS["tiny_top2_fp32"].with_(T=100, n_shared=2, f_shared=64, name="small_fp32_sh"),
+    # degenerate layers: k = E (the full softmax mixture), E = 1 (a dense SwiGLU FFN;
+    # the router is a transposed copy since E is not a multiple of 8), one token
+    "small_k_eq_E": WORKLOADS["mixtral_T256"].with_(T=200, d=256, E=4, k=4, f=128, name="small_k_eq_E"),
+    "small_dense_E1": WORKLOADS["mixtral_T256"].with_(T=130, d=256, E=1, k=1, f=256, name="small_dense_E1"),
+    "small_one_token": WORKLOADS["mixtral_T16"].with_(T=1, d=256, f=128, name="small_one_token"),
 }
 
 
