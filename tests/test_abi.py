@@ -130,3 +130,40 @@ def test_valid_call_without_gpu_reports_cuda_error():
     A = 0x10000
     st = B.lib().moe_combine(ctypes.byref(cfg), A, A, A, A, None, 0, None)
     assert st == B.MOE_ERR_CUDA
+
+
+# Kernels each call launches (moe_launch_count; bench.py's gpu_launches is K times the
+# forward count), per stage: route, dispatch, grouped FFN, combine, forward.
+#   route:    tensor-core router GEMM (W_r read in place) = 1; with fewer than 74 token
+#             tiles and a long d, split-K GEMM + select = 2; Expert Choice adds the
+#             column select; E not a multiple of 8 adds the W_r transpose; fp32: 1
+#   dispatch: single-CTA plan + gather = 2 (at most 32768 assignments), else count,
+#             scan, rank + gather = 4; Expert Choice: slots + gather = 2
+#   FFN:      one fused tensor-core launch; fp32: up + down = 2
+#   forward:  the stages, without the combine when it is folded into the down
+#             epilogue (one expert per token, no shared experts)
+LAUNCHES = {
+    "tiny_top2_fp32": [1, 2, 2, 1, 6],
+    "switch_top1_cap1.25": [1, 2, 1, 1, 4],
+    "mixtral_T16": [2, 2, 1, 1, 6],
+    "mixtral_T4096": [2, 2, 1, 1, 6],
+    "mixtral_T16384": [1, 2, 1, 1, 5],
+    "deepseek_v3": [2, 2, 1, 1, 6],
+    "expert_choice_zipf": [2, 2, 1, 1, 6],
+}
+LAUNCH_EXTRA = {
+    "transposed_router": (WORKLOADS["mixtral_T256"].with_(T=500, d=256, E=12, f=128, name="e12"), [2, 2, 1, 1, 6]),
+    "multi_cta_dispatch": (WORKLOADS["mixtral_T256"].with_(T=20000, d=256, E=16, f=128, name="n40000"),
+                           [1, 4, 1, 1, 7]),
+}
+
+
+@pytest.mark.parametrize("name", list(LAUNCHES) + list(LAUNCH_EXTRA))
+def test_launch_counts(name):
+    wl, want = (WORKLOADS[name], LAUNCHES[name]) if name in LAUNCHES else LAUNCH_EXTRA[name]
+    cfg = B.config_from_workload(wl)
+    got = [B.moe_launch_count(cfg, s) for s in (B.MOE_STAGE_ROUTE, B.MOE_STAGE_DISPATCH, B.MOE_STAGE_GROUPED_FFN,
+                                                 B.MOE_STAGE_COMBINE, B.MOE_STAGE_FORWARD)]
+    assert got == want
+    empty = B.config_from_workload(wl, T=0)
+    assert B.moe_launch_count(empty, B.MOE_STAGE_FORWARD) == 0
