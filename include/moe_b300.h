@@ -27,8 +27,9 @@
  *     library allocates nothing.  Scratch comes from `ws` (`ws_bytes` long, size
  *     from moe_workspace_size for the same stage).
  *   - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream).  No call synchronises the host, so a sequence of
- *     calls can be captured in a CUDA graph.  The kernels are programmatic
+ *     legacy default stream).  No call synchronises the host except
+ *     moe_check_device_error, which waits for its stream, so a sequence of the
+ *     other calls can be captured in a CUDA graph.  The kernels are programmatic
  *     dependent launches: one may start its setup while the previous kernel on
  *     the stream finishes, but it waits on the device for that kernel to complete
  *     before touching memory, so stream order holds against the caller's own work
