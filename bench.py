@@ -62,6 +62,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def layer_config(wl, ws_n):
+    """The layer both arms run (the `config` of the JSON line, before measured keys)."""
+    return {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "d_ff": wl.f, "k": wl.k, "gate": wl.gate,
+            "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
+            "n_shared": wl.n_shared, "f_shared": wl.f_shared,
+            "expert_weights": "e4m3 + fp32 scale per output channel" if wl.dtype == "fp8w" else wl.dtype,
+            "drop_policy": wl.drop_policy,
+            "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"}
+
+
 def kernel_hash(stage):
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[stage]:
@@ -499,15 +509,10 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": {"bf16": "bf16", "f32": "f32", "fp8w": "bf16 (E4M3 expert weights)"}[wl.dtype],
         "data": "synthetic (seeded; random-init expert weights)",
-        "config": {"workload": wl.name, "T": T, "d": d, "E": wl.E, "d_ff": wl.f, "k": wl.k, "gate": wl.gate,
-                   "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
-                   "n_shared": wl.n_shared, "f_shared": wl.f_shared,
-                   "expert_weights": "e4m3 + fp32 scale per output channel" if wl.dtype == "fp8w" else wl.dtype,
-                   "drop_policy": wl.drop_policy,
+        "config": {**layer_config(wl, ws_n),
                    "assignments_computed": A, "experts_touched": touched,
                    "l2": "inputs larger than L2: the expert weights read per step exceed 126 MB"
-                         if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2",
-                   "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"},
+                         if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2"},
         "grouped_gemm": {"tflops": round(gemm_tflops, 2),
                          "pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
                          "bf16_peak_tflops": peaks["bf16_tflops"], "flops_per_step": gemm_flops},
@@ -621,7 +626,7 @@ def run_reference(args):
     return {"metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(1e3 * float(np.mean(wall)), 2), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "d_ff": wl.f, "k": wl.k},
+            "config": layer_config(wl, ws_n),
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                              "sample": sample},
