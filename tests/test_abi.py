@@ -65,6 +65,17 @@ def test_workload_configs_are_valid(name):
     (dict(mode="ec", ec_capacity=8, gate="sigmoid"), B.MOE_ERR_UNSUPPORTED),
     (dict(n_shared=1, f_shared=0), B.MOE_ERR_INVALID_ARG),
     (dict(n_shared=1, f_shared=96), B.MOE_ERR_UNSUPPORTED),
+    # FP8 expert weights: 256-wide tiles in both GEMMs
+    (dict(dtype="fp8w", d=384), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="fp8w", f=64), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="fp8w", n_shared=1, f_shared=64), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="f32", d=96), B.MOE_ERR_UNSUPPORTED),
+    # accepted: the smallest shapes of each mode, an empty batch, the affinity drop
+    (dict(dtype="fp8w", d=256, f=128, n_shared=1, f_shared=128), B.MOE_OK),
+    (dict(dtype="f32", d=64, f=64), B.MOE_OK),
+    (dict(d=128, f=64), B.MOE_OK),
+    (dict(T=0), B.MOE_OK),
+    (dict(capacity_factor=1.0, drop_policy="affinity"), B.MOE_OK),
 ])
 def test_config_rejections(kw, want):
     base = dict(T=64, d=256, E=8, f=128, k=2)
