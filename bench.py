@@ -7,12 +7,18 @@ moe_forward call through the C ABI.  The headline value times K such steps; a
 second loop runs the same layer as separate stage calls with CUDA events
 between them for the per-kernel breakdown and roofline; a third runs
 moe_forward end to end from pinned host buffers.
-Default workload: Switch-style top-1 with capacity factor 1.25, bf16,
-T=8192, d=1024, E=64, d_ff=4096 (its 1.61 GB of expert weights stream through
-HBM every step, so the per-step working set is larger than the 126 MB L2).
+Default workload: the Mixtral-shaped layer at prefill size, bf16, T=16384,
+d=4096, E=8, d_ff=14336, top-2 softmax renormalised, per-expert logit offsets
+(the largest configuration, where the grouped expert GEMM is bound by the tensor
+cores; its 2.8 GB of expert weights and 0.4 GB of tokens exceed the 126 MB L2).
+After the headline, every other workload is measured once the same way and
+reported under "per_config" (tokens/s, layer-roofline fraction, grouped-GEMM
+TFLOP/s, per-stage device time and GB/s, SM clock).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
     python bench.py --impl reference ...     # the CPU oracle on the same workload
+    python bench.py --stage S --workload W   # one stage alone (route | dispatch |
+                                             # ffn | combine), e.g. under ncu
 
 Prints one JSON line (rank 0).  With N > 1 (torchrun), every rank runs its own
 replica on its own batch (no data exchange; the layer is replicated, tokens are
@@ -40,9 +46,12 @@ if ROOT not in sys.path:
 from workloads import WORKLOADS, make_inputs  # noqa: E402
 
 METRIC = "MoE-layer fwd tokens/s; grouped-GEMM TFLOP/s as % of B300 bf16 peak"
-DEFAULT_WORKLOAD = "switch_top1_cap1.25"
+DEFAULT_WORKLOAD = "mixtral_T16384"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 STAGES = ("route", "dispatch", "ffn", "combine")
+# workloads of the per_config table (the headline's own is skipped there)
+PER_CONFIG = ("tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T16", "mixtral_T256", "mixtral_T4096",
+              "mixtral_T16384", "deepseek_v3", "expert_choice_zipf")
 KERNEL_SOURCES = {   # files whose content defines each stage's kernels (for the ncu traffic record)
     "ffn": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
     "route": ["csrc/route.cu", "csrc/route_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
@@ -97,14 +106,16 @@ def recorded_traffic(stage, workload):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background."""
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms in the background;
+    window(t_lo, t_hi) summarises the samples inside one timed region."""
     FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self):
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        self.t0 = time.time()
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu=timestamp,{self.FIELDS}",
                                        "--format=csv,noheader,nounits", "-lms", "200"],
@@ -112,38 +123,60 @@ class ClockSampler:
         except OSError:
             self.p = None
 
-    def stop(self, bus_id, t_lo, t_hi):
-        if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.p.terminate()
-        try:
-            self.p.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.p.kill()
+    def _rows(self):
         self.f.flush()
-        rows, window = [], []
+        rows = []
         with open(self.f.name) as fh:
             for line in fh:
                 c = [x.strip() for x in line.split(",")]
                 if len(c) < 11:
                     continue
-                if bus_id and bus_id.lower() not in c[2].lower():
+                if self.bus_id and self.bus_id.lower() not in c[2].lower():
                     continue
-                rows.append(c)
                 try:
                     ts = datetime.datetime.strptime(c[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
                 except ValueError:
                     continue
-                if t_lo - 0.25 <= ts <= t_hi + 0.25:
-                    window.append(c)
-        os.unlink(self.f.name)
-        rows = window if window else rows   # samples inside the timed region when there are any
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        sm = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        mx = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[7 + i].lower() == "active"})
+                rows.append((ts, c))
+        return rows
+
+    def window(self, t_lo, t_hi):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = self._rows()
+        win = [c for ts, c in rows if t_lo - 0.25 <= ts <= t_hi + 0.25]
+        if not win:   # a region shorter than the sampling period: the nearest sample
+            near = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t_lo + t_hi)))[:1]
+            win = [c for _, c in near]
+        sm = [float(r[3]) for r in win if r[3].replace(".", "").isdigit()]
+        mx = [float(r[4]) for r in win if r[4].replace(".", "").isdigit()]
+        pw = [float(r[5]) for r in win if r[5].replace(".", "").isdigit()]
+        reasons = sorted({self.REASONS[i] for r in win for i in range(4) if r[7 + i].lower() == "active"})
         return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(win)}
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def close(self):
+        self.stop()
+        try:
+            os.unlink(self.f.name)
+        except OSError:
+            pass
+
+
+def pci_bus(dev):
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+        return f"{bus:02x}:" if isinstance(bus, int) else None
+    except Exception:
+        return None
 
 
 def dist_env():
@@ -198,10 +231,180 @@ def work_model(wl, off, E_used):
 
 
 # ------------------------------------------------------------------------------------ our arm
+_WEIGHT_KEYS = ("W1", "W3", "W2", "W1s", "W3s", "W2s")
+
+
+class LayerRun:
+    """One layer on the device: seeded inputs, packed expert weights, the stage
+    buffers, and the C-ABI calls of one step.  keep_weights=False frees the
+    unpacked expert weights once they are packed (the layer only reads the packed
+    copy)."""
+
+    def __init__(self, wl, dev, keep_weights=False):
+        from mixture_experts_sparse_gemm_b300 import binding as B
+        from mixture_experts_sparse_gemm_b300.layer import MoELayer
+        self.B = B
+        self.wl = wl
+        self.dev = dev
+        self.stream = torch.cuda.current_stream()
+        self.inp = make_inputs(wl, dev)
+        i = self.inp
+        self.cfg = B.config_from_workload(wl)
+        self.layer = MoELayer(self.cfg, i["W1"], i["W3"], i["W2"], i.get("W1s"), i.get("W3s"), i.get("W2s"))
+        if not keep_weights:
+            for k in _WEIGHT_KEYS:
+                i.pop(k, None)
+        T, d = wl.T, wl.d
+        dt = self.layer.dtype
+        ec = wl.mode == "ec"
+        sel = (wl.E, wl.ec_capacity) if ec else (T, wl.k)
+        slots = (T, wl.E) if ec else (T, wl.k)
+        self.idx = torch.empty(sel, dtype=torch.int32, device=dev)
+        self.gw = torch.empty(sel, dtype=torch.float32, device=dev)
+        self.off = torch.empty(wl.E + 1, dtype=torch.int32, device=dev)
+        self.cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
+        self.slot_of = torch.empty(slots, dtype=torch.int32, device=dev)
+        self.x_perm = torch.empty(self.layer.rows_routed, d, dtype=dt, device=dev)
+        self.Y = torch.empty(self.layer.rows_total, d, dtype=dt, device=dev)
+        self.y = torch.empty(T, d, dtype=dt, device=dev)
+        self.ws = {s: self.layer.workspace(s) for s in (B.MOE_STAGE_ROUTE, B.MOE_STAGE_DISPATCH,
+                                                      B.MOE_STAGE_GROUPED_FFN, B.MOE_STAGE_FORWARD)}
+
+    @property
+    def x(self):
+        return self.inp["x"]
+
+    def forward(self, s=None, x=None, y=None):
+        i, B = self.inp, self.B
+        B.moe_forward(self.cfg, self.x if x is None else x, i["W_r"], i["logit_offset"], i["sel_bias"],
+                      self.layer.packed, self.y if y is None else y, self.ws[B.MOE_STAGE_FORWARD],
+                      self.stream if s is None else s)
+
+    def stage_calls(self):
+        """The four stage calls of one step, each taking the stream to enqueue on."""
+        i, B, c = self.inp, self.B, self.cfg
+        return {
+            "route": lambda s: B.moe_route(c, self.x, i["W_r"], i["logit_offset"], i["sel_bias"], self.idx, self.gw,
+                                           self.ws[B.MOE_STAGE_ROUTE], s),
+            "dispatch": lambda s: B.moe_dispatch(c, self.idx, self.x, self.off, self.cnt, self.slot_of, self.x_perm,
+                                                 self.ws[B.MOE_STAGE_DISPATCH], s, self.gw),
+            "ffn": lambda s: B.moe_grouped_ffn(c, self.x_perm, self.off, self.layer.packed, self.x, self.Y,
+                                               self.ws[B.MOE_STAGE_GROUPED_FFN], s),
+            "combine": lambda s: B.moe_combine(c, self.Y, self.slot_of, self.gw, self.y, None, s),
+        }
+
+    def staged_step(self, ev=None):
+        """One step as the four stage calls, an event before and after each when given."""
+        calls = self.stage_calls()
+        for j, name in enumerate(STAGES):
+            if ev is not None:
+                ev[j].record(self.stream)
+            calls[name](self.stream)
+        if ev is not None:
+            ev[len(STAGES)].record(self.stream)
+
+    def work(self):
+        """Work model of the step the stage buffers hold (after a staged step)."""
+        offs = self.off.cpu().numpy()
+        return work_model(self.wl, offs, int((np.diff(offs) > 0).sum()))
+
+
+def time_calls(fn, n, stream):
+    """Device milliseconds of n calls of fn() on `stream` (CUDA events, synchronised)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def graph_call_us(fn_s, stream, n_cap=10, budget_s=0.2, max_reps=50):
+    """Device microseconds per call of fn_s(stream): n_cap back-to-back calls
+    captured in a CUDA graph on a side stream and replayed (no host launch gaps;
+    the inputs of a stage stay where the previous call left them, in L2 when they
+    fit)."""
+    cs = torch.cuda.Stream()
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(n_cap):
+            fn_s(cs)
+    with torch.cuda.stream(cs):
+        g.replay()
+        one = time_calls(g.replay, 1, cs)
+        reps = int(max(1, min(max_reps, budget_s * 1e3 / max(one, 1e-3))))
+        ms = time_calls(g.replay, reps, cs)
+    del g
+    return ms / (reps * n_cap) * 1e3
+
+
+def stage_table(stage_s, model, peaks):
+    """Per-stage achieved GB/s and TFLOP/s and the fraction of the stage's bound
+    (HBM copy bandwidth, or for a compute-bound expert stage the bf16 peak)."""
+    bw = peaks["hbm_gbs"]
+    out = {}
+    for s in STAGES:
+        t = stage_s[s]
+        gbs = model[s]["bytes"] / t / 1e9
+        tfl = model[s]["flops"] / t / 1e12
+        t_mem = model[s]["bytes"] / (bw * 1e9)
+        t_cmp = model[s]["flops"] / (peaks["bf16_tflops"] * 1e12)
+        bound = "tensor" if (s == "ffn" and t_cmp > t_mem) else "hbm"
+        out[s] = {"us": round(t * 1e6, 2), "GB/s": round(gbs, 1), "TFLOP/s": round(tfl, 2), "bound": bound,
+                  "frac": round(gbs / bw if bound == "hbm" else tfl / peaks["bf16_tflops"], 4)}
+    return out
+
+
+def layer_roofline_ms(model, peaks):
+    layer_bytes = sum(model[s]["bytes"] for s in STAGES)
+    flops = model["ffn"]["flops"]
+    return max(flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3, layer_bytes
+
+
+def measure_config(wl, dev, peaks, clocks):
+    """One workload measured on its own: moe_forward timed over ~0.4 s of steps,
+    then each stage replayed from a CUDA graph.  Returns the per_config entry."""
+    run = LayerRun(wl, dev)
+    B, st = run.B, run.stream
+    for _ in range(3):
+        run.forward()
+    run.staged_step()
+    est = time_calls(run.forward, 3, st) / 3
+    K = int(min(2000, max(10, 400.0 / max(est, 1e-3))))
+    t_lo = time.time()
+    ms = time_calls(run.forward, K, st)
+    t_hi = time.time()
+    clk = clocks.window(t_lo, t_hi)
+    B.moe_check_device_error(st)
+    calls = run.stage_calls()
+    stage_us = {s: graph_call_us(calls[s], st) for s in STAGES}
+    B.moe_check_device_error(st)
+    model, A, touched = run.work()
+    step_ms = ms / K
+    roof_ms, layer_bytes = layer_roofline_ms(model, peaks)
+    ffn_s = stage_us["ffn"] * 1e-6
+    gemm_tf = model["ffn"]["flops"] / ffn_s / 1e12
+    entry = {
+        "T": wl.T, "steps": K, "ms_per_step": round(step_ms, 5), "tokens_per_s": round(wl.T / (step_ms * 1e-3), 1),
+        "assignments_computed": A, "experts_touched": touched,
+        "layer_roofline": {"ms": round(roof_ms, 5), "frac": round(roof_ms / step_ms, 4)},
+        "grouped_gemm": {"tflops": round(gemm_tf, 2), "pct_bf16_peak": round(100 * gemm_tf / peaks["bf16_tflops"], 2)},
+        "stage_device": stage_table({s: stage_us[s] * 1e-6 for s in STAGES}, model, peaks),
+        "sm_mhz": clk["sm_mhz"], "clock_reasons": clk["reasons"],
+        "ms_x_mhz": round(step_ms * clk["sm_mhz"], 1) if clk["sm_mhz"] else None,
+        "launches_per_step": B.moe_launch_count(run.cfg, B.MOE_STAGE_FORWARD),
+    }
+    del run, calls
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_gpu(args):
     from mixture_experts_sparse_gemm_b300 import binding as B
     from mixture_experts_sparse_gemm_b300 import build as build_mod
-    from mixture_experts_sparse_gemm_b300.layer import MoELayer
 
     ws_n, rank, local = dist_env()
     if ws_n > 1:
@@ -224,44 +427,12 @@ def run_gpu(args):
         wl = wl.with_(drop_policy="affinity")
     if ws_n > 1:   # each replica gets its own batch of tokens
         wl = wl.with_(index=wl.index + 1000 * rank) if rank else wl
-    inp = make_inputs(wl, dev)
-    cfg = B.config_from_workload(wl)
-    layer = MoELayer(cfg, inp["W1"], inp["W3"], inp["W2"], inp.get("W1s"), inp.get("W3s"), inp.get("W2s"))
-    stream = torch.cuda.current_stream()
+    want_cpu = rank == 0 and ws_n == 1 and not args.no_cpu_baseline
+    run = LayerRun(wl, dev, keep_weights=want_cpu)
+    stream = run.stream
     T, d = wl.T, wl.d
-    dt = layer.dtype
-    rows_routed, rows_total = layer.rows_routed, layer.rows_total
-    ec = wl.mode == "ec"
-    sel = (wl.E, wl.ec_capacity) if ec else (T, wl.k)
-    slots = (T, wl.E) if ec else (T, wl.k)
-    idx = torch.empty(sel, dtype=torch.int32, device=dev)
-    gw = torch.empty(sel, dtype=torch.float32, device=dev)
-    off = torch.empty(wl.E + 1, dtype=torch.int32, device=dev)
-    cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
-    slot_of = torch.empty(slots, dtype=torch.int32, device=dev)
-    x_perm = torch.empty(rows_routed, d, dtype=dt, device=dev)
-    Y = torch.empty(rows_total, d, dtype=dt, device=dev)
-    y = torch.empty(T, d, dtype=dt, device=dev)
-    ws_route = layer.workspace(B.MOE_STAGE_ROUTE)
-    ws_disp = layer.workspace(B.MOE_STAGE_DISPATCH)
-    ws_ffn = layer.workspace(B.MOE_STAGE_GROUPED_FFN)
-    x, Wr, lo, sb = inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream)
-        if ev is not None:
-            ev[1].record(stream)
-        B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream, gw)
-        if ev is not None:
-            ev[2].record(stream)
-        B.moe_grouped_ffn(cfg, x_perm, off, layer.packed, x, Y, ws_ffn, stream)
-        if ev is not None:
-            ev[3].record(stream)
-        B.moe_combine(cfg, Y, slot_of, gw, y, None, stream)
-        if ev is not None:
-            ev[4].record(stream)
+    peaks, peak_src = load_peaks()
+    clocks = ClockSampler(pci_bus(dev))
 
     def barrier():
         if ws_n > 1:
@@ -272,49 +443,34 @@ def run_gpu(args):
 
     # ---- headline timed region: K layer forwards through moe_forward, inputs resident
     K = args.steps
-    fw_ws = layer.workspace()
-    clocks = ClockSampler()
     for _ in range(args.warmup):
-        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
-        step()
+        run.forward()
+        run.staged_step()
     torch.cuda.synchronize()
     B.moe_check_device_error(stream)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    torch.cuda.synchronize()
     t_lo = time.time()
-    e0.record(stream)
-    for _ in range(K):
-        B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, stream)
-    e1.record(stream)
-    torch.cuda.synchronize()
+    total_ms = slowest(time_calls(run.forward, K, stream))
     t_hi = time.time()
     barrier()
-    total_ms = slowest(e0.elapsed_time(e1))
+    clk = clocks.window(t_lo, t_hi)
     B.moe_check_device_error(stream)
 
     # ---- the same forward captured once in a CUDA graph and replayed K times (the
     # library never synchronises the host, so a serving loop can capture it): the
     # kernels are the same, only the launch overhead between them differs
-    graph = None
     try:
         cap_s = torch.cuda.Stream()
-        cap_s.wait_stream(torch.cuda.current_stream())
+        cap_s.wait_stream(stream)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap_s):
-            B.moe_forward(cfg, x, Wr, lo, sb, layer.packed, y, fw_ws, cap_s)
+            run.forward(cap_s)
         torch.cuda.synchronize()
         with torch.cuda.stream(cap_s):
             for _ in range(max(3, args.warmup)):
                 g.replay()
-            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            g0.record(cap_s)
-            for _ in range(K):
-                g.replay()
-            g1.record(cap_s)
-        torch.cuda.synchronize()
+            g_ms = slowest(time_calls(g.replay, K, cap_s))
         B.moe_check_device_error(stream)
-        g_ms = slowest(g0.elapsed_time(g1))
         graph = {"ms_per_step": round(g_ms / K, 5), "value": round(replica_throughput(ws_n, T, K, g_ms), 1),
                  "unit": "tokens/s"}
         del g
@@ -326,78 +482,45 @@ def run_gpu(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(K)]
     torch.cuda.synchronize()
     for i in range(K):
-        step(evs[i])
+        run.staged_step(evs[i])
     torch.cuda.synchronize()
-    t_hi2 = time.time()
     staged_ms = evs[0][0].elapsed_time(evs[K - 1][len(STAGES)]) / K
-    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)])) for j, s in enumerate(STAGES)}
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(dev).pci_bus_id
-        bus = f"{bus:02x}:" if isinstance(bus, int) else None
-    except Exception:
-        bus = None
-    clk = clocks.stop(bus, t_lo, t_hi2)
+    stage_ms = {s: float(np.mean([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)]))
+                for j, s in enumerate(STAGES)}
     B.moe_check_device_error(stream)
+    model, A, touched = run.work()
 
-    # ---- per-stage device time without host launch gaps: n_cap back-to-back calls of
-    # one stage captured in a CUDA graph and replayed (the stage loop above pays a
-    # launch gap at every event; here the inputs of route / dispatch / combine stay in
-    # L2 from one call to the next, unlike in the forward)
-    stage_dev_us = {}
+    # ---- per-stage device time without host launch gaps (graph replay of each stage)
     try:
-        n_cap = 10
-        reps = max(1, min(K, 200) // n_cap)
-        calls = {
-            "route": lambda s_: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, s_),
-            "dispatch": lambda s_: B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, s_, gw),
-            "ffn": lambda s_: B.moe_grouped_ffn(cfg, x_perm, off, layer.packed, x, Y, ws_ffn, s_),
-            "combine": lambda s_: B.moe_combine(cfg, Y, slot_of, gw, y, None, s_),
-        }
-        for name, fn in calls.items():
-            cs = torch.cuda.Stream()
-            cs.wait_stream(stream)
-            gs = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gs, stream=cs):
-                for _ in range(n_cap):
-                    fn(cs)
-            with torch.cuda.stream(cs):
-                gs.replay()
-                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a0.record(cs)
-                for _ in range(reps):
-                    gs.replay()
-                a1.record(cs)
-            torch.cuda.synchronize()
-            stage_dev_us[name] = a0.elapsed_time(a1) / (reps * n_cap) * 1e3
-            del gs
+        calls = run.stage_calls()
+        stage_dev_us = {s: graph_call_us(calls[s], stream) for s in STAGES}
         B.moe_check_device_error(stream)
+        stage_device = stage_table({s: stage_dev_us[s] * 1e-6 for s in STAGES}, model, peaks)
+        stage_device["method"] = ("10 back-to-back calls of the stage replayed from a CUDA graph; "
+                                  "route/dispatch/combine inputs L2-warm between calls")
     except Exception as ex:   # capture unsupported here: report why
-        stage_dev_us = {"unavailable": str(ex).splitlines()[0][:200]}
+        stage_device = {"unavailable": str(ex).splitlines()[0][:200]}
 
     # ---- load statistics (outside the timed regions): the router with its score sums,
     # and the statistics kernel, each averaged over a short loop of its own
-    psum = torch.empty(wl.E, dtype=torch.float32, device=dev)
-    frac = torch.empty(wl.E, dtype=torch.float32, device=dev)
-    pmean = torch.empty(wl.E, dtype=torch.float32, device=dev)
+    E = wl.E
+    psum = torch.empty(E, dtype=torch.float32, device=dev)
+    frac = torch.empty(E, dtype=torch.float32, device=dev)
+    pmean = torch.empty(E, dtype=torch.float32, device=dev)
     summary = torch.empty(5, dtype=torch.float64, device=dev)
-    n_ls = 20
+    i_, ws_r = run.inp, run.ws[B.MOE_STAGE_ROUTE]
 
-    def timed(fn):
-        for _ in range(3):
-            fn()
-        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(n_ls):
-            fn()
-        a1.record(stream)
-        torch.cuda.synchronize()
-        return a0.elapsed_time(a1) / n_ls
+    def route(prob_sum=None):
+        B.moe_route(run.cfg, run.x, i_["W_r"], i_["logit_offset"], i_["sel_bias"], run.idx, run.gw, ws_r, stream,
+                    prob_sum)
 
-    route_plain_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream))
-    route_probs_ms = timed(lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_route, stream, psum))
-    B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_disp, stream, gw)
-    stats_ms = timed(lambda: B.moe_load_stats(cfg, idx, cnt, psum, frac, pmean, summary, stream))
+    for _ in range(3):
+        route(psum)
+    route_plain_ms = time_calls(route, 20, stream) / 20
+    route_probs_ms = time_calls(lambda: route(psum), 20, stream) / 20
+    run.stage_calls()["dispatch"](stream)
+    stats_ms = time_calls(lambda: B.moe_load_stats(run.cfg, run.idx, run.cnt, psum, frac, pmean, summary, stream),
+                          20, stream) / 20
     B.moe_check_device_error(stream)
     load_stats = {"route_ms": round(route_plain_ms, 5), "route_with_prob_sum_ms": round(route_probs_ms, 5),
                   "stats_kernel_ms": round(stats_ms, 5),
@@ -409,10 +532,11 @@ def run_gpu(args):
     # tokens host -> device, runs moe_forward and copies its output device -> host.  The
     # copies of neighbouring steps overlap the compute on their own streams (double
     # buffers), as a serving loop would run it.
-    x_host = [x.cpu().pin_memory(), x.cpu().pin_memory()]
+    dt = run.layer.dtype
+    x_host = [run.x.cpu().pin_memory(), run.x.cpu().pin_memory()]
     y_host = [torch.empty(T, d, dtype=dt).pin_memory() for _ in range(2)]
-    x_dev = [torch.empty_like(x) for _ in range(2)]
-    y_dev = [torch.empty_like(y) for _ in range(2)]
+    x_dev = [torch.empty_like(run.x) for _ in range(2)]
+    y_dev = [torch.empty_like(run.y) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
@@ -429,7 +553,7 @@ def run_gpu(args):
             stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])             # step i-2's output has left y_dev[b]
-            B.moe_forward(cfg, x_dev[b], Wr, lo, sb, layer.packed, y_dev[b], fw_ws, stream)
+            run.forward(x=x_dev[b], y=y_dev[b])
             ev_done[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev_done[b])
@@ -439,6 +563,7 @@ def run_gpu(args):
     e2e_steps(args.warmup)
     barrier()
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s_in)
     e2e_steps(K)
     e1.record(s_out)
@@ -446,56 +571,41 @@ def run_gpu(args):
     barrier()
     e2e_ms = slowest(e0.elapsed_time(e1))
     B.moe_check_device_error(stream)
+    del x_host, y_host, x_dev, y_dev
 
-    # ---- work model and roofline
-    peaks, peak_src = load_peaks()
-    offs = off.cpu().numpy()
-    model, A, touched = work_model(wl, offs, int((np.diff(offs) > 0).sum()))
-    bw = peaks["hbm_gbs"]
-    stage_info = {}
+    # ---- work model and roofline of the dominant kernel
+    stage_info = stage_table({s: stage_ms[s] * 1e-3 for s in STAGES}, model, peaks)
     for s in STAGES:
-        t_s = stage_ms[s] * 1e-3
-        gbs = model[s]["bytes"] / t_s / 1e9
-        tfl = model[s]["flops"] / t_s / 1e12
-        t_mem = model[s]["bytes"] / (bw * 1e9)
-        t_cmp = model[s]["flops"] / (peaks["bf16_tflops_sustained"] * 1e12)
-        bound = "tensor" if (s.startswith("ffn") and t_cmp > t_mem) else "hbm"
-        stage_info[s] = {"ms": round(stage_ms[s], 5), "GB/s": round(gbs, 1), "TFLOP/s": round(tfl, 2),
-                         "bound": bound,
-                         "frac": round(gbs / bw if bound == "hbm" else tfl / peaks["bf16_tflops_sustained"], 4)}
-    stage_device = {}
-    if "unavailable" in stage_dev_us:
-        stage_device = stage_dev_us
-    else:
-        for s in STAGES:
-            t_s = stage_dev_us[s] * 1e-6
-            gbs = model[s]["bytes"] / t_s / 1e9
-            stage_device[s] = {"us": round(stage_dev_us[s], 2), "GB/s": round(gbs, 1), "frac": round(gbs / bw, 4)}
-        stage_device["method"] = ("10 back-to-back calls of the stage replayed from a CUDA graph; "
-                                  "route/dispatch/combine inputs L2-warm between calls")
+        stage_info[s]["ms"] = round(stage_ms[s], 5)
     dom = max(STAGES, key=lambda s: stage_ms[s])
     di = stage_info[dom]
     if di["bound"] == "hbm":
-        roof = {"bound": "hbm", "achieved": di["GB/s"], "peak": bw, "unit": "GB/s",
-                "frac": round(di["GB/s"] / bw, 4)}
+        bw = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": di["GB/s"], "peak": bw, "unit": "GB/s", "frac": round(di["GB/s"] / bw, 4)}
+        peak_kind = "copy bandwidth"
     else:
-        p = peaks["bf16_tflops_sustained"]
+        # the denominator matching the clock the kernel ran at: the burst bf16 figure
+        # when the timed region held the maximum SM clock, the power-capped sustained
+        # figure when the clock sat lower
+        capped = clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"]
+        key = "bf16_tflops_sustained" if capped else "bf16_tflops"
+        p = peaks[key]
         roof = {"bound": "tensor", "achieved": di["TFLOP/s"], "peak": p, "unit": "TFLOP/s",
                 "frac": round(di["TFLOP/s"] / p, 4)}
+        peak_kind = ("sustained bf16 (timed region under the power cap)" if capped
+                     else "burst bf16 (timed region at the maximum SM clock)")
     roof["kernel"] = dom
-    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'}), "
+                           f"{peak_kind}")
     roof["traffic"] = recorded_traffic(dom, wl.name)
     roof["algorithmic_bytes_per_launch"] = model[dom]["bytes"]
+    roof["algorithmic_flops_per_launch"] = model[dom]["flops"]
 
     step_ms = total_ms / K
-    ffn_s = stage_ms["ffn"] * 1e-3
     gemm_flops = model["ffn"]["flops"]
-    gemm_tflops = gemm_flops / ffn_s / 1e12
-    layer_bytes = sum(model[s]["bytes"] for s in STAGES)
-    layer_flops = model["ffn"]["flops"]
-    layer_roof_ms = max(layer_flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (bw * 1e9)) * 1e3
+    gemm_tflops = gemm_flops / (stage_ms["ffn"] * 1e-3) / 1e12
+    roof_ms, layer_bytes = layer_roofline_ms(model, peaks)
     value = replica_throughput(ws_n, T, K, total_ms)
-    x_bytes = T * d * x.element_size()
     out = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -512,12 +622,12 @@ def run_gpu(args):
         "config": {**layer_config(wl, ws_n),
                    "assignments_computed": A, "experts_touched": touched,
                    "l2": "inputs larger than L2: the expert weights read per step exceed 126 MB"
-                         if touched * 3 * d * wl.f * x.element_size() > 126e6 else "working set fits L2"},
+                         if touched * 3 * d * wl.f * run.x.element_size() > 126e6 else "working set fits L2"},
         "grouped_gemm": {"tflops": round(gemm_tflops, 2),
                          "pct_bf16_peak": round(100 * gemm_tflops / peaks["bf16_tflops"], 2),
                          "bf16_peak_tflops": peaks["bf16_tflops"], "flops_per_step": gemm_flops},
-        "layer_roofline": {"ms": round(layer_roof_ms, 5), "frac": round(layer_roof_ms / step_ms, 4),
-                           "bytes_per_step": layer_bytes, "flops_per_step": layer_flops},
+        "layer_roofline": {"ms": round(roof_ms, 5), "frac": round(roof_ms / step_ms, 4),
+                           "bytes_per_step": layer_bytes, "flops_per_step": gemm_flops},
         "stages": stage_info,
         "staged_ms_per_step": round(staged_ms, 5),
         "stage_device": stage_device,
@@ -525,16 +635,118 @@ def run_gpu(args):
         "load_stats": load_stats,
         "roofline": roof,
         "e2e": {"value": round(replica_throughput(ws_n, T, K, e2e_ms), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": x_bytes, "d2h_bytes_per_step": T * d * y.element_size(),
+                "h2d_bytes_per_step": T * d * run.x.element_size(),
+                "d2h_bytes_per_step": T * d * run.y.element_size(),
                 "ms_per_step": round(e2e_ms / K, 5)},
-        "gpu_launches": K * B.moe_launch_count(cfg, B.MOE_STAGE_FORWARD),
-        "clocks": clk,
+        "gpu_launches": K * B.moe_launch_count(run.cfg, B.MOE_STAGE_FORWARD),
+        "clocks": {**clk, "ms_x_mhz": round(step_ms * clk["sm_mhz"], 1) if clk.get("sm_mhz") else None},
     }
-    if rank == 0 and ws_n == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens)
+    inp = run.inp
+    del run
+    torch.cuda.empty_cache()
+    if want_cpu:
+        out["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_tokens, args.cpu_budget)
+    del inp
+    torch.cuda.empty_cache()
+
+    # ---- every other workload, measured once the same way (single GPU only)
+    if ws_n == 1 and not args.no_per_config:
+        per = {}
+        for name in PER_CONFIG:
+            if name == wl.name:
+                continue
+            try:
+                per[name] = measure_config(WORKLOADS[name], dev, peaks, clocks)
+            except Exception as ex:   # report, keep the headline
+                per[name] = {"error": str(ex).splitlines()[0][:200]}
+                torch.cuda.empty_cache()
+        out["per_config"] = {"method": "moe_forward timed over about 0.4 s of steps (CUDA events); stages from "
+                                       "CUDA-graph replays of 10 calls; fractions of MEASURED_PEAKS.json "
+                                       "(burst bf16, copy bandwidth); sm_mhz = median nvidia-smi SM clock "
+                                       "during the forward loop", **per}
+    clocks.close()
     if ws_n > 1:
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+# ------------------------------------------------------------------------------------ one stage alone
+def run_stage(args):
+    """One stage of the layer called --steps times after --warmup calls, with only
+    the buffers it needs on the device (the small captures of ncu).  Prints the
+    stage's device time per call and its achieved bandwidth against the work model."""
+    from mixture_experts_sparse_gemm_b300 import binding as B
+    from mixture_experts_sparse_gemm_b300 import build as build_mod
+    from mixture_experts_sparse_gemm_b300.layer import MoELayer
+    build_mod.build()
+    B.lib()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = WORKLOADS[args.workload]
+    if args.T:
+        wl = wl.with_(T=args.T)
+    S = args.stage
+    st = torch.cuda.current_stream()
+    cfg = B.config_from_workload(wl)
+    need_w = S == "ffn"
+    inp = make_inputs(wl, dev, weights=need_w)
+    layer = None
+    if need_w:
+        layer = MoELayer(cfg, inp["W1"], inp["W3"], inp["W2"], inp.get("W1s"), inp.get("W3s"), inp.get("W2s"))
+        for k in _WEIGHT_KEYS:
+            inp.pop(k, None)
+        torch.cuda.empty_cache()
+
+    def ws(stage):
+        n = B.moe_workspace_size(cfg, stage)
+        return torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
+
+    ec = wl.mode == "ec"
+    sel = (wl.E, wl.ec_capacity) if ec else (wl.T, wl.k)
+    idx = torch.empty(sel, dtype=torch.int32, device=dev)
+    gw = torch.empty(sel, dtype=torch.float32, device=dev)
+    ws_r = ws(B.MOE_STAGE_ROUTE)
+    x, Wr, lo, sb = inp["x"], inp["W_r"], inp["logit_offset"], inp["sel_bias"]
+    B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_r, st)
+    rows_routed, rows_total = B.moe_buffer_rows(cfg)
+    off = torch.zeros(wl.E + 1, dtype=torch.int32, device=dev)
+    fn = lambda: B.moe_route(cfg, x, Wr, lo, sb, idx, gw, ws_r, st)   # noqa: E731
+    if S != "route":
+        cnt = torch.empty(wl.E, dtype=torch.int32, device=dev)
+        slot_of = torch.empty((wl.T, wl.E) if ec else (wl.T, wl.k), dtype=torch.int32, device=dev)
+        x_perm = torch.empty(rows_routed, wl.d, dtype=x.dtype, device=dev)
+        ws_d = ws(B.MOE_STAGE_DISPATCH)
+        B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_d, st, gw)
+        fn = lambda: B.moe_dispatch(cfg, idx, x, off, cnt, slot_of, x_perm, ws_d, st, gw)   # noqa: E731
+        if S == "ffn":
+            Y = torch.empty(rows_total, wl.d, dtype=x.dtype, device=dev)
+            ws_f = ws(B.MOE_STAGE_GROUPED_FFN)
+            fn = lambda: B.moe_grouped_ffn(cfg, x_perm, off, layer.packed, x, Y, ws_f, st)   # noqa: E731
+        elif S == "combine":
+            # the combine's input rows: seeded values in the expert outputs' place
+            # (the stage's traffic and time do not depend on them)
+            Y = torch.empty(rows_total, wl.d, dtype=x.dtype, device=dev).normal_()
+            y = torch.empty(wl.T, wl.d, dtype=x.dtype, device=dev)
+            fn = lambda: B.moe_combine(cfg, Y, slot_of, gw, y, None, st)   # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    B.moe_check_device_error(st)
+    ms = time_calls(fn, args.steps, st)
+    B.moe_check_device_error(st)
+    offs = off.cpu().numpy()
+    model, A, touched = work_model(wl, offs, int((np.diff(offs) > 0).sum()))
+    peaks, peak_src = load_peaks()
+    t = ms * 1e-3 / args.steps
+    m = model[S]
+    return {"stage": S, "workload": wl.name, "calls": args.steps, "us_per_call": round(t * 1e6, 3),
+            "launches_per_call": B.moe_launch_count(cfg, {"route": B.MOE_STAGE_ROUTE, "dispatch": B.MOE_STAGE_DISPATCH,
+                                                          "ffn": B.MOE_STAGE_GROUPED_FFN,
+                                                          "combine": B.MOE_STAGE_COMBINE}[S]),
+            "algorithmic_bytes": m["bytes"], "algorithmic_flops": m["flops"],
+            "GB/s": round(m["bytes"] / t / 1e9, 1), "frac_hbm": round(m["bytes"] / t / 1e9 / peaks["hbm_gbs"], 4),
+            "TFLOP/s": round(m["flops"] / t / 1e12, 2),
+            "frac_bf16_burst": round(m["flops"] / t / 1e12 / peaks["bf16_tflops"], 4),
+            "peaks": f"{peak_src}", "note": "back-to-back calls on one stream; inputs stay in L2 when they fit"}
 
 
 # ------------------------------------------------------------------------------------ oracle arms
@@ -588,12 +800,17 @@ def _sample_text(wl, n):
             f"the capacity dispatch of the batch, their experts + combine; tokens/s = sample tokens / step time")
 
 
-def cpu_baseline(wl, inp, n_tokens):
+def cpu_baseline(wl, inp, max_tokens, budget_s):
+    """The oracle, as it stands, on 1 host thread, on a seeded token sample of the
+    same batch sized to about budget_s seconds (at most max_tokens tokens)."""
     import oracle
     oracle.build()
     h = _oracle_host_inputs(wl, inp)
     st = _oracle_setup(oracle, wl, h)
-    toks = _sample_tokens(wl, n_tokens)
+    probe = _sample_tokens(wl, 2, seed=1)
+    per_tok = _oracle_step(oracle, wl, h, st, probe) / len(probe)
+    n = int(max(4, min(max_tokens, budget_s / max(per_tok, 1e-9))))
+    toks = _sample_tokens(wl, n)
     dt = _oracle_step(oracle, wl, h, st, toks)
     return {"value": round(len(toks) / dt, 2), "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": _sample_text(wl, len(toks)) + f" ({dt:.1f} s)", "host_cpus": os.cpu_count()}
@@ -636,12 +853,16 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--T", type=int, default=0, help="override the token count")
-    ap.add_argument("--cpu-tokens", type=int, default=768, help="oracle sample for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=768, help="largest oracle sample for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds the cpu_baseline sample aims to take")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per_config table of the other workloads")
+    ap.add_argument("--stage", choices=list(STAGES), default=None,
+                    help="time one stage alone (only its buffers on the device) and print its line")
     ap.add_argument("--ref-tokens", type=int, default=256, help="largest oracle sample per reference step")
     ap.add_argument("--ref-budget", type=float, default=120.0, help="seconds the reference arm aims to take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -652,7 +873,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    out = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if args.stage:
+        out = run_stage(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

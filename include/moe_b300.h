@@ -46,6 +46,10 @@
  *     Scores and gate weights are always fp32; indices are int32.
  *   - Device-side waits are bounded.  A wait that gives up sets a device error
  *     word; moe_check_device_error reports it as MOE_ERR_TIMEOUT.
+ *   - On first use of a device the library looks up, and keeps, the device
+ *     addresses of its own device variables (the error word; the scratch array of
+ *     moe_dispatch_noalloc).  Do not use the library on a device after a
+ *     cudaDeviceReset of that device in the same process.
  */
 #ifndef MOE_B300_H
 #define MOE_B300_H
@@ -296,6 +300,34 @@ moe_status moe_load_stats(const moe_config *cfg, const int32_t *topk_idx, const 
 /* Number of CUDA kernels one call of `stage` enqueues for this configuration
  * (memsets not counted; MOE_STAGE_FORWARD: the whole layer).  No CUDA call. */
 moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *kernels);
+
+/*
+ * Limit of every bounded device-side wait of the tensor-core kernels, in
+ * nanoseconds: a pipeline stage, an accumulator, or (fused expert launch) the up
+ * tiles that produce a down tile's rows.  A wait that reaches the limit gives up:
+ * the kernel records the timeout in the device error word, drains the copies and
+ * MMAs it has issued, frees its tensor memory and ends, so the context stays
+ * usable, and moe_check_device_error reports MOE_ERR_TIMEOUT.  The limit is
+ * process-wide and read when a call launches its kernels.  0 restores the
+ * default of 2 s; values outside [1e3, 6e10] return MOE_ERR_INVALID_ARG.  A limit
+ * shorter than the longest legitimate wait (a down tile waits for its up tiles,
+ * milliseconds on large layers) makes correct calls report timeouts.  No CUDA call.
+ */
+moe_status moe_set_wait_limit_ns(uint64_t limit_ns);
+moe_status moe_get_wait_limit_ns(uint64_t *limit_ns);
+
+/*
+ * Probe of the failure path of the bounded waits (the pages define no failure
+ * behaviour; this is a diagnostic of the library).  Launches one small kernel on
+ * `stream` that runs the two wait routines of the tensor-core kernels with the
+ * current limit: first until the device int32 *flag reaches `target` (read with
+ * acquire semantics; the caller owns the flag and decides whether anything sets
+ * it), then on a shared-memory barrier that completes only if the first wait
+ * succeeded.  With the condition met both waits succeed and nothing is recorded;
+ * otherwise each gives up after the limit (about twice the limit in all) and the
+ * next moe_check_device_error returns MOE_ERR_TIMEOUT.
+ */
+moe_status moe_wait_probe(const int32_t *flag, int32_t target, void *stream);
 
 /*
  * Waits for `stream`, then reads and clears the device error word.  Returns

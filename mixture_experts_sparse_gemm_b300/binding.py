@@ -25,7 +25,8 @@ MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, M
 EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "moe_buffer_rows",
            "moe_workspace_size", "moe_packed_weights_size", "moe_pack_weights", "moe_route", "moe_dispatch",
            "moe_grouped_ffn", "moe_grouped_ffn_up", "moe_grouped_ffn_down", "moe_combine", "moe_forward",
-           "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc", "moe_load_stats")
+           "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc", "moe_load_stats",
+           "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_wait_probe")
 MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS = 65536
 
 
@@ -75,6 +76,9 @@ def lib():
             "moe_check_device_error": [vp],
             "moe_dispatch_noalloc": [cfgp, vp, vp, vp, vp, vp, vp, vp],
             "moe_load_stats": [cfgp, vp, vp, vp, vp, vp, vp, vp],
+            "moe_set_wait_limit_ns": [ctypes.c_uint64],
+            "moe_get_wait_limit_ns": [ctypes.POINTER(ctypes.c_uint64)],
+            "moe_wait_probe": [vp, ctypes.c_int32, vp],
         }
         for name, args in sigs.items():
             fn = getattr(L, name)
@@ -222,6 +226,20 @@ def moe_combine(cfg, Y, slot_of, topk_w, y, ws=None, stream=None):
 def moe_forward(cfg, x, W_r, logit_offset, sel_bias, packed, y, ws, stream=None):
     _check(lib().moe_forward(ctypes.byref(cfg), _p(x), _p(W_r), _p(logit_offset), _p(sel_bias), _p(packed), _p(y),
                              _p(ws), _nbytes(ws), _stream(stream)), "moe_forward")
+
+
+def moe_set_wait_limit_ns(limit_ns: int):
+    _check(lib().moe_set_wait_limit_ns(int(limit_ns)), "moe_set_wait_limit_ns")
+
+
+def moe_get_wait_limit_ns() -> int:
+    v = ctypes.c_uint64()
+    _check(lib().moe_get_wait_limit_ns(ctypes.byref(v)), "moe_get_wait_limit_ns")
+    return int(v.value)
+
+
+def moe_wait_probe(flag, target=1, stream=None):
+    _check(lib().moe_wait_probe(_p(flag), int(target), _stream(stream)), "moe_wait_probe")
 
 
 def moe_check_device_error(stream=None):

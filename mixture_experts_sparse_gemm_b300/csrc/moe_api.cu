@@ -1,6 +1,7 @@
 // C ABI of the MoE layer: argument checks, workspace carving and the launch
 // sequence route -> dispatch -> grouped experts -> combine.  Every argument check
 // runs before any CUDA call, so a rejected call touches no device state.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -15,6 +16,10 @@ __device__ unsigned g_moe_error_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kMinWaitNs = 1000ull;             // 1 us
+constexpr uint64_t kMaxWaitNs = 60000000000ull;      // 60 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
 int g_sm_count[kMaxDevices];
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 sm_103, -1 other
 unsigned *g_err_ptr[kMaxDevices];
@@ -260,6 +265,8 @@ PackedLayout packed_layout(const moe_config &c) {
 }
 
 moe_status device_ready(unsigned **err_word) { return device_setup(err_word); }
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 int num_sms() {
     int dev = 0;
@@ -622,6 +629,28 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, co
     st = do_ffn(c, x_perm, off, packed, x, Y, w + L.ffn, err, s);
     if (st != MOE_OK) return st;
     return from_cuda(launch_combine(c, sizes_of(c), Y, slot_of, gw, y, s));
+}
+
+moe_status moe_set_wait_limit_ns(uint64_t limit_ns) {
+    if (limit_ns == 0) limit_ns = kDefaultWaitNs;
+    if (limit_ns < kMinWaitNs || limit_ns > kMaxWaitNs) return MOE_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+moe_status moe_get_wait_limit_ns(uint64_t *limit_ns) {
+    if (!limit_ns) return MOE_ERR_INVALID_ARG;
+    *limit_ns = wait_limit_ns();
+    return MOE_OK;
+}
+
+moe_status moe_wait_probe(const int32_t *flag, int32_t target, void *stream) {
+    MOE_REQUIRE(flag, MOE_ERR_INVALID_ARG);
+    MOE_REQUIRE(aligned4(flag), MOE_ERR_MISALIGNED);
+    unsigned *err = nullptr;
+    moe_status st = device_setup(&err);
+    if (st != MOE_OK) return st;
+    return from_cuda(launch_wait_probe(flag, target, wait_limit_ns(), err, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_check_device_error(void *stream) {

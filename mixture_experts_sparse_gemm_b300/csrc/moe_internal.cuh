@@ -177,6 +177,11 @@ int route_tcgen05_launches(const moe_config &c);
 int num_sms();
 // architecture check and device error word of the current device (set up once per device)
 moe_status device_ready(unsigned **err_word);
+// limit of the bounded device-side waits (process-wide; moe_set_wait_limit_ns)
+uint64_t wait_limit_ns();
+// one CTA that runs the two bounded-wait routines of the tensor-core kernels (see
+// moe_wait_probe); sets kErrWaitTimeout in *err when they give up
+cudaError_t launch_wait_probe(const int32_t *flag, int32_t target, uint64_t limit_ns, unsigned *err, cudaStream_t s);
 
 // ----------------------------------------------------------------------------- dependent launches
 // The hot kernels (tensor-core GEMMs, split-K select, dispatch plan, gather,

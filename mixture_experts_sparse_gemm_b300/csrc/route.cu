@@ -119,6 +119,22 @@ __device__ __forceinline__ void warp_score_select(const RouteArgs &a, const floa
                 bp = op;
             }
         }
+        if (bi == 0x7fffffff) {
+            // no unchosen key compares above -FLT_MAX (NaN scores from non-finite
+            // inputs): take the lowest unchosen expert, so every index stays in range
+            int low = 0x7fffffff;
+#pragma unroll
+            for (int i = kPerLane - 1; i >= 0; --i)
+                if (lane + 32 * i < E && !(chosen >> i & 1u)) low = lane + 32 * i;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) low = min(low, __shfl_xor_sync(0xffffffffu, low, o));
+            bi = low;
+            bp = 0.f;
+#pragma unroll
+            for (int i = 0; i < kPerLane; ++i)
+                if (lane + 32 * i == bi) bp = p[i];
+            bp = __shfl_sync(0xffffffffu, bp, bi & 31);   // the owner's score (not finite here)
+        }
         if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
         wsum += bp;
         if (lane == j) {

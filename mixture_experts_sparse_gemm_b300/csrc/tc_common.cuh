@@ -11,9 +11,12 @@
 namespace moe {
 namespace tc {
 
-// Every wait on an mbarrier is bounded: after this long the waiting role records
-// kErrWaitTimeout in the device error word, raises the CTA's abort flag and leaves.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Every wait on an mbarrier or on another CTA's progress is bounded: after the
+// launch's wait limit (TcArgs::wait_ns; moe_set_wait_limit_ns, 2 s by default) the
+// waiting role records kErrWaitTimeout in the device error word, raises the CTA's
+// abort flag and leaves.  Draining the copies and MMAs already issued, on the way
+// out, is bounded by a fixed limit of its own (those always complete).
+constexpr uint64_t kDrainLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -54,16 +57,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of parity `parity` to complete.  Returns false when the CTA
-// aborts (another role gave up) or when this wait itself times out.
+// aborts (another role gave up) or when this wait itself gives up after
+// `limit_ns` (then it records the timeout and raises the abort flag).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             unsigned *err) {
+                                             unsigned *err, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) {
+            if (globaltimer() - t0 > limit_ns) {
+                atomicOr(err, kErrWaitTimeout);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Wait until the global counter *cnt (written by other CTAs with release
+// semantics) reaches `need`, reading it with acquire semantics.  Same contract as
+// wait_bounded.
+__device__ __forceinline__ bool wait_counter_bounded(const int *cnt, int need, volatile int *abort_flag,
+                                                     unsigned *err, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= need) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > limit_ns) {
                 atomicOr(err, kErrWaitTimeout);
                 *abort_flag = 1;
                 return false;

@@ -123,6 +123,7 @@ struct TcArgs {
     const float *row_gate;
     RouteEpi route;
     unsigned *err;
+    uint64_t wait_ns;     // limit of every bounded wait (set by launch_gemm)
 };
 
 // SiLU(z) = z / (1 + e^-z) with the fast exponential and division (the result is
@@ -262,6 +263,25 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
     }
     if (!valid) return;
     const int k = r.k;
+    if (ti[k - 1] == 0x7fffffff) {
+        // fewer than k keys compared above -FLT_MAX (NaN scores from non-finite
+        // inputs): fill the empty slots with the lowest experts not chosen, so every
+        // index stays in range
+        int e = 0;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (j < k && ti[j] == 0x7fffffff) {
+                for (;; ++e) {
+                    bool used = false;
+#pragma unroll
+                    for (int q = 0; q < KMAX; ++q) used |= (q < k && ti[q] == e);
+                    if (!used) break;
+                }
+                ti[j] = e;
+                tu[j] = 0.f;
+            }
+        }
+    }
     float p[KMAX], wsum = 0.f;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
@@ -514,20 +534,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     // H rows of this (segment, M tile) come from the up tiles: wait until all
                     // of them have published (release/acquire through dep), bounded
                     const int need = routed ? a.p[0].g.nblk_routed : a.p[0].g.nblk_shared;
-                    const int *cnt = a.dep + mtile_start[t.s] + t.mb;
-                    const uint64_t t0 = globaltimer();
-                    for (uint32_t i = 0;; ++i) {
-                        int v;
-                        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-                        if (v >= need) break;
-                        if ((i & 15u) == 0 && (*abort_flag || globaltimer() - t0 > kWaitLimitNs)) {
-                            if (!*abort_flag) atomicOr(a.err, kErrWaitTimeout);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
-                        }
+                    if (!wait_counter_bounded(a.dep + mtile_start[t.s] + t.mb, need, abort_flag, a.err, a.wait_ns)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
                     asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes -> TMA reads
                 }
                 const CUtensorMap *mA = (t.phase == 0) ? (routed ? &tmA0 : &tmA1) : (routed ? &tmA2 : &tmA3);
@@ -548,7 +558,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                          (size_t)sub * kBCopy;
                 }
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err)) {
+                    if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     }
                     const uint32_t fb = smem_u32(&full[st]);
                     const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(fb, ph) && globaltimer() - t0 < kWaitLimitNs) {
+                    while (!mbar_try_wait(fb, ph) && globaltimer() - t0 < kDrainLimitNs) {
                     }
                 }
             }
@@ -607,19 +617,19 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                 krange(t, G, kb0, nk);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-                if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err)) {
+                if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
                     ok = false;
                     break;
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err)) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
                     }
                     if constexpr (W8) {
-                        if (!wait_bounded(smem_u32(&conv[bb]), bph, abort_flag, a.err)) {
+                        if (!wait_bounded(smem_u32(&conv[bb]), bph, abort_flag, a.err, a.wait_ns)) {
                             ok = false;
                             break;
                         }
@@ -656,7 +666,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             // every MMA issued has finished before TMEM is released
             mma_commit(smem_u32(drain));
             const uint64_t t0 = globaltimer();
-            while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kDrainLimitNs) {
             }
         }
     } else if (W8 && warp == C::kB8Warp) {
@@ -680,7 +690,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                 const uint8_t *bt = (routed ? G.Bt0 + (size_t)t.s * G.bt_seg0 : G.Bt1) + (size_t)img * nk * img_bytes +
                                     (size_t)sub * C::kB8Bytes;
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bounded(smem_u32(&f8empty[f]), fph ^ 1u, abort_flag, a.err)) {
+                    if (!wait_bounded(smem_u32(&f8empty[f]), fph ^ 1u, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -704,7 +714,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                         fph ^= 1u;
                     }
                     const uint64_t t0 = globaltimer();
-                    while (!mbar_try_wait(smem_u32(&f8full[f]), fph) && globaltimer() - t0 < kWaitLimitNs) {
+                    while (!mbar_try_wait(smem_u32(&f8full[f]), fph) && globaltimer() - t0 < kDrainLimitNs) {
                     }
                 }
             }
@@ -729,8 +739,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             for (int kb = 0; kb < nk; ++kb) {
                 int okw = 1;
                 if (lane == 0)
-                    okw = wait_bounded(smem_u32(&f8full[f]), fph, abort_flag, a.err) &&
-                          wait_bounded(smem_u32(&bempty[bb]), bph ^ 1u, abort_flag, a.err);
+                    okw = wait_bounded(smem_u32(&f8full[f]), fph, abort_flag, a.err, a.wait_ns) &&
+                          wait_bounded(smem_u32(&bempty[bb]), bph ^ 1u, abort_flag, a.err, a.wait_ns);
                 if (!__shfl_sync(0xffffffffu, okw, 0)) {
                     ok = false;
                     break;
@@ -774,7 +784,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             const int acc = it & 1;
             const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
             int ok = 1;
-            if (lane == 0) ok = wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, a.err);
+            if (lane == 0) ok = wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, a.err, a.wait_ns);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             fence_after();
@@ -827,7 +837,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                 // the phase of tempty[acc] completes once all four epilogue warps have
                 // stored their rows (this warp cannot fall a phase behind: the next one
                 // needs its own arrival), then a GPU-scope release of the counter
-                if (wait_bounded(smem_u32(&tempty[acc]), acc_phase, abort_flag, a.err)) {
+                if (wait_bounded(smem_u32(&tempty[acc]), acc_phase, abort_flag, a.err, a.wait_ns)) {
                     __threadfence();
                     asm volatile("fence.proxy.async.global;" ::: "memory");
                     int *cnt = a.dep + mtile_start[t.s] + t.mb;
@@ -857,10 +867,12 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
 // access, so the launch is a dependent one and its setup overlaps that kernel.
 template <int BN, int EPI, bool W8 = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args, int64_t max_tiles,
+                        const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args_in, int64_t max_tiles,
                         cudaStream_t s) {
     auto kern = tc_grouped_gemm_kernel<BN, EPI, W8>;
     constexpr int kBlock = TcCfg<BN, W8>::kThreadsCta;
+    TcArgs args = args_in;
+    args.wait_ns = wait_limit_ns();
     const size_t smem = TcCfg<BN, W8>::kSmem;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;

@@ -178,3 +178,23 @@ def test_launch_counts(name):
     assert got == want
     empty = B.config_from_workload(wl, T=0)
     assert B.moe_launch_count(empty, B.MOE_STAGE_FORWARD) == 0
+
+
+def test_wait_limit_setting_is_host_only_and_checked():
+    build_mod.build()
+    L = B.lib()
+    default = B.moe_get_wait_limit_ns()
+    assert default == 2_000_000_000
+    try:
+        B.moe_set_wait_limit_ns(1_000_000)
+        assert B.moe_get_wait_limit_ns() == 1_000_000
+        for bad in (1, 999, 60_000_000_001):
+            assert L.moe_set_wait_limit_ns(bad) == B.MOE_ERR_INVALID_ARG
+        assert B.moe_get_wait_limit_ns() == 1_000_000   # a rejected value changes nothing
+        B.moe_set_wait_limit_ns(0)                      # 0 restores the default
+        assert B.moe_get_wait_limit_ns() == default
+    finally:
+        B.moe_set_wait_limit_ns(0)
+    assert L.moe_get_wait_limit_ns(None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_wait_probe(None, 1, None) == B.MOE_ERR_INVALID_ARG
+    assert L.moe_wait_probe(0x10002, 1, None) == B.MOE_ERR_MISALIGNED

@@ -96,6 +96,30 @@ def test_route_token_choice(name, cuda_device):
     assert np.abs(gw[keep] - ow[keep]).max() <= 2e-5
 
 
+@pytest.mark.parametrize("name", ["ragged_top2", "sigmoid_top8_splitk", "tiny_top2_fp32", "sigmoid_top8_e256"])
+def test_route_nan_token_stays_in_range(name, cuda_device):
+    """A token whose input row holds a NaN has NaN logits; its slots must still name
+    distinct experts in range (the lowest ones), and the other tokens' routing is
+    unaffected.  Covers the fused tensor-core epilogue, the split-K select and the
+    CUDA-core router."""
+    wl = _wl(name)
+    inp = make_inputs(wl, cuda_device, weights=False)
+    x = inp["x"].clone()
+    x[0, 5] = float("nan")
+    cfg = B.config_from_workload(wl)
+    ws = torch.empty(max(1, B.moe_workspace_size(cfg, B.MOE_STAGE_ROUTE)), dtype=torch.uint8, device=cuda_device)
+    idx = torch.empty(wl.T, wl.k, dtype=torch.int32, device=cuda_device)
+    w = torch.empty(wl.T, wl.k, dtype=torch.float32, device=cuda_device)
+    B.moe_route(cfg, x, inp["W_r"], inp["logit_offset"], inp["sel_bias"], idx, w, ws)
+    _check_device_error()
+    gi = _np(idx)
+    np.testing.assert_array_equal(gi[0], np.arange(wl.k))
+    oi, _, gap = oracle.route_tc(inp["x"][1:], inp["W_r"], wl.k, wl.gate, inp["logit_offset"], inp["sel_bias"],
+                                 wl.renorm, nthreads=NTH)
+    keep = gap >= GAP
+    np.testing.assert_array_equal(gi[1:][keep], oi[keep])
+
+
 EC_CASES = {
     "expert_choice_zipf": WORKLOADS["expert_choice_zipf"],
     "ec_small": WORKLOADS["expert_choice_zipf"].with_(T=1000, d=256, E=16, f=128, ec_capacity=100, name="ec_small"),
@@ -330,6 +354,62 @@ def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
         assert rel_err(Yn[T * k:], sref) <= TOL[dt]
 
 
+# The fine-grained layout at its widest: 256 routed experts plus one shared expert
+# (257 segments) with small d and f, so that every row of every segment can be
+# compared with the oracle.  The segment sizes are seeded and skewed and include
+# empty experts and sizes on both sides of the 128-row M tile.
+MANY_SEG_CASES = [
+    # d, f, f_shared: both tiles 256 wide (one fused launch with its per-M-tile
+    # counters), then 128-wide up tiles (f % 128 != 0: separate up and down launches)
+    (256, 128, 128),
+    (384, 192, 64),
+]
+
+
+@pytest.mark.parametrize("d,f,fs", MANY_SEG_CASES)
+def test_grouped_ffn_257_segments(d, f, fs, cuda_device):
+    E, k = 256, 8
+    rng = np.random.default_rng(d + f)
+    counts = rng.choice([0, 1, 2, 17, 63, 64, 65, 127, 128, 129, 200, 255, 256, 257], size=E)
+    counts[:6] = [0, 129, 1, 128, 0, 256]   # fixed edges first
+    A = int(counts.sum())
+    T = (A + k - 1) // k + 3                 # rows_routed = T * k >= A; T rows of shared input
+    cfg = B.config(T=T, d=d, E=E, f=f, k=k, n_shared=1, f_shared=fs)
+    g = torch.Generator(device="cpu").manual_seed(4242 + d)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).bfloat16()
+    Ws = [(torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, fs, d, generator=g) / fs ** 0.5).bfloat16()]
+    off = np.zeros(E + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    x_perm = torch.zeros(T * k, d, dtype=torch.bfloat16)
+    x_perm[:A] = random_rows(A, d, seed=77 + d, dtype=torch.bfloat16)
+    x = random_rows(T, d, seed=78 + d, dtype=torch.bfloat16)
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    Y = layer.grouped_ffn(x_perm.to(dev), torch.from_numpy(off).to(dev), x.to(dev))
+    _check_device_error()
+    Yn = _np(Y)
+    ref = np.zeros((A, d))
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            ref[a:b] = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
+    # every routed row, per segment (a failing segment is named), then the shared rows
+    scale = np.abs(ref).max()
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            err = np.abs(Yn[a:b] - ref[a:b]).max() / scale
+            assert err <= TOL["bf16"], f"expert {e} ({b - a} rows): {err:.3e}"
+    sref = oracle.expert_rows(x, Ws[0][0], Ws[1][0], Ws[2][0], nthreads=NTH)
+    assert rel_err(Yn[T * k:], sref) <= TOL["bf16"]
+    print(f"257 segments, {A} routed rows + {T} shared rows compared, "
+          f"max|err|/max|ref| = {rel_err(Yn[:A], ref):.3e}")
+
+
 # Segment sizes around the 128-row M tile: 1, 15, 16, 17, 111, 112, 113, 127, 128,
 # 129, 240 rows and an empty expert; the shared segment (T = 1029 rows) ends in a
 # 5-row tile.
@@ -482,15 +562,39 @@ def _sample_tokens(T, n, seed, must=()):
     return np.array(sorted(pick), np.int64)
 
 
+def _segment_tails(gi, g_slot, usable, E):
+    """For every expert with kept rows, the token of its last kept row in the GPU's
+    own routing (the row that ends its segment, in its last M tile).  A tail
+    token whose routing differs from the oracle's (a near tie) cannot be compared;
+    the expert's last usable token stands in for it.  Returns (tokens, experts
+    with rows, experts whose true tail token is compared)."""
+    T, k = gi.shape
+    kept = g_slot >= 0
+    ts = np.repeat(np.arange(T), k)[kept.ravel()]
+    es = gi.ravel()[kept.ravel()]
+    last = np.full(E, -1)
+    np.maximum.at(last, es, ts)
+    ok = usable[ts]
+    last_ok = np.full(E, -1)
+    np.maximum.at(last_ok, es[ok], ts[ok])
+    with_rows = np.nonzero(last >= 0)[0]
+    exact = int(sum(last_ok[e] == last[e] for e in with_rows))
+    toks = np.unique(last_ok[last_ok >= 0]).astype(np.int64)
+    return toks, len(with_rows), exact
+
+
+# tokens compared at full size: None = all; an int = a seeded sample of that many;
+# "tails" = the last row of every expert segment (+ a seeded sample of 24 and the
+# shared segment's last token), so each segment's tail M tile is checked
 E2E_CASES = {
-    "tiny_top2_fp32": (None, 0),
-    "switch_top1_cap1.25": (48, 0),
-    "mixtral_T16": (None, 0),
-    "mixtral_T256": (24, 0),
-    "mixtral_T4096": (16, 0),
-    "mixtral_T16384": (12, 0),
-    "deepseek_v3": (6, 0),
-    "expert_choice_zipf": (16, 0),
+    "tiny_top2_fp32": None,
+    "switch_top1_cap1.25": 48,
+    "mixtral_T16": None,
+    "mixtral_T256": 24,
+    "mixtral_T4096": 16,
+    "mixtral_T16384": 12,
+    "deepseek_v3": "tails",
+    "expert_choice_zipf": 16,
 }
 E2E_SMALL = {
     "small_top2_ragged": WORKLOADS["mixtral_T256"].with_(T=333, d=256, f=384, name="small_top2_ragged"),
@@ -542,7 +646,15 @@ def _run_e2e(wl, n_sample, cuda_device):
         g_off, g_cnt, g_slot, _ = oracle.dispatch_tc(gi, wl.E, cap)   # the GPU's own choices, dispatched
         same = (gi == oi).all(axis=1) & ((g_slot >= 0) == (o_slot >= 0)).all(axis=1)
         dropped = np.nonzero((o_slot < 0).any(axis=1))[0]
-        toks = np.arange(T) if n_sample is None else _sample_tokens(T, n_sample, T, dropped[:64])
+        if n_sample == "tails":
+            tails, n_rows, n_tail = _segment_tails(gi, g_slot, same, wl.E)
+            reached = np.unique(gi[tails][g_slot[tails] >= 0])
+            print(f"{wl.name}: {n_rows} of {wl.E} experts have rows, {len(reached)} reached by the sample; "
+                  f"the segment's last row compared for {n_tail} of them")
+            assert len(reached) == n_rows and n_tail >= 0.95 * n_rows
+            toks = _sample_tokens(T, 24, T, list(tails) + [T - 1])
+        else:
+            toks = np.arange(T) if n_sample is None else _sample_tokens(T, n_sample, T, dropped[:64])
         toks = np.array([t for t in toks if same[t]], np.int64)
         print(f"{wl.name}: {int(near.sum())} near-tie tokens, {len(dropped)} tokens with a dropped slot")
         ref = oracle.forward_tc_streamed(inp["x"], oi, ow, o_slot, inp["W1"], inp["W3"], inp["W2"], toks,
@@ -556,8 +668,7 @@ def _run_e2e(wl, n_sample, cuda_device):
 
 @pytest.mark.parametrize("name", list(E2E_CASES))
 def test_forward_full_size(name, cuda_device):
-    n, _ = E2E_CASES[name]
-    _run_e2e(WORKLOADS[name], n, cuda_device)
+    _run_e2e(WORKLOADS[name], E2E_CASES[name], cuda_device)
     torch.cuda.empty_cache()
 
 

@@ -56,11 +56,39 @@ def test_noalloc_dispatch_matches_moe_dispatch_twice(cuda_device):
         (B.config(T=4096, d=256, E=256, f=64, k=8), 0.5, 12),
         (B.config(T=4096, d=256, E=256, f=64, k=8), 0.0, 13),   # same shape again, other routing
         (B.config(T=777, d=128, E=8, f=64, k=2, capacity_factor=0.9), 1.5, 14),
+        # more than 32768 assignments: the multi-CTA count / scan / rank kernels, which
+        # keep per-chunk expert counts in the first part of the array.  8192 x 8 at
+        # E = 256 is the documented maximum and fills all of it (256 chunks x 256
+        # experts + 65536 row tokens = 131072 ints).
+        (B.config(T=8192, d=256, E=256, f=64, k=8), 0.7, 15),
+        (B.config(T=8192, d=256, E=256, f=64, k=8, capacity_factor=1.0), 1.2, 16),
+        (B.config(T=65536, d=128, E=64, f=64, k=1, capacity_factor=1.25), 1.0, 17),
+        (B.config(T=20000, d=128, E=128, f=64, k=2, capacity_factor=1.0), 0.8, 18),
+        # back to a single-CTA call after the array was filled by the larger ones
+        (B.config(T=777, d=128, E=8, f=64, k=2, capacity_factor=0.9), 1.5, 19),
     ]
     for cfg, skew, seed in cases:
         idx = random_assignment(cfg.T, cfg.E, cfg.k, seed=seed, skew=skew, device=cuda_device)
         x = random_rows(cfg.T, cfg.d, seed=seed, device=cuda_device)
-        ref, got = _dispatch_both(cfg, idx, x, cuda_device)
-        for r, g in zip(ref, got):
-            assert torch.equal(r, g)
-        assert int(got[0][-1]) > 0
+        for call in range(2):   # each case twice in a row
+            ref, got = _dispatch_both(cfg, idx, x, cuda_device)
+            for r, g in zip(ref, got):
+                assert torch.equal(r, g), (cfg.T, cfg.k, cfg.E, call)
+            assert int(got[0][-1]) > 0
+
+
+@pytest.mark.gpu
+def test_noalloc_accepts_the_documented_maximum(cuda_device):
+    build_mod.build()
+    n_max = B.MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS
+    cfg = B.config(T=n_max // 8, d=128, E=256, f=64, k=8)
+    idx = random_assignment(cfg.T, cfg.E, cfg.k, seed=20, device=cuda_device)
+    x = random_rows(cfg.T, cfg.d, seed=20, device=cuda_device)
+    off = torch.empty(cfg.E + 1, dtype=torch.int32, device=cuda_device)
+    cnt = torch.empty(cfg.E, dtype=torch.int32, device=cuda_device)
+    slot = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=cuda_device)
+    x_perm = torch.empty(cfg.T * cfg.k, cfg.d, dtype=x.dtype, device=cuda_device)
+    B.moe_dispatch_noalloc(cfg, idx, x, off, cnt, slot, x_perm)   # raises unless MOE_OK
+    torch.cuda.synchronize()
+    B.moe_check_device_error()
+    assert int(off[-1]) == n_max
