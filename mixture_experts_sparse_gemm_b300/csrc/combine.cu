@@ -5,8 +5,9 @@
 // One warp per (token, span of the row).  The warp first lists the token's
 // (row, weight) pairs in order -- slots j = 0..k-1 for token choice, experts e
 // ascending for Expert Choice -- then every lane accumulates 16-byte vectors of
-// those Y rows in fp32 (four rows in flight) and writes its part of the token's
-// output row once.  A span is the whole row unless there are fewer tokens than
+// those Y rows in fp32 -- four of its vectors of two rows in flight at once, so a
+// token with few experts still has eight loads outstanding per lane -- and writes
+// its part of the token's output row once.  A span is the whole row unless there are fewer tokens than
 // eight warps per SM; then the rows are split so that the work spreads.
 #include "moe_internal.cuh"
 
@@ -71,6 +72,8 @@ struct CombineArgs {
 };
 
 constexpr int kStepVecs = 32;   // vectors one warp step covers: one per lane
+constexpr int kCols = 4;        // vectors per lane handled together (4 x 32 x 16 bytes of a row per warp)
+constexpr int kRows = 2;        // rows loaded together
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
@@ -104,29 +107,44 @@ __global__ void __launch_bounds__(32 * kWarps) combine_kernel(CombineArgs a) {
         __syncwarp();
         const uint4 *ys = a.shared_row0 >= 0 ? a.Y + (size_t)(a.shared_row0 + t) * a.vecs : nullptr;
         const int vend = min(a.vecs, (c + 1) * a.span);
-        for (int v = c * a.span + lane; v < vend; v += kStepVecs) {
-            float acc[Vec<T>::N];
+        // kCols vectors of the lane (32 apart) at a time; rows kRows at a time, all
+        // kRows x kCols loads in flight before they are accumulated.  Every output
+        // element still adds its rows in slot order, then the shared row.
+        for (int v0 = c * a.span + lane; v0 < vend; v0 += kStepVecs * kCols) {
+            float acc[kCols][Vec<T>::N];
 #pragma unroll
-            for (int i = 0; i < Vec<T>::N; ++i) acc[i] = 0.f;
-            int i = 0;
-            for (; i + 3 < n; i += 4) {   // four rows in flight, accumulated in slot order
-                uint4 r[4];
+            for (int u = 0; u < kCols; ++u)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) r[q] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v];
+                for (int q = 0; q < Vec<T>::N; ++q) acc[u][q] = 0.f;
+            for (int i = 0; i < n; i += kRows) {
+                uint4 r[kRows][kCols];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) accumulate<T>(acc, r[q], s_w[warp][i + q]);
+                for (int q = 0; q < kRows; ++q)
+#pragma unroll
+                    for (int u = 0; u < kCols; ++u)
+                        if (i + q < n && v0 + kStepVecs * u < vend)
+                            r[q][u] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v0 + kStepVecs * u];
+#pragma unroll
+                for (int q = 0; q < kRows; ++q)
+                    if (i + q < n) {
+                        const float w = s_w[warp][i + q];
+#pragma unroll
+                        for (int u = 0; u < kCols; ++u)
+                            if (v0 + kStepVecs * u < vend) accumulate<T>(acc[u], r[q][u], w);
+                    }
             }
-            uint4 r[4];
-            const int rem = n - i;
+            if (ys) {
+                uint4 r[kCols];
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-                if (q < rem) r[q] = a.Y[(size_t)s_row[warp][i + q] * a.vecs + v];
-            r[3] = ys ? ys[v] : make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < kCols; ++u)
+                    if (v0 + kStepVecs * u < vend) r[u] = ys[v0 + kStepVecs * u];
 #pragma unroll
-            for (int q = 0; q < 3; ++q)
-                if (q < rem) accumulate<T>(acc, r[q], s_w[warp][i + q]);
-            if (ys) accumulate<T>(acc, r[3], 1.f);
-            a.y[(size_t)t * a.vecs + v] = pack<T>(acc);
+                for (int u = 0; u < kCols; ++u)
+                    if (v0 + kStepVecs * u < vend) accumulate<T>(acc[u], r[u], 1.f);
+            }
+#pragma unroll
+            for (int u = 0; u < kCols; ++u)
+                if (v0 + kStepVecs * u < vend) a.y[(size_t)t * a.vecs + v0 + kStepVecs * u] = pack<T>(acc[u]);
         }
         __syncwarp();
     }

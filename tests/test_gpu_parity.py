@@ -192,6 +192,7 @@ DISPATCH_CASES = [
     (500, 8, 2, 1.25, 1.0, 64, "f32"),
     (6000, 32, 2, 1.25, 1.0, 128, "bf16"),   # 12000 assignments: 16 per lane in the single-CTA plan
     (16384, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 32768: the largest single-CTA plan (32 per lane)
+    (70, 8, 1, 0.5, 2.0, 128, "bf16"),       # fewer assignments than one warp's share, drops
     (16385, 8, 2, 1.0, 1.0, 128, "bf16"),    # 32770: just past it, the multi-CTA count/scan/rank path
     (40000, 16, 2, 1.1, 1.0, 128, "bf16"),   # 80000: multi-CTA
     (32768, 256, 2, 1.0, 0.3, 128, "bf16"),  # 65536: multi-CTA with E = 256
