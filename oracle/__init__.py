@@ -282,6 +282,32 @@ def expert_rows_fp8(x, q1, s1, q3, s3, q2, s2):
     return (h @ np.asarray(q2, np.float64)) * np.asarray(s2, np.float64)
 
 
+def quantize_e4m3_rows(X):
+    """Per-row (per-token) E4M3 quantisation of activations X[rows][K], as the
+    MOE_BF16_FP8UP layer defines it in fp32: s_r = amax_r / 448, code = E4M3(x / s_r)
+    (fp32 division, round to nearest even, saturate); s_r = 0 and codes 0 for an
+    all-zero row.  A row of X is a column of X^T, so this is the channel quantiser
+    applied to the transpose.  Returns (q [rows][K] as E4M3 values in fp64, s [rows] fp32)."""
+    q, s = quantize_e4m3_columns(np.asarray(X, np.float32).T)
+    return np.ascontiguousarray(q.T), s
+
+
+def expert_rows_fp8up(x, W1, W3, W2):
+    """SwiGLU expert whose up projection runs on E4M3 operands (MOE_BF16_FP8UP), in
+    fp64: every row of x quantised per row (quantize_e4m3_rows: codes qx, scale sx),
+    W1 and W3 per output column (quantize_e4m3_columns: q1, s1, q3, s3); then
+    gate = (qx q1) * sx * s1, up = (qx q3) * sx * s3, h = SiLU(gate) * up, and the
+    down projection h W2 with W2 as given -- the expert of "lnwmold.com GPT-4 MoE
+    article" §2.2 with the scales taken out of each sum."""
+    qx, sx = quantize_e4m3_rows(x)
+    (q1, s1), (q3, s3) = quantize_e4m3_columns(W1), quantize_e4m3_columns(W3)
+    sx = np.asarray(sx, np.float64)[:, None]
+    g = (qx @ q1) * sx * np.asarray(s1, np.float64)
+    u = (qx @ q3) * sx * np.asarray(s3, np.float64)
+    h = g / (1.0 + np.exp(-g)) * u
+    return h @ np.asarray(W2, np.float64)
+
+
 def load_stats(topk_idx, cnt_raw, scores, expert_choice=False):
     """Load statistics of one routing, from the definitions of "技术日报 2026-04-14"
     §4.4 (token fraction, LIF, CV, router entropy) and §4.2 (the Switch auxiliary

@@ -593,6 +593,44 @@ def test_expert_rows_fp8_equals_expert_of_dequantised_weights():
     assert np.abs(got - full).max() <= 0.2 * np.abs(full).max()
 
 
+def test_quantize_e4m3_rows_is_the_channel_quantiser_of_the_transpose():
+    rng = np.random.default_rng(8)
+    X = rng.normal(0, 1.5, (7, 40)).astype(np.float32)
+    X[4] = 0.0                                                     # an all-zero token
+    q, s = oracle.quantize_e4m3_rows(X)
+    qt, st = oracle.quantize_e4m3_columns(X.T)
+    assert np.array_equal(q, qt.T) and np.array_equal(s, st)
+    assert s[4] == 0 and not q[4].any()
+    for r in (0, 3, 6):                                            # each row's amax maps to the top code
+        assert abs(q[r, np.argmax(np.abs(X[r]))]) == 448.0
+    # a hand row: amax 7 -> scale 1/64; 3.5 -> 224 exactly; 0.05 -> 3.2 -> 3.25 (step 0.25 in [2, 4))
+    q1, s1 = oracle.quantize_e4m3_rows(np.array([[7.0, -3.5, 0.05, 0.0]], np.float32))
+    assert s1[0] == np.float32(7.0) / np.float32(448.0)
+    assert list(q1[0]) == [448.0, -224.0, 3.25, 0.0]
+
+
+def test_expert_rows_fp8up_reduces_to_the_plain_expert_when_exact():
+    # operands on the E4M3 grid times a power of two, with row / column maxima of
+    # 448 times that power: every scale is exactly the power of two and every
+    # code the grid value, so the FP8 up projection is exact
+    rng = np.random.default_rng(9)
+    grid = _e4m3_table()
+    d, f, n = 24, 16, 5
+    x = rng.choice(grid, (n, d)) * 2.0 ** -10
+    x[:, 0] = 448.0 * 2.0 ** -10
+    W1, W3 = rng.choice(grid, (d, f)) * 2.0 ** -12, rng.choice(grid, (d, f)) * 2.0 ** -12
+    W1[0], W3[1] = 448.0 * 2.0 ** -12, -448.0 * 2.0 ** -12
+    W2 = rng.normal(0, 0.2, (f, d)).astype(np.float32).astype(np.float64)   # the C expert reads fp32
+    got = oracle.expert_rows_fp8up(x, W1, W3, W2)
+    ref = oracle.expert_rows(x, W1, W3, W2)
+    assert np.abs(got - ref).max() <= 1e-12 * np.abs(ref).max()
+    # with general operands it tracks the unquantised expert to the E4M3 precision
+    x2, A1, A3 = rng.normal(0, 1, (n, d)), rng.normal(0, 0.2, (d, f)), rng.normal(0, 0.2, (d, f))
+    full = oracle.expert_rows(x2, A1, A3, W2)
+    got2 = oracle.expert_rows_fp8up(x2, A1, A3, W2)
+    assert np.abs(got2 - full).max() <= 0.25 * np.abs(full).max()
+
+
 # ------------------------------------------------------------------ affinity-ordered capacity drop
 def test_affinity_drop_hand_example():
     # expert 0 gets 4 assignments with cap 2: it keeps the two largest weights (tokens 3
