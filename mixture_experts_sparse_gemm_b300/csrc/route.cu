@@ -8,164 +8,22 @@
 //
 // route_simt_kernel: one CTA computes the logits of 32 tokens for all E experts
 // (fp32 FMA over d, x and W_r staged through shared memory), then every warp
-// scores 4 tokens and selects their top-k with warp shuffles: each lane holds the
-// keys of experts lane, lane+32, ...; k rounds of a warp arg-max on (key, -index)
-// give the slots in descending key order with ties to the lower expert index.
+// scores 4 tokens and selects their top-k: each lane holds the keys of experts
+// lane, lane+32, ...; k rounds of a warp arg-max on (key, -index) -- a warp max
+// of the keys, then a warp min of the indices holding it -- give the slots in
+// descending key order with ties to the lower expert index.
 #include <float.h>
 
-#include "moe_internal.cuh"
+#include "route_common.cuh"
 
 namespace moe {
 namespace {
 
+constexpr int kPerLane = kMaxE / 32;   // experts per lane, the most a warp holds
 constexpr int kTM = 32;    // tokens per CTA
 constexpr int kKC = 32;    // d-chunk staged per step
 constexpr int kThreads = 256;
 
-struct RouteArgs {
-    const void *x;
-    const void *Wr;
-    const float *logit_offset;
-    const float *sel_bias;
-    int T, d, E, k, gate, mode, renorm;
-    int32_t *topk_idx;
-    float *topk_w;
-    float *scores_t;   // expert choice: [E][T]
-    float *psum_rows;  // [kPsumRows][E] or null: += each block's sums of the experts' scores
-};
-
-constexpr int kPerLane = kMaxE / 32;   // experts per lane, the most a warp holds
-
-// Scores and selection of one token by one warp.  u[i] is the logit (offset
-// included) of expert lane + 32 i, -FLT_MAX past E.  Softmax (max and sum by warp
-// reduction) or sigmoid; Expert Choice writes the scores expert-major; token
-// choice takes k rounds of a warp arg-max on (key desc, index asc) over the keys
-// score + selection bias, so slots come out in descending key order with ties to
-// the lower expert index, and writes indices and (renormalised) weights.
-// With a.psum_rows, every score is also added to the lane's running sums pacc
-// (expert lane + 32 i), which the caller flushes once.
-template <int KPL>
-__device__ __forceinline__ void warp_score_select(const RouteArgs &a, const float (&u)[KPL], int t, int lane,
-                                                  float (&pacc)[KPL]) {
-    constexpr int kPerLane = KPL;
-    const int E = a.E;
-    float p[kPerLane];
-    if (a.gate == MOE_GATE_SIGMOID) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) p[i] = 1.f / (1.f + expf(-u[i]));
-    } else {
-        float mx = -FLT_MAX;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) mx = fmaxf(mx, u[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float sum = 0.f;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int e = lane + 32 * i;
-            p[i] = (e < E) ? expf(u[i] - mx) : 0.f;
-            sum += p[i];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        const float inv = 1.f / sum;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) p[i] *= inv;
-    }
-    if (a.psum_rows) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i)
-            if (lane + 32 * i < E) pacc[i] += p[i];
-    }
-
-    if (a.mode == MOE_EXPERT_CHOICE) {
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) a.scores_t[(size_t)e * a.T + t] = p[i];
-        }
-        return;
-    }
-
-    float key[kPerLane];
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = (e < E) ? p[i] + (a.sel_bias ? a.sel_bias[e] : 0.f) : -FLT_MAX;
-    }
-    unsigned chosen = 0;     // bit i: expert lane + 32 i already selected
-    float wsum = 0.f, wj = 0.f;
-    int ij = 0;
-    for (int j = 0; j < a.k; ++j) {
-        float bk = -FLT_MAX, bp = 0.f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kPerLane; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !(chosen >> i & 1u) && key[i] > bk) {   // ascending e: ties keep the lower
-                bk = key[i];
-                bi = e;
-                bp = p[i];
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            const float op = __shfl_xor_sync(0xffffffffu, bp, o);
-            if (ok > bk || (ok == bk && oi < bi)) {
-                bk = ok;
-                bi = oi;
-                bp = op;
-            }
-        }
-        if (bi == 0x7fffffff) {
-            // no unchosen key compares above -FLT_MAX (NaN scores from non-finite
-            // inputs): take the lowest unchosen expert, so every index stays in range
-            int low = 0x7fffffff;
-#pragma unroll
-            for (int i = kPerLane - 1; i >= 0; --i)
-                if (lane + 32 * i < E && !(chosen >> i & 1u)) low = lane + 32 * i;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) low = min(low, __shfl_xor_sync(0xffffffffu, low, o));
-            bi = low;
-            bp = 0.f;
-#pragma unroll
-            for (int i = 0; i < kPerLane; ++i)
-                if (lane + 32 * i == bi) bp = p[i];
-            bp = __shfl_sync(0xffffffffu, bp, bi & 31);   // the owner's score (not finite here)
-        }
-        if ((bi & 31) == lane) chosen |= 1u << (bi >> 5);
-        wsum += bp;
-        if (lane == j) {
-            ij = bi;
-            wj = bp;
-        }
-    }
-    if (lane < a.k) {
-        a.topk_idx[(size_t)t * a.k + lane] = ij;
-        a.topk_w[(size_t)t * a.k + lane] = a.renorm ? wj / wsum : wj;
-    }
-}
-
-// Adds the warps' running score sums to the block's row of psum_rows: shared-memory
-// sums per block, then one global atomic per expert.  Every thread of the block
-// calls it.
-template <int KPL>
-__device__ __forceinline__ void flush_prob_sum(const RouteArgs &a, const float (&pacc)[KPL], int lane,
-                                               float *sacc) {
-    if (!a.psum_rows) return;
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) sacc[e] = 0.f;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < a.E && pacc[i] != 0.f) atomicAdd(sacc + e, pacc[i]);
-    }
-    __syncthreads();
-    float *row = a.psum_rows + (size_t)(blockIdx.x % kPsumRows) * a.E;
-    for (int e = threadIdx.x; e < a.E; e += blockDim.x) atomicAdd(row + e, sacc[e]);
-}
 
 template <typename Tin, int NPT>
 __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
@@ -234,47 +92,6 @@ __global__ void __launch_bounds__(kThreads) route_simt_kernel(RouteArgs a) {
     }
     __shared__ float sacc[kMaxE];
     flush_prob_sum<kPerLane>(a, pacc, lane, sacc);
-}
-
-// Scoring and selection from split-K partial logits of the tensor-core router:
-// one warp per token sums partial[0..splits)[t][e] in split order, adds the logit
-// offset, and runs warp_score_select.
-// KPL = experts per lane (E <= 32 * KPL); the warps loop over tokens.
-template <int KPL>
-__global__ void __launch_bounds__(256) route_select_kernel(RouteArgs a, const float *__restrict__ partial, int splits,
-                                                           int npad) {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int nwarps = gridDim.x * (blockDim.x >> 5);
-    float pacc[KPL];
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) pacc[i] = 0.f;
-    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += nwarps) {
-        // every partial of the token is loaded before the sums (split order kept)
-        float pv[kMaxRouteSplits][KPL];
-#pragma unroll
-        for (int s = 0; s < kMaxRouteSplits; ++s)
-#pragma unroll
-            for (int i = 0; i < KPL; ++i) {
-                const int e = lane + 32 * i;
-                pv[s][i] = (s < splits && e < a.E) ? partial[((size_t)s * a.T + t) * npad + e] : 0.f;
-            }
-        float u[KPL];
-#pragma unroll
-        for (int i = 0; i < KPL; ++i) {
-            const int e = lane + 32 * i;
-            float v = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxRouteSplits; ++s)
-                if (s < splits) v += pv[s][i];
-            if (e < a.E && a.logit_offset) v += a.logit_offset[e];
-            u[i] = (e < a.E) ? v : -FLT_MAX;
-        }
-        warp_score_select<KPL>(a, u, t, lane, pacc);
-    }
-    __shared__ float sacc[kMaxE];
-    flush_prob_sum<KPL>(a, pacc, lane, sacc);
 }
 
 template <typename Tin, int NPT>
@@ -461,31 +278,6 @@ cudaError_t launch_route_simt(const moe_config &c, const void *x, const void *W_
     a.psum_rows = psum_rows;
     if (c.dtype == MOE_F32) return launch_typed<float>(a, s);
     return launch_typed<__nv_bfloat16>(a, s);
-}
-
-cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
-                                int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
-                                const float *partial, int splits, int npad, cudaStream_t s) {
-    RouteArgs a{};
-    a.logit_offset = logit_offset;
-    a.sel_bias = sel_bias;
-    a.T = c.T;
-    a.d = c.d;
-    a.E = c.E;
-    a.k = c.k;
-    a.gate = c.gate;
-    a.mode = c.mode;
-    a.renorm = c.renormalize;
-    a.topk_idx = topk_idx;
-    a.topk_w = topk_w;
-    a.scores_t = scores_t;
-    a.psum_rows = psum_rows;
-    int blocks = (c.T + 7) / 8;
-    const int cap = num_sms() * 2;   // warps loop over tokens: the body stays in the instruction cache
-    if (blocks > cap) blocks = cap;
-    auto kern = c.E <= 32 ? route_select_kernel<1> : c.E <= 64 ? route_select_kernel<2>
-              : c.E <= 128 ? route_select_kernel<4> : route_select_kernel<8>;
-    return launch_dependent(kern, dim3(blocks), dim3(256), 0, s, false, a, partial, splits, npad);
 }
 
 cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t *ec_tok, float *ec_w,

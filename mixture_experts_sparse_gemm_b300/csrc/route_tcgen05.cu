@@ -27,7 +27,8 @@ int padded_n(int E) {
 
 // K splits of the router GEMM: with few 128-token tiles (T small, d large) the
 // d-reduction is spread over up to 8 CTAs per tile so that ~all 148 SMs of a B300
-// stream x; the partial logits then go through route_select_kernel.  Fixed SM
+// stream x; the CTAs of one tile form a cluster that sums their partial logits
+// through distributed shared memory and selects in the same launch.  Fixed SM
 // count: workspace sizes are computed without a device query.
 constexpr int kRouteSms = 148;
 int route_splits(const moe_config &c) {
@@ -84,14 +85,16 @@ cudaError_t launch_route_n(int npad, const CUtensorMap &a0, const CUtensorMap &b
     }
 }
 
-cudaError_t launch_partial_n(int npad, const CUtensorMap &a0, const CUtensorMap &b0, const TcArgs &g, int64_t tiles,
-                             cudaStream_t s) {
+// split-K router in clusters of `splits` CTAs; the selecting warps hold
+// max(1, npad / 32) experts per lane
+cudaError_t launch_split_n(int npad, const CUtensorMap &a0, const CUtensorMap &b0, const TcArgs &g, int tiles,
+                           int splits, cudaStream_t s) {
     switch (npad) {
-        case 16: return launch_gemm<16, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
-        case 32: return launch_gemm<32, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
-        case 64: return launch_gemm<64, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
-        case 128: return launch_gemm<128, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
-        default: return launch_gemm<256, kEpiPartial>(a0, a0, b0, b0, g, tiles, s);
+        case 16: return launch_gemm_split_route<16, kEpiSplitRoute + 1>(a0, b0, g, tiles, splits, s);
+        case 32: return launch_gemm_split_route<32, kEpiSplitRoute + 1>(a0, b0, g, tiles, splits, s);
+        case 64: return launch_gemm_split_route<64, kEpiSplitRoute + 2>(a0, b0, g, tiles, splits, s);
+        case 128: return launch_gemm_split_route<128, kEpiSplitRoute + 4>(a0, b0, g, tiles, splits, s);
+        default: return launch_gemm_split_route<256, kEpiSplitRoute + 8>(a0, b0, g, tiles, splits, s);
     }
 }
 
@@ -99,19 +102,15 @@ cudaError_t launch_partial_n(int npad, const CUtensorMap &a0, const CUtensorMap 
 
 bool route_tcgen05_supported(const moe_config &c) { return bf16_acts(c) && c.E <= kMaxE && c.d % 64 == 0; }
 
-size_t route_tcgen05_scratch_bytes(const moe_config &c) {
-    const int s = route_splits(c);
-    return wr_t_bytes(c) + (s > 1 ? sizeof(float) * (size_t)s * c.T * route_n(c) : 0);
-}
+size_t route_tcgen05_scratch_bytes(const moe_config &c) { return wr_t_bytes(c); }
 
-int route_tcgen05_launches(const moe_config &c) { return (wr_in_place(c) ? 0 : 1) + (route_splits(c) > 1 ? 2 : 1); }
+int route_tcgen05_launches(const moe_config &c) { return (wr_in_place(c) ? 0 : 1) + 1; }
 
 cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void *W_r, const float *logit_offset,
                                  const float *sel_bias, int32_t *topk_idx, float *topk_w, float *scores_t,
                                  float *psum_rows, void *wr_t, unsigned *err, cudaStream_t s) {
     const int npad = route_n(c);
     char *scratch = static_cast<char *>(wr_t);
-    float *partial = reinterpret_cast<float *>(scratch + wr_t_bytes(c));
     const int splits = route_splits(c);
     CUtensorMap a0, b0;
     bool ok = make_tmap_bf16(&a0, x, (uint64_t)c.T, c.d, kBM);
@@ -137,15 +136,10 @@ cudaError_t launch_route_tcgen05(const moe_config &c, const void *x, const void 
     g.err = err;
     const int64_t tiles = (c.T + kBM - 1) / kBM;
     if (splits > 1) {
-        // split-K partial logits, then warp-per-token scoring and selection
+        // split-K partial logits, reduced and selected inside each token tile's cluster
         g.p[0].g.nblk_shared = splits;
         g.p[0].ksplit = splits;
-        g.p[0].C0 = partial;
-        g.p[0].ldc0 = c.T;
-        cudaError_t e = launch_partial_n(npad, a0, b0, g, tiles * splits, s);
-        if (e != cudaSuccess) return e;
-        return launch_route_select(c, logit_offset, sel_bias, topk_idx, topk_w, scores_t, psum_rows, partial, splits,
-                                   npad, s);
+        return launch_split_n(npad, a0, b0, g, (int)tiles, splits, s);
     }
     const int kmax = (c.mode == MOE_EXPERT_CHOICE || c.k <= 1) ? 1 : (c.k <= 2 ? 2 : (c.k <= 4 ? 4 : 8));
     switch (kmax) {
