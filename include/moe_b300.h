@@ -42,7 +42,11 @@
  *     dtype MOE_F32: all of those are fp32 (no TF32 anywhere);
  *     dtype MOE_BF16_FP8W: as MOE_BF16, except that moe_pack_weights stores the
  *     expert weights as FP8 E4M3 with one fp32 scale per output channel (the
- *     grouped FFN streams half the weight bytes; see moe_pack_weights).
+ *     grouped FFN streams half the weight bytes; see moe_pack_weights);
+ *     dtype MOE_BF16_FP8UP: as MOE_BF16, except that the up projection (x W1,
+ *     x W3) runs on the FP8 tensor cores: its input rows are quantised to E4M3
+ *     with one fp32 scale per token row, W1 and W3 with one scale per output
+ *     channel (see moe_pack_weights); H, W2 and Y stay bf16.
  *     Scores and gate weights are always fp32; indices are int32.
  *   - Device-side waits are bounded.  A wait that gives up sets a device error
  *     word; moe_check_device_error reports it as MOE_ERR_TIMEOUT.
@@ -73,7 +77,7 @@ typedef enum {
 
 typedef enum { MOE_GATE_SOFTMAX = 0, MOE_GATE_SIGMOID = 1 } moe_gate;
 typedef enum { MOE_TOKEN_CHOICE = 0, MOE_EXPERT_CHOICE = 1 } moe_mode;
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_BF16_FP8W = 2 } moe_dtype;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_BF16_FP8W = 2, MOE_BF16_FP8UP = 3 } moe_dtype;
 typedef enum { MOE_DROP_TOKEN_ORDER = 0, MOE_DROP_AFFINITY = 1 } moe_drop_policy;
 typedef enum {
     MOE_STAGE_ROUTE = 0,
@@ -97,14 +101,15 @@ typedef enum {
  *   ec_capacity: expert choice; tokens each expert takes (1..T).
  *   n_shared, f_shared: always-on shared experts (§3.4), each of hidden width
  *     f_shared; their outputs are added unweighted.
- *   dtype: MOE_BF16, MOE_F32 or MOE_BF16_FP8W.
+ *   dtype: MOE_BF16, MOE_F32, MOE_BF16_FP8W or MOE_BF16_FP8UP.
  *   drop_policy: token choice with a capacity limit; which assignments an
  *     expert over capacity keeps: MOE_DROP_TOKEN_ORDER the first `cap` in token
  *     order (§3.2), MOE_DROP_AFFINITY the `cap` with the largest gate weights
  *     (DeepSeek-V2, "技术日报" §5.2: tokens dropped by descending affinity).
  * Build limits: MOE_BF16 needs d % 128 == 0, f % 64 == 0, f_shared % 64 == 0;
  * MOE_F32 needs d % 64 == 0, f % 64 == 0, f_shared % 64 == 0;
- * MOE_BF16_FP8W needs d % 256 == 0, f % 128 == 0, n_shared * f_shared % 128 == 0.
+ * MOE_BF16_FP8W and MOE_BF16_FP8UP need d % 256 == 0, f % 128 == 0,
+ * n_shared * f_shared % 128 == 0.
  */
 typedef struct moe_config {
     int32_t T, d, E, f, k;
@@ -158,6 +163,14 @@ moe_status moe_packed_weights_size(const moe_config *cfg, size_t *bytes);
  *   The packed buffer is about half the bf16 one.  The grouped FFN expands the
  *   codes to bf16 in shared memory; on B300 this mode runs slower than MOE_BF16
  *   (it saves memory, not time).
+ * MOE_BF16_FP8UP (weights given in bf16): W1 and W3 are quantised as above (a
+ *   scale per hidden column of each, E4M3 codes in the operand layout of the FP8
+ *   MMA); W2 is packed in bf16 as for MOE_BF16.  At run time each row entering the
+ *   up projection (a token's x) gets the scale s = amax / 448 over its d values
+ *   and the codes E4M3(x / s) by the same rule (all-zero row: s = 0, codes 0);
+ *   the up GEMM multiplies codes by codes and scales the fp32 sums by the row and
+ *   column scales ("技术日报" §7.4 FP8 for the expert GEMMs).  The packed buffer is
+ *   two thirds of the bf16 one.
  */
 moe_status moe_pack_weights(const moe_config *cfg, const void *W1, const void *W3, const void *W2,
                             const void *W1s, const void *W3s, const void *W2s, void *packed,
@@ -249,7 +262,9 @@ moe_status moe_grouped_ffn(const moe_config *cfg, const void *x_perm, const int3
  *   shared hidden activations of x (Hs may be NULL when n_shared == 0).
  * moe_grouped_ffn_down: Y rows [0, off[E]) = H W2 of each row's expert; with shared
  *   experts rows [rows_routed, rows_routed + T) = Hs times the merged shared W2.
- * H, Hs in cfg->dtype.  Neither call needs workspace.
+ * H, Hs in cfg->dtype.  Neither call needs workspace.  MOE_BF16_FP8UP returns
+ * MOE_ERR_UNSUPPORTED (its up projection quantises rows into a workspace; use
+ * moe_grouped_ffn or moe_forward).
  */
 moe_status moe_grouped_ffn_up(const moe_config *cfg, const void *x_perm, const int32_t *off,
                               const void *packed, const void *x, void *H, void *Hs, void *stream);

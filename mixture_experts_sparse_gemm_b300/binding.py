@@ -18,7 +18,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_MISALIGNED = 0, 1, 2, 
 MOE_ERR_WORKSPACE, MOE_ERR_CUDA, MOE_ERR_TIMEOUT = 4, 5, 6
 MOE_GATE_SOFTMAX, MOE_GATE_SIGMOID = 0, 1
 MOE_TOKEN_CHOICE, MOE_EXPERT_CHOICE = 0, 1
-MOE_F32, MOE_BF16, MOE_BF16_FP8W = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_BF16_FP8W, MOE_BF16_FP8UP = 0, 1, 2, 3
 MOE_DROP_TOKEN_ORDER, MOE_DROP_AFFINITY = 0, 1
 MOE_STAGE_ROUTE, MOE_STAGE_DISPATCH, MOE_STAGE_GROUPED_FFN, MOE_STAGE_COMBINE, MOE_STAGE_FORWARD = range(5)
 
@@ -129,9 +129,10 @@ def config(T, d, E, f, k=1, gate="softmax", mode="tc", renormalize=True, capacit
                       _DTYPES[dtype], MOE_DROP_AFFINITY if drop_policy == "affinity" else MOE_DROP_TOKEN_ORDER)
 
 
-# run dtype names: "fp8w" = bf16 activations with FP8 E4M3 expert weights
+# run dtype names: "fp8w" = bf16 activations with FP8 E4M3 expert weights; "fp8up" =
+# the up projection on E4M3 activations and weights (H, W2, Y bf16)
 _DTYPES = {"f32": MOE_F32, "fp32": MOE_F32, "float32": MOE_F32, "bf16": MOE_BF16, "bfloat16": MOE_BF16,
-           "fp8w": MOE_BF16_FP8W}
+           "fp8w": MOE_BF16_FP8W, "fp8up": MOE_BF16_FP8UP}
 
 
 def config_from_workload(w, T=None) -> moe_config:

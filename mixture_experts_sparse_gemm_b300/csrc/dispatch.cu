@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(256)
             while (m) {
                 const int b = __ffs(m) - 1;
                 m &= m - 1;
-                uint4 *row = z.y + (size_t)(t0 + b) * vecs;
-                for (int v = lane; v < vecs; v += 32) row[v] = make_uint4(0, 0, 0, 0);
+                uint4 *row = z.y + (size_t)(t0 + b) * z.y_vecs;
+                for (int v = lane; v < z.y_vecs; v += 32) row[v] = make_uint4(0, 0, 0, 0);
             }
         }
         if (blockIdx.x == 0)
@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_gather(const void *x, int vecs, const int32_t *row_token, const int32_t *rows_dev,
-                          int64_t rows_host, void *x_perm, const GatherZero &z, cudaStream_t s) {
+                          int64_t rows_host, void *x_perm, const GatherZero &z_in, cudaStream_t s) {
+    GatherZero z = z_in;
+    if (z.y_vecs == 0) z.y_vecs = vecs;
     constexpr int kSpanStep = 128;   // vectors of one warp step (four per lane)
     const int64_t target = (int64_t)num_sms() * 16;   // rows split only below 16 warps per SM
     const int max_ch = (vecs + kSpanStep - 1) / kSpanStep;
@@ -366,7 +368,7 @@ size_t dispatch_tc_scratch_ints(int64_t assignments, int E) {
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s,
-                               const GatherZero &zero) {
+                               const GatherZero &zero, int row_bytes) {
     const int64_t n = (int64_t)c.T * c.k;
     if (n <= kPlanMax) {
         const int per = (int)((n + 32 * kPlanWarps - 1) / (32 * kPlanWarps));   // assignments per lane
@@ -382,15 +384,14 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
         dispatch_rank_kernel<<<blocks, 32 * kWarpsPerCta, smem, s>>>(topk_idx, n, c.k, c.E, nchunks, chunk_cnt, off,
                                                                      cap, slot_of, row_token, err);
     }
-    const int elt = c.dtype == MOE_F32 ? 4 : 2;
-    const int vecs = c.d * elt / 16;
+    const int vecs = (row_bytes ? row_bytes : c.d * (c.dtype == MOE_F32 ? 4 : 2)) / 16;
     return launch_gather(x, vecs, row_token, off + c.E, n, x_perm, zero, s);
 }
 
 cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
                                      const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                      float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
-                                     cudaStream_t s, const GatherZero &zero) {
+                                     cudaStream_t s, const GatherZero &zero, int row_bytes) {
     const int64_t n = (int64_t)c.T * c.k;
     cudaError_t ce = cudaMemsetAsync(S, 0, sizeof(float) * (size_t)c.E * c.T, s);
     if (ce == cudaSuccess) ce = cudaMemsetAsync(cnt_raw, 0, sizeof(int32_t) * c.E, s);
@@ -402,21 +403,20 @@ cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int
     ce = launch_column_select(c, S, cap, cnt_raw, kept, kept_w, s);
     if (ce != cudaSuccess) return ce;
     affinity_rows_kernel<<<c.E, 256, 0, s>>>(kept, cnt_raw, cap, topk_idx, c.k, c.E, off, slot_of, row_token);
-    const int elt = c.dtype == MOE_F32 ? 4 : 2;
-    const int vecs = c.d * elt / 16;
+    const int vecs = (row_bytes ? row_bytes : c.d * (c.dtype == MOE_F32 ? 4 : 2)) / 16;
     return launch_gather(x, vecs, row_token, off + c.E, n, x_perm, zero, s);
 }
 
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
-                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s) {
+                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s,
+                               int row_bytes) {
     const int64_t n = (int64_t)c.E * c.ec_capacity;
     cudaError_t ce = cudaMemsetAsync(slot_of, 0xff, sizeof(int32_t) * (size_t)c.T * c.E, s);
     if (ce != cudaSuccess) return ce;
     int blocks = (int)((n + 255) / 256);
     if (blocks > num_sms() * 4) blocks = num_sms() * 4;
     ec_slots_kernel<<<blocks, 256, 0, s>>>(ec_tok, c.T, c.E, c.ec_capacity, off, cnt_raw, slot_of, err);
-    const int elt = c.dtype == MOE_F32 ? 4 : 2;
-    const int vecs = c.d * elt / 16;
+    const int vecs = (row_bytes ? row_bytes : c.d * (c.dtype == MOE_F32 ? 4 : 2)) / 16;
     return launch_gather(x, vecs, ec_tok, nullptr, n, x_perm, GatherZero{}, s);
 }
 

@@ -11,6 +11,9 @@
 // FP8 weights (MOE_BF16_FP8W): the same launches with the W8 kernel, which streams
 //     E4M3 tile images, expands them to bf16 in shared memory and applies the
 //     per-column scales in the epilogue.
+// FP8 up projection (MOE_BF16_FP8UP): the fused launch with the F8A kernel; the up
+//     tiles multiply E4M3 activation rows by E4M3 W1|W3 images on kind::f8f6f4 and
+//     scale by row and column, the down tiles stay bf16.
 #include <algorithm>
 
 #include "tc_gemm.cuh"
@@ -23,28 +26,37 @@ struct FfnMaps {
 };
 
 // Up projection: A = x_perm (routed) / x (shared), B = [W1|W3] images, C = H / Hs.
+// FP8 up projection (f8 != nullptr): x_perm and x hold E4M3 codes, with the row
+// scales of f8.
 bool up_gemm(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off, const void *packed,
-             const void *x, void *H, void *Hs, TcGemm &G, FfnMaps &m) {
+             const void *x, void *H, void *Hs, TcGemm &G, FfnMaps &m, const F8Rows *f8 = nullptr) {
     const PackedLayout L = packed_layout(c);
     const char *pk = static_cast<const char *>(packed);
     const bool shared = c.n_shared > 0;
     const int fs = z.fs_tot;
     const int bn = up_tile_n(c);
     const uint64_t rr = (uint64_t)z.rows_routed;
-    bool ok = make_tmap_bf16(&m.a0, x_perm, rr, c.d, kBM);
-    ok = ok && make_tmap_bf16(&m.a1, shared ? x : x_perm, shared ? (uint64_t)c.T : rr, c.d, kBM);
+    auto tmap = f8 ? make_tmap_u8 : make_tmap_bf16;
+    bool ok = tmap(&m.a0, x_perm, rr, c.d, kBM);
+    ok = ok && tmap(&m.a1, shared ? x : x_perm, shared ? (uint64_t)c.T : rr, c.d, kBM);
     G = TcGemm{};
     G.g = GroupedShape{off, c.E, shared ? c.T : 0, 2 * c.f / bn, shared ? 2 * fs / bn : 0};
     G.K0 = c.d;
     G.K1 = c.d;
     G.b_rows0 = 2 * c.f;
-    const size_t wb = fp8_weights(c) ? 1 : 2;   // bytes per stored weight
+    const size_t wb = (fp8_weights(c) || fp8_up(c)) ? 1 : 2;   // bytes per stored weight
     G.Bt0 = reinterpret_cast<const uint8_t *>(pk + L.w13);
     G.Bt1 = reinterpret_cast<const uint8_t *>(pk + L.w13s);
     G.bt_seg0 = (size_t)2 * c.f * c.d * wb;
-    if (fp8_weights(c)) {
+    if (fp8_weights(c) || fp8_up(c)) {
         G.sc0 = reinterpret_cast<const float *>(pk + L.sc13);
         G.sc1 = reinterpret_cast<const float *>(pk + L.sc13s);
+    }
+    if (f8) {
+        G.a_f8 = 1;
+        G.rs0 = f8->rs0;
+        G.rtok0 = f8->rtok0;
+        G.rs1 = f8->rs1;
     }
     G.img_rows = bn;
     G.C0 = H;
@@ -129,10 +141,10 @@ cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const v
 cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                      const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
                                      unsigned *err, cudaStream_t s, const int32_t *row_token, const float *row_gate,
-                                     bool dep_zeroed) {
+                                     bool dep_zeroed, const F8Rows *f8) {
     TcArgs g{};
     FfnMaps mu, md;
-    if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], mu)) return cudaErrorInvalidValue;
+    if (!up_gemm(c, z, x_perm, off, packed, x, H, Hs, g.p[0], mu, f8)) return cudaErrorInvalidValue;
     if (!down_gemm(c, z, H, Hs, off, packed, Y, g.p[1], md)) return cudaErrorInvalidValue;
     g.dep = dep;
     g.err = err;
@@ -145,6 +157,7 @@ cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const 
     }
     const int64_t tiles = max_mtiles(c, z) * (g.p[0].g.nblk_routed + g.p[1].g.nblk_routed);
     if (fp8_weights(c)) return launch_gemm<256, kEpiFfn, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
+    if (f8) return launch_gemm<256, kEpiFfn, false, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
     return launch_gemm<256, kEpiFfn>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
 }
 

@@ -117,8 +117,11 @@ DispatchWs dispatch_ws(const moe_config &c) {
 // the two expert GEMMs run as one persistent launch when both use 256-wide tiles
 bool ffn_fused(const moe_config &c) { return bf16_acts(c) && ffn_fused_supported(c); }
 
+// FP8 up projection: aq / asc = E4M3 codes and scales of the x_perm rows (the
+// grouped-FFN stage quantises its input), xq / xsc = those of the T token rows (the
+// shared experts' input; in moe_forward also the rows the dispatch gathers).
 struct FfnWs {
-    size_t H, Hs, dep, total;
+    size_t H, Hs, dep, aq, asc, xq, xsc, total;
 };
 FfnWs ffn_ws(const moe_config &c) {
     const Sizes z = sizes_of(c);
@@ -127,6 +130,11 @@ FfnWs ffn_ws(const moe_config &c) {
     w.H = k.take((size_t)z.rows_routed * c.f * z.elt);
     w.Hs = k.take((size_t)(c.n_shared > 0 ? c.T : 0) * z.fs_tot * z.elt);
     w.dep = k.take(ffn_fused(c) ? sizeof(int) * ffn_dep_counters(c) : 0);
+    const bool q = fp8_up(c);
+    w.aq = k.take(q ? (size_t)z.rows_routed * c.d : 0);
+    w.asc = k.take(q ? sizeof(float) * (size_t)z.rows_routed : 0);
+    w.xq = k.take(q ? (size_t)c.T * c.d : 0);
+    w.xsc = k.take(q ? sizeof(float) * (size_t)c.T : 0);
     w.total = k.off;
     return w;
 }
@@ -176,21 +184,22 @@ moe_status do_route(const moe_config &c, const void *x, const void *W_r, const f
     return MOE_OK;
 }
 
+// row_bytes: bytes of a row of x (0: d in the activation type; E4M3 rows: d)
 moe_status do_dispatch(const moe_config &c, const int32_t *idx, const float *topk_w, const void *x, int32_t *off,
                        int32_t *cnt_raw, int32_t *slot_of, void *x_perm, char *ws, unsigned *err, cudaStream_t s,
-                       const GatherZero &zero = GatherZero{}) {
+                       const GatherZero &zero = GatherZero{}, int row_bytes = 0) {
     if (c.mode == MOE_EXPERT_CHOICE)
-        return from_cuda(launch_dispatch_ec(c, idx, x, off, cnt_raw, slot_of, x_perm, err, s));
+        return from_cuda(launch_dispatch_ec(c, idx, x, off, cnt_raw, slot_of, x_perm, err, s, row_bytes));
     const DispatchWs L = dispatch_ws(c);
     const Sizes z = sizes_of(c);
     if (affinity_drop(c))
         return from_cuda(launch_dispatch_affinity(
             c, z.cap, idx, topk_w, x, off, cnt_raw, slot_of, x_perm, reinterpret_cast<float *>(ws + L.aff_S),
             reinterpret_cast<int32_t *>(ws + L.aff_kept), reinterpret_cast<float *>(ws + L.aff_w),
-            reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero));
+            reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero, row_bytes));
     return from_cuda(launch_dispatch_tc(c, z.cap, idx, x, off, cnt_raw, slot_of, x_perm,
                                         reinterpret_cast<int32_t *>(ws + L.chunk),
-                                        reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero));
+                                        reinterpret_cast<int32_t *>(ws + L.row_token), err, s, zero, row_bytes));
 }
 
 moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, const void *packed, const void *x,
@@ -199,6 +208,19 @@ moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, c
     const Sizes z = sizes_of(c);
     void *H = ws + L.H;
     void *Hs = ws + L.Hs;
+    if (fp8_up(c)) {
+        // quantise the rows to E4M3 per row, then the fused launch on them
+        uint8_t *aq = reinterpret_cast<uint8_t *>(ws + L.aq), *xq = reinterpret_cast<uint8_t *>(ws + L.xq);
+        float *asc = reinterpret_cast<float *>(ws + L.asc), *xsc = reinterpret_cast<float *>(ws + L.xsc);
+        if (launch_quantize_rows(x_perm, z.rows_routed, c.d, aq, asc, s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (c.n_shared > 0 && launch_quantize_rows(x, c.T, c.d, xq, xsc, s) != cudaSuccess) return MOE_ERR_CUDA;
+        F8Rows f8;
+        f8.rs0 = asc;
+        f8.rs1 = xsc;
+        return from_cuda(launch_ffn_fused_tcgen05(c, z, aq, off, packed, c.n_shared > 0 ? xq : nullptr, H, Hs, Y,
+                                                  reinterpret_cast<int *>(ws + L.dep), err, s, nullptr, nullptr,
+                                                  false, &f8));
+    }
     if (ffn_fused(c))
         return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, x, H, Hs, Y,
                                                   reinterpret_cast<int *>(ws + L.dep), err, s));
@@ -211,6 +233,10 @@ moe_status do_ffn(const moe_config &c, const void *x_perm, const int32_t *off, c
 }
 
 // kernels enqueued per stage; mirrors the launch sequence of the do_* bodies above
+int ffn_launches(const moe_config &c) {
+    if (fp8_up(c)) return 1 + (c.n_shared > 0 ? 1 : 0) + 1;   // quantise x_perm (and x), fused launch
+    return ffn_fused(c) ? 1 : 2;
+}
 int route_launches(const moe_config &c) {
     const int base = (bf16_acts(c) && route_tcgen05_supported(c)) ? route_tcgen05_launches(c) : 1;
     return base + (c.mode == MOE_EXPERT_CHOICE ? 1 : 0);
@@ -251,14 +277,15 @@ PackedLayout packed_layout(const moe_config &c) {
     Carver k;
     PackedLayout L{};
     const size_t we = fp8_weights(c) ? 1 : z.elt;   // bytes per stored weight
-    L.w13 = k.take((size_t)c.E * 2 * c.f * c.d * we);
+    const size_t we13 = (fp8_weights(c) || fp8_up(c)) ? 1 : z.elt;   // the up projection's
+    L.w13 = k.take((size_t)c.E * 2 * c.f * c.d * we13);
     L.w2 = k.take((size_t)c.E * c.d * c.f * we);
-    L.w13s = k.take((size_t)2 * z.fs_tot * c.d * we);
+    L.w13s = k.take((size_t)2 * z.fs_tot * c.d * we13);
     L.w2s = k.take((size_t)c.d * z.fs_tot * we);
-    const bool sc = fp8_weights(c);
-    L.sc13 = k.take(sc ? sizeof(float) * (size_t)c.E * 2 * c.f : 0);
+    const bool sc = fp8_weights(c), sc13 = sc || fp8_up(c);
+    L.sc13 = k.take(sc13 ? sizeof(float) * (size_t)c.E * 2 * c.f : 0);
     L.sc2 = k.take(sc ? sizeof(float) * (size_t)c.E * c.d : 0);
-    L.sc13s = k.take(sc ? sizeof(float) * (size_t)2 * z.fs_tot : 0);
+    L.sc13s = k.take(sc13 ? sizeof(float) * (size_t)2 * z.fs_tot : 0);
     L.sc2s = k.take(sc ? sizeof(float) * (size_t)c.d : 0);
     L.total = k.off;
     return L;
@@ -272,6 +299,38 @@ int num_sms() {
     int dev = 0;
     if (current_device(dev) != cudaSuccess || g_sm_count[dev] <= 0) return 148;
     return g_sm_count[dev];
+}
+
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn tmap_encoder() {
+    static EncodeTiledFn encode = nullptr;
+    if (!encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return nullptr;
+        encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return encode;
+}
+}  // namespace
+
+bool make_tmap_u8(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    const EncodeTiledFn encode = tmap_encoder();
+    if (!encode) return false;
+    if (rows == 0) rows = 1;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
@@ -323,7 +382,8 @@ moe_status moe_validate_config(const moe_config *cfg) {
     if (c.T < 0 || c.d <= 0 || c.f <= 0 || c.E <= 0) return MOE_ERR_INVALID_ARG;
     if (c.gate != MOE_GATE_SOFTMAX && c.gate != MOE_GATE_SIGMOID) return MOE_ERR_INVALID_ARG;
     if (c.mode != MOE_TOKEN_CHOICE && c.mode != MOE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
-    if (c.dtype != MOE_F32 && c.dtype != MOE_BF16 && c.dtype != MOE_BF16_FP8W) return MOE_ERR_INVALID_ARG;
+    if (c.dtype != MOE_F32 && c.dtype != MOE_BF16 && c.dtype != MOE_BF16_FP8W && c.dtype != MOE_BF16_FP8UP)
+        return MOE_ERR_INVALID_ARG;
     if (c.drop_policy != MOE_DROP_TOKEN_ORDER && c.drop_policy != MOE_DROP_AFFINITY) return MOE_ERR_INVALID_ARG;
     if (c.n_shared < 0 || (c.n_shared > 0 && c.f_shared <= 0)) return MOE_ERR_INVALID_ARG;
     if (std::isnan(c.capacity_factor)) return MOE_ERR_INVALID_ARG;
@@ -341,7 +401,7 @@ moe_status moe_validate_config(const moe_config *cfg) {
     if (fs > INT32_MAX) return MOE_ERR_UNSUPPORTED;
     if (c.dtype == MOE_BF16) {
         if (c.d % 128 != 0 || c.f % 64 != 0 || fs % 64 != 0) return MOE_ERR_UNSUPPORTED;
-    } else if (c.dtype == MOE_BF16_FP8W) {   // 256-wide tiles for both GEMMs (one fused launch)
+    } else if (c.dtype == MOE_BF16_FP8W || c.dtype == MOE_BF16_FP8UP) {   // 256-wide tiles (one fused launch)
         if (c.d % 256 != 0 || c.f % 128 != 0 || fs % 128 != 0) return MOE_ERR_UNSUPPORTED;
     } else {
         if (c.d % 64 != 0 || c.f % 64 != 0 || fs % 64 != 0) return MOE_ERR_UNSUPPORTED;
@@ -489,6 +549,7 @@ moe_status moe_grouped_ffn_up(const moe_config *cfg, const void *x_perm, const i
     moe_status st = moe_validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    MOE_REQUIRE(!fp8_up(c), MOE_ERR_UNSUPPORTED);   // needs a workspace for its E4M3 rows
     MOE_REQUIRE(x_perm && off && packed && H, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(c.n_shared == 0 || (x && Hs), MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(aligned16(x_perm) && aligned16(x) && aligned16(H) && aligned16(Hs) && aligned4(off),
@@ -508,6 +569,7 @@ moe_status moe_grouped_ffn_down(const moe_config *cfg, const void *H, const void
     moe_status st = moe_validate_config(cfg);
     if (st != MOE_OK) return st;
     const moe_config &c = *cfg;
+    MOE_REQUIRE(!fp8_up(c), MOE_ERR_UNSUPPORTED);   // the halves of the FP8 layer run fused
     MOE_REQUIRE(H && off && packed && Y, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(c.n_shared == 0 || Hs, MOE_ERR_INVALID_ARG);
     MOE_REQUIRE(aligned16(H) && aligned16(Hs) && aligned16(Y) && aligned4(off), MOE_ERR_MISALIGNED);
@@ -530,11 +592,12 @@ moe_status moe_launch_count(const moe_config *cfg, moe_stage stage, int32_t *ker
     switch (stage) {
         case MOE_STAGE_ROUTE: *kernels = empty ? 0 : route_launches(c); break;
         case MOE_STAGE_DISPATCH: *kernels = empty ? 0 : dispatch_launches(c); break;
-        case MOE_STAGE_GROUPED_FFN: *kernels = empty ? 0 : (ffn_fused(c) ? 1 : 2); break;
+        case MOE_STAGE_GROUPED_FFN: *kernels = empty ? 0 : ffn_launches(c); break;
         case MOE_STAGE_COMBINE: *kernels = empty ? 0 : 1; break;
         case MOE_STAGE_FORWARD:
+            // the FP8 up projection quantises x once (before the dispatch gathers its rows)
             *kernels = empty ? 0
-                             : route_launches(c) + dispatch_launches(c) + (ffn_fused(c) ? 1 : 2) +
+                             : route_launches(c) + dispatch_launches(c) + (fp8_up(c) ? 2 : (ffn_fused(c) ? 1 : 2)) +
                                    (gated_down(c) ? 0 : 1);
             break;
         default: return MOE_ERR_INVALID_ARG;
@@ -599,6 +662,42 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const void *W_r, co
     void *Y = w + L.Y;
     st = do_route(c, x, W_r, logit_offset, sel_bias, idx, gw, w + L.route, err, s);
     if (st != MOE_OK) return st;
+    if (fp8_up(c)) {
+        // the tokens to E4M3 once: the dispatch gathers their codes into x_perm and the
+        // shared experts read them; the up tiles look up each row's scale by its token
+        const Sizes z = sizes_of(c);
+        const FfnWs F = ffn_ws(c);
+        uint8_t *xq = reinterpret_cast<uint8_t *>(w + L.ffn + F.xq);
+        float *xsc = reinterpret_cast<float *>(w + L.ffn + F.xsc);
+        int *dep = reinterpret_cast<int *>(w + L.ffn + F.dep);
+        if (launch_quantize_rows(x, c.T, c.d, xq, xsc, s) != cudaSuccess) return MOE_ERR_CUDA;
+        const int32_t *row_token = c.mode == MOE_EXPERT_CHOICE
+                                       ? idx
+                                       : reinterpret_cast<const int32_t *>(w + L.dispatch + dispatch_ws(c).row_token);
+        const bool gated = gated_down(c);
+        GatherZero zero;
+        if (gated) {
+            zero.slot_of = slot_of;
+            zero.T = c.T;
+            zero.y = static_cast<uint4 *>(y);
+            zero.y_vecs = c.d * 2 / 16;
+            zero.dep = dep;
+            zero.ndep = (int)ffn_dep_counters(c);
+        }
+        st = do_dispatch(c, idx, gw, xq, off, cnt_raw, slot_of, x_perm, w + L.dispatch, err, s, zero, c.d);
+        if (st != MOE_OK) return st;
+        F8Rows f8;
+        f8.rs0 = xsc;
+        f8.rtok0 = row_token;
+        f8.rs1 = xsc;
+        if (gated)
+            return from_cuda(launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, xq, w + L.ffn + F.H, nullptr, y, dep,
+                                                      err, s, row_token, gw, /*dep_zeroed=*/true, &f8));
+        if (launch_ffn_fused_tcgen05(c, z, x_perm, off, packed, c.n_shared > 0 ? xq : nullptr, w + L.ffn + F.H,
+                                     w + L.ffn + F.Hs, Y, dep, err, s, nullptr, nullptr, false, &f8) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return from_cuda(launch_combine(c, z, Y, slot_of, gw, y, s));
+    }
     if (gated_down(c)) {
         // one expert per token and no shared experts: the down GEMM writes each kept
         // row straight to its token's output, scaled by the gate; the dispatch gather

@@ -24,10 +24,15 @@ constexpr unsigned kErrBadIndex = 2u;     // an expert or token id outside its r
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// bf16 activations (MOE_BF16, MOE_BF16_FP8W): the tensor-core paths
-inline bool bf16_acts(const moe_config &c) { return c.dtype == MOE_BF16 || c.dtype == MOE_BF16_FP8W; }
+// bf16 activations (MOE_BF16, MOE_BF16_FP8W, MOE_BF16_FP8UP): the tensor-core paths
+inline bool bf16_acts(const moe_config &c) {
+    return c.dtype == MOE_BF16 || c.dtype == MOE_BF16_FP8W || c.dtype == MOE_BF16_FP8UP;
+}
 // expert weights stored as E4M3 codes + per-output-channel fp32 scales
 inline bool fp8_weights(const moe_config &c) { return c.dtype == MOE_BF16_FP8W; }
+// the up projection on E4M3 operands (kind::f8f6f4): activations per token, W1/W3
+// per output channel; H, W2 and Y in bf16
+inline bool fp8_up(const moe_config &c) { return c.dtype == MOE_BF16_FP8UP; }
 
 // ----------------------------------------------------------------------------- sizes
 struct Sizes {
@@ -66,6 +71,15 @@ __host__ __device__ inline size_t tiled_offset8(int p, int i, int BN, int K) {
     return (((size_t)nb * (K / 64) + kb) * BN + r) * 64 + (size_t)(i % 64);
 }
 
+// Byte offset of (row p, column i) of a [N][K] E4M3 operand stored as the
+// tensor-core tile images of kind::f8f6f4: tiles of BN rows x 128 one-byte
+// columns (one k block of 128), N-tile major then K-tile, each row 128 bytes with
+// its 16-byte chunks permuted by chunk ^ (r % 8), the 128-byte swizzle.
+__host__ __device__ inline size_t tiled_offset_f8(int p, int i, int BN, int K) {
+    const int nb = p / BN, r = p % BN, kb = i / 128, ch = (i % 128) / 16, w = i % 16;
+    return (((size_t)nb * (K / 128) + kb) * BN + r) * 128 + (size_t)((ch ^ (r & 7)) * 16 + w);
+}
+
 // Byte offsets inside the packed weight buffer.
 //   w13 : [E][2f][d]      up-projection, K-major, W1/W3 interleaved in groups of kGroup rows
 //   w2  : [E][d][f]       down-projection, K-major
@@ -73,6 +87,8 @@ __host__ __device__ inline size_t tiled_offset8(int p, int i, int BN, int K) {
 //   w2s : [d][fs_tot]
 //   FP8 weights: the same matrices as E4M3 codes (one byte each), then fp32 scales
 //   sc13: [E][2f] and sc2: [E][d] per output row of w13 / w2, sc13s: [2*fs_tot], sc2s: [d]
+//   FP8 up projection: w13 / w13s as E4M3 codes (tiled_offset_f8), w2 / w2s bf16
+//   tile images, scales sc13 and sc13s only
 struct PackedLayout {
     size_t w13, w2, w13s, w2s, sc13, sc2, sc13s, sc2s, total;
 };
@@ -99,10 +115,6 @@ cudaError_t launch_ec_select(const moe_config &c, const float *scores_t, int32_t
 // token), ascending token ids -> tok[e][0..), their scores -> w[e][0..)
 cudaError_t launch_column_select(const moe_config &c, const float *scores_t, int cap, const int32_t *col_cnt,
                                  int32_t *tok, float *w, cudaStream_t s);
-// scoring + selection from split-K partial logits partial[splits][T][npad] (fp32)
-cudaError_t launch_route_select(const moe_config &c, const float *logit_offset, const float *sel_bias,
-                                int32_t *topk_idx, float *topk_w, float *scores_t, float *psum_rows,
-                                const float *partial, int splits, int npad, cudaStream_t s);
 // Extra work of the dispatch gather in the forward of a layer whose down GEMM
 // writes each kept token's output row itself (one expert per token, no shared
 // experts): zero the output rows of the dropped tokens (slot_of[t] < 0) and the
@@ -111,13 +123,16 @@ struct GatherZero {
     const int32_t *slot_of = nullptr;   // [T] (k = 1)
     int64_t T = 0;
     uint4 *y = nullptr;                 // [T][d] in the activation type
+    int y_vecs = 0;                     // 16-byte vectors of a row of y
     int *dep = nullptr;
     int ndep = 0;
 };
+// row_bytes: bytes of a row of x / x_perm (0: d times the activation size; the FP8
+// up projection gathers one-byte E4M3 rows)
 cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *topk_idx, const void *x,
                                int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                int32_t *chunk_cnt, int32_t *row_token, unsigned *err, cudaStream_t s,
-                               const GatherZero &zero = GatherZero{});
+                               const GatherZero &zero = GatherZero{}, int row_bytes = 0);
 size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
 // affinity-ordered capacity drop (token choice): scratch S[E][T] fp32, kept[E][cap]
 // tokens and weights; launches a scatter, the column select, the row placement
@@ -125,10 +140,11 @@ size_t dispatch_tc_scratch_ints(int64_t assignments, int E);
 cudaError_t launch_dispatch_affinity(const moe_config &c, int32_t cap, const int32_t *topk_idx, const float *topk_w,
                                      const void *x, int32_t *off, int32_t *cnt_raw, int32_t *slot_of, void *x_perm,
                                      float *S, int32_t *kept, float *kept_w, int32_t *row_token, unsigned *err,
-                                     cudaStream_t s, const GatherZero &zero = GatherZero{});
+                                     cudaStream_t s, const GatherZero &zero = GatherZero{}, int row_bytes = 0);
 int dispatch_tc_launches(int64_t assignments);
 cudaError_t launch_dispatch_ec(const moe_config &c, const int32_t *ec_tok, const void *x, int32_t *off,
-                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s);
+                               int32_t *cnt_raw, int32_t *slot_of, void *x_perm, unsigned *err, cudaStream_t s,
+                               int row_bytes = 0);
 cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, const int32_t *slot_of,
                            const float *w, void *y, cudaStream_t s);
 cudaError_t launch_pack(const moe_config &c, const void *W1, const void *W3, const void *W2,
@@ -148,13 +164,21 @@ cudaError_t launch_ffn_up_tcgen05(const moe_config &c, const Sizes &z, const voi
 cudaError_t launch_ffn_down_tcgen05(const moe_config &c, const Sizes &z, const void *H, const void *Hs,
                                     const int32_t *off, const void *packed, void *Y, unsigned *err, cudaStream_t s,
                                     const int32_t *row_token = nullptr, const float *row_gate = nullptr);
+// Row scales of E4M3 activations (the FP8 up projection): routed row r has scale
+// rs0[rtok0 ? rtok0[r] : r], shared-expert row t has rs1[t].
+struct F8Rows {
+    const float *rs0 = nullptr;
+    const int32_t *rtok0 = nullptr;
+    const float *rs1 = nullptr;
+};
 // Both expert GEMMs in one persistent (cooperative) launch: up tiles, then down tiles,
 // each waiting for the up tiles of its rows through `dep` (ffn_dep_counters ints,
 // zeroed here).  Needs 256-wide tiles for both (ffn_fused_supported).
 cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const void *x_perm, const int32_t *off,
                                      const void *packed, const void *x, void *H, void *Hs, void *Y, int *dep,
                                      unsigned *err, cudaStream_t s, const int32_t *row_token = nullptr,
-                                     const float *row_gate = nullptr, bool dep_zeroed = false);
+                                     const float *row_gate = nullptr, bool dep_zeroed = false,
+                                     const F8Rows *f8 = nullptr);
 size_t ffn_dep_counters(const moe_config &c);
 bool ffn_fused_supported(const moe_config &c);
 // psum_rows (nullable, [kPsumRows][E], zeroed by the caller): every CTA adds the
@@ -179,6 +203,10 @@ int num_sms();
 moe_status device_ready(unsigned **err_word);
 // limit of the bounded device-side waits (process-wide; moe_set_wait_limit_ns)
 uint64_t wait_limit_ns();
+// Per-row E4M3 quantisation of bf16 rows: s[r] = amax_r / 448, q[r][i] = E4M3(x / s[r])
+// (fp32 division, round to nearest even, saturated; an all-zero row gets s = 0 and
+// zero codes).  rows x d, one warp per row.
+cudaError_t launch_quantize_rows(const void *x, int64_t rows, int d, uint8_t *q, float *s, cudaStream_t st);
 // one CTA that runs the two bounded-wait routines of the tensor-core kernels (see
 // moe_wait_probe); sets kErrWaitTimeout in *err when they give up
 cudaError_t launch_wait_probe(const int32_t *flag, int32_t target, uint64_t limit_ns, unsigned *err, cudaStream_t s);
@@ -217,6 +245,28 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// A dependent launch (as above) of thread-block clusters of `cluster` CTAs along x
+// (gridDim.x a multiple of it).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     int cluster, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

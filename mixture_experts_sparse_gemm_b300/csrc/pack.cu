@@ -145,10 +145,12 @@ __global__ void amax_down_kernel(const unsigned short *__restrict__ W2, float *s
     sc[(size_t)e * d + n] = amax / 448.f;
 }
 
-// Codes of the up projection, transposed through shared memory into FP8 tile images.
+// Codes of the up projection, transposed through shared memory into FP8 tile images:
+// 64-byte rows for the converter warps (mma_ready == 0), or the 128-byte swizzled
+// rows that kind::f8f6f4 reads directly (mma_ready == 1, tiled_offset_f8).
 __global__ void quant_up_kernel(const unsigned short *__restrict__ W1, const unsigned short *__restrict__ W3,
                                 const float *__restrict__ sc, uint8_t *__restrict__ out, int d, int nsub, int fsub,
-                                int tile_n) {
+                                int tile_n, int mma_ready) {
     __shared__ float tile[32][33];
     const int ftot = nsub * fsub;
     const int e = blockIdx.z >> 1, m = blockIdx.z & 1;
@@ -167,7 +169,8 @@ __global__ void quant_up_kernel(const unsigned short *__restrict__ W1, const uns
         if (i < d && h < ftot) {
             const int r = (h / kGroup) * (2 * kGroup) + m * kGroup + (h % kGroup);
             const float s = sc[(size_t)e * 2 * ftot + r];
-            out[(size_t)e * 2 * ftot * d + tiled_offset8(r, i, tile_n, d)] = e4m3_code(tile[threadIdx.x][hh], s);
+            const size_t o = mma_ready ? tiled_offset_f8(r, i, tile_n, d) : tiled_offset8(r, i, tile_n, d);
+            out[(size_t)e * 2 * ftot * d + o] = e4m3_code(tile[threadIdx.x][hh], s);
         }
     }
 }
@@ -211,7 +214,7 @@ cudaError_t pack_fp8(const moe_config &c, const void *W1, const void *W3, const 
     amax_down_kernel<<<dim3((c.d + 255) / 256, c.E), 256, 0, s>>>(static_cast<const U *>(W2), f(L.sc2), c.d, 1,
                                                                   c.f);
     quant_up_kernel<<<dim3((c.f + 31) / 32, (c.d + 31) / 32, c.E * 2), blk, 0, s>>>(
-        static_cast<const U *>(W1), static_cast<const U *>(W3), f(L.sc13), q(L.w13), c.d, 1, c.f, tn_up);
+        static_cast<const U *>(W1), static_cast<const U *>(W3), f(L.sc13), q(L.w13), c.d, 1, c.f, tn_up, 0);
     quant_down_kernel<<<dim3((c.d + 31) / 32, (c.f + 31) / 32, c.E), blk, 0, s>>>(
         static_cast<const U *>(W2), f(L.sc2), q(L.w2), c.d, 1, c.f, tn_dn);
     if (c.n_shared > 0) {
@@ -223,9 +226,41 @@ cudaError_t pack_fp8(const moe_config &c, const void *W1, const void *W3, const 
                                                                      c.n_shared, c.f_shared);
         quant_up_kernel<<<dim3((fs + 31) / 32, (c.d + 31) / 32, 2), blk, 0, s>>>(
             static_cast<const U *>(W1s), static_cast<const U *>(W3s), f(L.sc13s), q(L.w13s), c.d, c.n_shared,
-            c.f_shared, tn_up);
+            c.f_shared, tn_up, 0);
         quant_down_kernel<<<dim3((c.d + 31) / 32, (fs + 31) / 32, 1), blk, 0, s>>>(
             static_cast<const U *>(W2s), f(L.sc2s), q(L.w2s), c.d, c.n_shared, c.f_shared, tn_dn);
+    }
+    return cudaGetLastError();
+}
+
+// FP8 up projection: W1 / W3 as E4M3 codes in the tile images kind::f8f6f4 reads
+// (one scale per output channel), W2 as bf16 tile images.
+cudaError_t pack_fp8_up(const moe_config &c, const void *W1, const void *W3, const void *W2, const void *W1s,
+                        const void *W3s, const void *W2s, void *packed, cudaStream_t s) {
+    const PackedLayout L = packed_layout(c);
+    char *base = static_cast<char *>(packed);
+    const dim3 blk(32, 8);
+    const int tn_up = up_tile_n(c), tn_dn = down_tile_n(c);
+    using U = unsigned short;
+    auto f = [&](size_t off) { return reinterpret_cast<float *>(base + off); };
+    auto q = [&](size_t off) { return reinterpret_cast<uint8_t *>(base + off); };
+    amax_up_kernel<<<dim3((c.f + 255) / 256, c.E * 2), 256, 0, s>>>(static_cast<const U *>(W1),
+                                                                   static_cast<const U *>(W3), f(L.sc13), c.d, 1,
+                                                                   c.f, 2 * c.f);
+    quant_up_kernel<<<dim3((c.f + 31) / 32, (c.d + 31) / 32, c.E * 2), blk, 0, s>>>(
+        static_cast<const U *>(W1), static_cast<const U *>(W3), f(L.sc13), q(L.w13), c.d, 1, c.f, tn_up, 1);
+    pack_down_kernel<U><<<dim3((c.d + 31) / 32, (c.f + 31) / 32, c.E), blk, 0, s>>>(
+        static_cast<const U *>(W2), reinterpret_cast<U *>(base + L.w2), c.d, 1, c.f, tn_dn);
+    if (c.n_shared > 0) {
+        const int fs = c.n_shared * c.f_shared;
+        amax_up_kernel<<<dim3((fs + 255) / 256, 2), 256, 0, s>>>(static_cast<const U *>(W1s),
+                                                                  static_cast<const U *>(W3s), f(L.sc13s), c.d,
+                                                                  c.n_shared, c.f_shared, 2 * fs);
+        quant_up_kernel<<<dim3((fs + 31) / 32, (c.d + 31) / 32, 2), blk, 0, s>>>(
+            static_cast<const U *>(W1s), static_cast<const U *>(W3s), f(L.sc13s), q(L.w13s), c.d, c.n_shared,
+            c.f_shared, tn_up, 1);
+        pack_down_kernel<U><<<dim3((c.d + 31) / 32, (fs + 31) / 32, 1), blk, 0, s>>>(
+            static_cast<const U *>(W2s), reinterpret_cast<U *>(base + L.w2s), c.d, c.n_shared, c.f_shared, tn_dn);
     }
     return cudaGetLastError();
 }
@@ -236,6 +271,7 @@ cudaError_t launch_pack(const moe_config &c, const void *W1, const void *W3, con
                         const void *W3s, const void *W2s, void *packed, cudaStream_t s) {
     if (c.dtype == MOE_F32) return pack_typed<float>(c, W1, W3, W2, W1s, W3s, W2s, packed, s);
     if (fp8_weights(c)) return pack_fp8(c, W1, W3, W2, W1s, W3s, W2s, packed, s);
+    if (fp8_up(c)) return pack_fp8_up(c, W1, W3, W2, W1s, W3s, W2s, packed, s);
     return pack_typed<unsigned short>(c, W1, W3, W2, W1s, W3s, W2s, packed, s);   // bf16 bits
 }
 

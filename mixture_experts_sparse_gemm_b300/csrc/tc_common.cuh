@@ -144,6 +144,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 inputs (K = 32 per instruction), fp32
+// accumulate, one CTA.  Same shared-memory descriptors as mma_bf16: a K step of
+// 32 one-byte elements is 32 bytes of the 128-byte swizzled row.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -199,6 +212,12 @@ __device__ __forceinline__ uint64_t sdesc_mn128(uint32_t saddr, uint32_t lbo) {
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor of kind::f8f6f4 with E4M3 A/B, fp32 D, both K-major:
+// D format [4,6) = 1 (f32), A format [7,10) = 0 (E4M3), B format [10,13) = 0,
+// N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 // bit 16 of the instruction descriptor: B is MN-major ("transpose B")
 constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
@@ -206,5 +225,7 @@ constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // host: 2-D bf16 tensor map [rows][cols] row-major, box = [box_rows][64], 128-byte swizzle
 bool make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// host: 2-D one-byte (E4M3 codes) tensor map [rows][cols], box = [box_rows][128], 128-byte swizzle
+bool make_tmap_u8(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 
 }  // namespace moe

@@ -14,6 +14,12 @@
 //               scales are applied in the epilogue
 //   warp 14     (W8 only) FP8 producer: the weight tiles into their own ring,
 //               ahead of the MMA (warp 0 then brings only A, into its own ring)
+//   warps 6..15 (split-K router only) selection warps, idle until the tile's
+//               partial logits are reduced across the cluster
+// F8A instantiations run the tiles of a GEMM marked a_f8 (the up projection) on
+// E4M3 operands: kind::f8f6f4 MMAs of K = 32, a k block of 128 one-byte elements
+// (the same 128-byte swizzled rows as a bf16 block of 64), and the epilogue scales
+// the accumulator by the row's activation scale and the column's weight scale.
 // Tiles never straddle segments: the tile table is built on the device from
 // off[] (segment s < E = routed expert s, segment E = merged shared experts), and
 // a segment's last M tile reads rows past its end (the next segment's rows, or
@@ -28,11 +34,15 @@
 //               selection-only bias, top-k by insertion in ascending expert order
 //               (ties keep the lower index), renormalised weights; or, for Expert
 //               Choice, the softmax scores written expert-major.
+//   kEpiSplitRoute  router with K split over a cluster: partial logits to shared
+//               memory, summed across the cluster's CTAs and selected one warp per
+//               token (split_route_select).
 #pragma once
 
 #include <cuda_fp16.h>
 #include <float.h>
 
+#include "route_common.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
@@ -46,9 +56,17 @@ constexpr int kThreads = 192;
 constexpr int kEpiSwiGLU = 0;   // up projection (+ SwiGLU)
 constexpr int kEpiStore = 1;    // down projection (optionally gated, see TcArgs::gated)
 constexpr int kEpiFfn = 2;      // both: up tiles, then down tiles, in one persistent launch
-constexpr int kEpiPartial = 3;  // split-K partial sums: fp32 rows of C0[split][rows][BN]
+constexpr int kEpiPartial = 3;  // router kinds start here (kEpiRoute.., kEpiSplitRoute..)
 // router epilogue keeping the best KMAX candidates: kEpiRoute + KMAX, KMAX in {1, 2, 4, 8}
 constexpr int kEpiRoute = 10;
+// split-K router reduced inside a thread-block cluster: kEpiSplitRoute + KPL, KPL =
+// experts per lane of the selecting warps (E <= 32 KPL).  The cluster is the K
+// splits of one token tile: each CTA leaves its partial logits in shared memory,
+// and after a cluster barrier CTA q sums the partials of its share of the tile's
+// tokens from every CTA's shared memory (in split order) and scores and selects
+// them one warp per token.  No partial logits go through global memory.
+constexpr int kEpiSplitRoute = 20;
+constexpr int kSplitSelectWarps = 10;   // extra warps of a split-K router CTA (16 select in all)
 
 // W8: B arrives as FP8 E4M3 tiles (BN x 64 bytes) in a ring of its own (6 slots),
 // brought by an FP8 producer warp and released by eight converter warps as soon as
@@ -56,7 +74,9 @@ constexpr int kEpiRoute = 10;
 // and releases.  A has its own ring (3 stages).  The weights thus run up to eight
 // k blocks ahead of the MMA, as many weight bytes in flight as the bf16 kernel has.
 // Shared memory: stages (bf16: A | B; W8: A) | W8: bf16 B buffers | W8: FP8 slots.
-template <int BN, bool W8 = false>
+// EXTRA: warps beyond the GEMM roles (the cluster-reduced split-K router adds
+// kSplitSelectWarps that only take part in its selection phase).
+template <int BN, bool W8 = false, int EXTRA = 0>
 struct TcCfg {
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = BN * kBK * 2;      // bf16 B tile, as the MMA reads it
@@ -67,7 +87,7 @@ struct TcCfg {
     static constexpr int kB8Stages = W8 ? 4 : 0;      // FP8 ring slots
     static constexpr int kConvWarps = W8 ? 12 : 0;
     static constexpr int kB8Warp = kThreads / 32 + kConvWarps;   // W8: warp of the FP8 copies
-    static constexpr int kThreadsCta = kThreads + 32 * kConvWarps + (W8 ? 32 : 0);
+    static constexpr int kThreadsCta = kThreads + 32 * kConvWarps + (W8 ? 32 : 0) + 32 * EXTRA;
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
     static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kBBufs + 2 * kB8Stages) * 8;
     static constexpr int kMiscBytes = 64 + sizeof(int) * (6 * (kMaxE + 2));
@@ -101,7 +121,7 @@ struct TcGemm {
     void *C1;             // shared output rows (bf16)
     int ldc0, ldc1;       // output row pitch in elements
     // > 1: the K range is split over ksplit tiles (the N-block index is the split;
-    // one N tile of width BN covers all of N), each writing its partial sums
+    // one N tile of width BN covers all of N; cluster-reduced router only)
     int ksplit;
     // FP8 weights (W8 kernels): fp32 scale of every B row (output column), routed
     // [E][b_rows0] and shared [N]; applied to the accumulator in the epilogue
@@ -109,6 +129,14 @@ struct TcGemm {
     // B given MN-major through tmB0 / tmB1: a row-major [K][N] matrix read in place,
     // each stage BN / 64 boxes of [64 K rows][64 N] (BN >= 64; router launches only)
     int b_mn;
+    // E4M3 A and B (kernels instantiated with F8A): kind::f8f6f4, 128 K per stage;
+    // the accumulator is scaled by the row scale of A and the column scale of B
+    // (sc0 / sc1).  Row r of a routed segment has scale rs0[rtok0 ? rtok0[r] : r],
+    // row r of the shared segment rs1[r].
+    int a_f8;
+    const float *rs0;
+    const int32_t *rtok0;
+    const float *rs1;
 };
 
 struct TcArgs {
@@ -133,6 +161,29 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __ex
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// all threads of every CTA of the cluster; shared-memory writes before it are
+// visible to the other CTAs' reads after it
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // Keep the best KMAX (key, index, logit) triples in (key desc, index asc) order.
@@ -298,23 +349,97 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
     }
 }
 
+// KPL consecutive floats of another CTA's shared memory (16-byte loads where they fit)
+template <int KPL>
+__device__ __forceinline__ void ld_dsmem_vec(uint32_t addr, float (&v)[KPL]) {
+    if constexpr (KPL % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < KPL; q += 4)
+            asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v[q]), "=f"(v[q + 1]), "=f"(v[q + 2]), "=f"(v[q + 3])
+                         : "r"(addr + 4u * q)
+                         : "memory");
+    } else if constexpr (KPL == 2) {
+        asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(addr) : "memory");
+    } else {
+        v[0] = ld_dsmem(addr);
+    }
+}
+
+// Selection of a cluster-reduced split-K router tile, run by every thread of each
+// CTA of the cluster after the cluster barrier.  Every CTA holds its partial
+// logits of the tile's rows at red + row * pitch floats; CTA q takes the rows
+// [q * ceil(128 / splits), ...) of the tile, and one warp per row sums the
+// partials of all CTAs of the cluster in split order (reading the others' shared
+// memory; lane l holds experts l * KPL ..), adds the logit offset, and scores and
+// selects it (warp_score_select).
+template <int KPL>
+__device__ __forceinline__ void split_route_select(const RouteEpi &r, const uint8_t *red, int pitch, int splits,
+                                                   int T, int mb, float *sacc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+    const int rank = (int)cluster_ctarank();
+    const int row0 = mb * kBM;
+    const int rows = min(kBM, T - row0);
+    const int per = (kBM + splits - 1) / splits;
+    const int lo = rank * per, hi = min(rows, lo + per);
+    RouteArgs a{};
+    a.logit_offset = r.logit_offset;
+    a.sel_bias = r.sel_bias;
+    a.T = r.T;
+    a.E = r.E;
+    a.k = r.k;
+    a.gate = r.gate;
+    a.mode = r.mode;
+    a.renorm = r.renorm;
+    a.topk_idx = r.topk_idx;
+    a.topk_w = r.topk_w;
+    a.scores_t = r.scores_t;
+    a.psum_rows = r.psum_rows;
+    const uint32_t base = smem_u32(red);
+    float pacc[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) pacc[i] = 0.f;
+    for (int rr = lo + warp; rr < hi; rr += nwarps) {
+        // every split's values of the row are loaded before the sums (split order kept)
+        float pv[kMaxRouteSplits][KPL];
+        const uint32_t off = base + (uint32_t)((rr * pitch + lane * KPL) * 4);
+#pragma unroll
+        for (int q = 0; q < kMaxRouteSplits; ++q)
+            if (q < splits) ld_dsmem_vec<KPL>(mapa_shared(off, (uint32_t)q), pv[q]);
+        float u[KPL];
+#pragma unroll
+        for (int i = 0; i < KPL; ++i) {
+            const int e = lane * KPL + i;
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < kMaxRouteSplits; ++q)
+                if (q < splits) v += pv[q][i];
+            if (e < a.E && a.logit_offset) v += a.logit_offset[e];
+            u[i] = (e < a.E) ? v : -FLT_MAX;
+        }
+        warp_score_select<KPL, true>(a, u, row0 + rr, lane, pacc);
+    }
+    flush_prob_sum<KPL, true>(a, pacc, lane, sacc);
+}
+
 // Tile epilogues (all 32 lanes of each epilogue warp run them; `row` is the
 // thread's accumulator row, `rows` the valid rows of the tile).
 // sc (FP8 weights, else null): scales of the tile's BN accumulator columns
-__device__ __forceinline__ void scale16(uint32_t (&v)[16], const float *sc) {
+// rs: scale of the thread's row (E4M3 activations), 1 otherwise
+__device__ __forceinline__ void scale16(uint32_t (&v)[16], const float *sc, float rs = 1.f) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const float4 f = *reinterpret_cast<const float4 *>(sc + 4 * q);
-        v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) * f.x);
-        v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * f.y);
-        v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * f.z);
-        v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * f.w);
+        v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) * (f.x * rs));
+        v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) * (f.y * rs));
+        v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) * (f.z * rs));
+        v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) * (f.w * rs));
     }
 }
 
 template <int BN>
 __device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, int ldc, int grow, int row, int rows,
-                                           int nb, const float *sc) {
+                                           int nb, const float *sc, float rs = 1.f) {
 #pragma unroll 1
     for (int grp = 0; grp < BN / 128; ++grp) {
 #pragma unroll 1
@@ -324,8 +449,8 @@ __device__ __forceinline__ void epi_swiglu(uint32_t taddr, __nv_bfloat16 *Cp, in
             tmem_ld16(taddr + grp * 128 + 64 + c * 16, u);
             tmem_ld_wait();
             if (sc) {
-                scale16(g, sc + grp * 128 + c * 16);
-                scale16(u, sc + grp * 128 + 64 + c * 16);
+                scale16(g, sc + grp * 128 + c * 16, rs);
+                scale16(u, sc + grp * 128 + 64 + c * 16, rs);
             }
             uint32_t o[8];
 #pragma unroll
@@ -395,15 +520,17 @@ struct TileAt {
     int phase, s, mb, nb;
 };
 
-template <int BN, int EPI, bool W8>
-__global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
+template <int BN, int EPI, bool W8, bool F8A = false>
+__global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0>::kThreadsCta, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                            const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
                            TcArgs a) {
-    using C = TcCfg<BN, W8>;
+    using C = TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0>;
     constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
     constexpr bool kRouter = EPI >= kEpiPartial;   // router launches may read B (W_r) MN-major
+    constexpr bool kFusedRoute = EPI > kEpiRoute && EPI < kEpiSplitRoute;
+    constexpr bool kSplitRoute = EPI > kEpiSplitRoute;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *tiles = smem;
@@ -429,7 +556,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
     float *psum_cta = reinterpret_cast<float *>(mtile_start + (kMaxE + 2));   // router score sums of this CTA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if constexpr (EPI > kEpiRoute) {
+    if constexpr (kFusedRoute) {
         for (int e = threadIdx.x; e < kMaxE; e += C::kThreadsCta) psum_cta[e] = 0.f;   // before the first barrier
     }
 
@@ -495,9 +622,22 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
         __syncthreads();
         total += tile_start1[S];
     }
+    // Tiles of this CTA: tile0, tile0 + tstep, ...  A cluster-reduced split-K router
+    // launch has one CTA per tile, and the CTAs of a cluster (consecutive blocks)
+    // take the K splits of one token tile: split = rank, M block = block / splits.
+    const int mblk0 = (seg_rows[0] + kBM - 1) / kBM;
+    int tile0 = blockIdx.x, tstep = gridDim.x;
+    if constexpr (kSplitRoute) {
+        const int splits = a.p[0].ksplit;
+        tile0 = (int)(blockIdx.x % splits) * mblk0 + (int)(blockIdx.x / splits);
+        tstep = total;
+    }
+    static_assert(!(W8 && F8A), "FP8 weights go through the converters or straight to the MMA, not both");
+    // E4M3 operands: a k block holds 128 K (128 bytes per row, as the bf16 block's 64)
+    auto tile_f8 = [&](const TileAt &t) { return F8A && a.p[t.phase].a_f8 != 0; };
     // k blocks [kb0, kb0 + nk) of a tile (a K split takes its share of them)
     auto krange = [&](const TileAt &t, const TcGemm &G, int &kb0, int &nk) {
-        const int all = ((t.s < G.g.E) ? G.K0 : G.K1) / kBK;
+        const int all = ((t.s < G.g.E) ? G.K0 : G.K1) / (tile_f8(t) ? 128 : kBK);
         if (G.ksplit > 1) {
             const int per = (all + G.ksplit - 1) / G.ksplit;
             kb0 = t.nb * per;
@@ -526,7 +666,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int tile = tile0; tile < total && ok; tile += tstep) {
                 const TileAt t = locate(tile);
                 const TcGemm &G = a.p[t.phase];
                 const bool routed = t.s < G.g.E;
@@ -557,7 +697,13 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     bt = (routed ? G.Bt0 + (size_t)t.s * G.bt_seg0 : G.Bt1) + (size_t)img * nk * img_bytes +
                          (size_t)sub * kBCopy;
                 }
-                for (int kb = 0; kb < nk; ++kb) {
+                // router tiles read their token rows once, all CTAs at the same time: each
+                // starts at its own k block, so that concurrent requests fall on different
+                // column offsets of rows whose stride is a power of two (spread over the
+                // DRAM channels); the MMA sums the k blocks in this rotated order
+                const int rot = kRouter ? (int)((tile * 5) % nk) : 0;
+                for (int kb_ = 0; kb_ < nk; ++kb_) {
+                    const int kb = (kb_ + rot) % nk;
                     if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
@@ -565,7 +711,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     const uint32_t fb = smem_u32(&full[stage]);
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
                     mbar_arrive_expect_tx(fb, C::kABytes + (W8 ? 0 : kBCopy));   // A + B (W8: A only)
-                    tma_load_2d(smem_u32(st), mA, (kb0 + kb) * kBK, arow, fb);
+                    tma_load_2d(smem_u32(st), mA, (kb0 + kb) * (tile_f8(t) ? 128 : kBK), arow, fb);
                     if (W8)
                         ;   // the FP8 B tiles come through their own ring (B8 producer warp)
                     else if (bt)
@@ -604,17 +750,19 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
         if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
+            constexpr uint32_t kIdescF8 = idesc_e4m3_f32(kBM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int bb = 0;           // W8: bf16 B buffer
             uint32_t bph = 0;
             int it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+            for (int tile = tile0; tile < total && ok; tile += tstep, ++it) {
                 const TileAt t = locate(tile);
                 const TcGemm &G = a.p[t.phase];
                 int kb0, nk;
                 krange(t, G, kb0, nk);
+                const bool f8 = tile_f8(t);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
                 if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
@@ -644,9 +792,17 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                     // the MN-major tile (encoded >> 4)
                     const uint64_t bstep = bmn ? (2048 >> 4) : 2;
                     const uint32_t idesc = bmn ? (kIdesc | kIdescBMajorMN) : kIdesc;
+                    if (F8A && f8) {
+                        // four K steps of 32 E4M3 elements, 32 bytes each
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc, (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_f8(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + 2 * kk, kIdescF8, (kb | kk) != 0);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc,
+                                     (kb | kk) != 0);
+                    }
                     mma_commit(smem_u32(&empty[stage]));
                     if constexpr (W8) {
                         mma_commit(smem_u32(&bempty[bb]));
@@ -678,7 +834,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             uint32_t fph = 0;
             int issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int tile = tile0; tile < total && ok; tile += tstep) {
                 const TileAt t = locate(tile);
                 const TcGemm &G = a.p[t.phase];
                 const bool routed = t.s < G.g.E;
@@ -732,7 +888,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
         int bb = 0, f = 0;
         uint32_t bph = 0, fph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int tile = tile0; tile < total && ok; tile += tstep) {
             const TileAt t = locate(tile);
             int kb0, nk;
             krange(t, a.p[t.phase], kb0, nk);
@@ -773,12 +929,14 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
                 }
             }
         }
+    } else if (kSplitRoute && warp >= kThreads / 32) {
+        // extra warps of the split router: they only take part in the selection
     } else {
         // ---------------------------------------------------------------- epilogue
         const int quarter = warp & 3;   // TMEM lanes [32*quarter, 32*quarter + 32)
         const int row = quarter * 32 + lane;
         int it = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+        for (int tile = tile0; tile < total; tile += tstep, ++it) {
             const TileAt t = locate(tile);
             const TcGemm &G = a.p[t.phase];
             const int acc = it & 1;
@@ -792,32 +950,35 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
             const int rows = min(kBM, seg_rows[t.s] - t.mb * kBM);
             const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-            if constexpr (EPI > kEpiRoute) {
+            if constexpr (kFusedRoute) {
                 route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows, psum_cta);
-            } else if constexpr (EPI == kEpiPartial) {
-                // fp32 partial sums of K split t.nb: C0[split][row][BN], row stride BN
-                float *P = static_cast<float *>(G.C0) + ((size_t)t.nb * G.ldc0 + grow) * BN;
-                const int nchunk = min(BN / 16, (a.route.E + 15) / 16);   // chunks holding experts
+            } else if constexpr (kSplitRoute) {
+                // this CTA's partial logits of the tile -> shared memory, row r at r * (BN + 4)
+                // floats (the stage ring is idle: every MMA of the tile has completed)
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                float *red = reinterpret_cast<float *>(tiles) + (size_t)row * (BN + 4);
+                const int nchunk = min(BN / 16, (a.route.E + 15) / 16);
 #pragma unroll 1
                 for (int c = 0; c < nchunk; ++c) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c * 16, v);
                     tmem_ld_wait();
-                    if (row < rows) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(P + c * 16);
+                    uint4 *dst = reinterpret_cast<uint4 *>(red + c * 16);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                    }
+                    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             } else {
                 __nv_bfloat16 *Cp = static_cast<__nv_bfloat16 *>(routed ? G.C0 : G.C1);
                 const int ldc = routed ? G.ldc0 : G.ldc1;
                 const bool up = (EPI == kEpiSwiGLU) || (EPI == kEpiFfn && t.phase == 0);
-                // W8: scales of this tile's BN output columns
-                const float *sc =
-                    W8 ? (routed ? G.sc0 + (size_t)t.s * G.b_rows0 : G.sc1) + (size_t)t.nb * BN : nullptr;
+                const bool f8 = tile_f8(t);
+                // W8 or E4M3 operands: scales of this tile's BN output columns
+                const float *sc = (W8 || f8) ? (routed ? G.sc0 + (size_t)t.s * G.b_rows0 : G.sc1) + (size_t)t.nb * BN
+                                             : nullptr;
                 if (up) {
-                    epi_swiglu<BN>(taddr, Cp, ldc, grow, row, rows, t.nb, sc);
+                    float rs = 1.f;   // E4M3 activations: the scale of this row's token
+                    if (f8 && row < rows) rs = routed ? G.rs0[G.rtok0 ? G.rtok0[grow] : grow] : G.rs1[grow];
+                    epi_swiglu<BN>(taddr, Cp, ldc, grow, row, rows, t.nb, sc, rs);
                 } else {
                     size_t orow = (size_t)grow;
                     float scale = 1.f;
@@ -848,7 +1009,13 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
     }
 
     __syncthreads();
-    if constexpr (EPI > kEpiRoute) {
+    if constexpr (kSplitRoute) {
+        cluster_sync();   // every CTA of the cluster holds its partial rows in shared memory
+        split_route_select<EPI - kEpiSplitRoute>(a.route, tiles, BN + 4, a.p[0].ksplit, seg_rows[0],
+                                                 tile0 % mblk0, psum_cta);
+        cluster_sync();   // no CTA leaves while another may still read its rows
+    }
+    if constexpr (kFusedRoute) {
         if (a.route.psum_rows) {   // this CTA's router score sums into its row: one atomic per expert
             float *row = a.route.psum_rows + (size_t)(blockIdx.x % kPsumRows) * a.route.E;
             for (int e = threadIdx.x; e < a.route.E; e += C::kThreadsCta) atomicAdd(row + e, psum_cta[e]);
@@ -865,11 +1032,11 @@ __global__ void __launch_bounds__(TcCfg<BN, W8>::kThreadsCta, 1)
 // waiting on other CTAs' up tiles, so it is a cooperative launch (all CTAs resident).
 // Every CTA waits for the previous kernel on the stream before its first global
 // access, so the launch is a dependent one and its setup overlaps that kernel.
-template <int BN, int EPI, bool W8 = false>
+template <int BN, int EPI, bool W8 = false, bool F8A = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
                         const CUtensorMap &a2, const CUtensorMap &a3, const TcArgs &args_in, int64_t max_tiles,
                         cudaStream_t s) {
-    auto kern = tc_grouped_gemm_kernel<BN, EPI, W8>;
+    auto kern = tc_grouped_gemm_kernel<BN, EPI, W8, F8A>;
     constexpr int kBlock = TcCfg<BN, W8>::kThreadsCta;
     TcArgs args = args_in;
     args.wait_ns = wait_limit_ns();
@@ -894,11 +1061,30 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
     return err;
 }
 
+// Cluster-reduced split-K router (kEpiSplitRoute + KPL): one CTA per (token tile,
+// K split), clusters of `splits` CTAs, each cluster one token tile.
+template <int BN, int EPI>
+cudaError_t launch_gemm_split_route(const CUtensorMap &a0, const CUtensorMap &b0, const TcArgs &args_in, int tiles,
+                                    int splits, cudaStream_t s) {
+    static_assert(EPI > kEpiSplitRoute, "cluster launch of the split-K router only");
+    auto kern = tc_grouped_gemm_kernel<BN, EPI, false>;
+    constexpr int kBlock = TcCfg<BN, false, kSplitSelectWarps>::kThreadsCta;
+    static_assert(kBM * (BN + 4) * 4 <= TcCfg<BN, false>::kStages * TcCfg<BN, false>::kStageBytes,
+                  "partial rows fit in the stage ring");
+    TcArgs args = args_in;
+    args.wait_ns = wait_limit_ns();
+    const size_t smem = TcCfg<BN, false>::kSmem;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    return launch_dependent_cluster(kern, dim3(tiles * splits), dim3(kBlock), smem, s, splits, a0, a0, b0, b0, a0, a0,
+                                    args);
+}
+
 // Single-GEMM launches pass their A maps again for the unused second phase.
-template <int BN, int EPI, bool W8 = false>
+template <int BN, int EPI, bool W8 = false, bool F8A = false>
 cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &b1,
                         const TcArgs &args, int64_t max_tiles, cudaStream_t s) {
-    return launch_gemm<BN, EPI, W8>(a0, a1, b0, b1, a0, a1, args, max_tiles, s);
+    return launch_gemm<BN, EPI, W8, F8A>(a0, a1, b0, b1, a0, a1, args, max_tiles, s);
 }
 
 }  // namespace

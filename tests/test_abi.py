@@ -51,6 +51,17 @@ def test_workload_configs_are_valid(name):
     assert B.moe_packed_weights_size(cfg) > 0
 
 
+def test_fp8up_sizes():
+    # the up projection's weights are one byte each, W2 stays bf16; scales for W1 | W3 only
+    cfg = B.config(T=64, d=256, E=4, f=128, k=1, dtype="fp8up")
+    ref = B.config(T=64, d=256, E=4, f=128, k=1, dtype="bf16")
+    kib = lambda n: (n + 1023) // 1024 * 1024   # noqa: E731
+    assert B.moe_packed_weights_size(cfg) == kib(4 * 2 * 128 * 256) + kib(4 * 256 * 128 * 2) + kib(4 * 4 * 2 * 128)
+    assert B.moe_packed_weights_size(ref) == kib(4 * 2 * 128 * 256 * 2) + kib(4 * 256 * 128 * 2)
+    # the FFN stage holds E4M3 codes and scales of its rows and of the tokens
+    assert B.moe_workspace_size(cfg, B.MOE_STAGE_GROUPED_FFN) > B.moe_workspace_size(ref, B.MOE_STAGE_GROUPED_FFN)
+
+
 @pytest.mark.parametrize("kw,want", [
     (dict(k=9, E=16), B.MOE_ERR_UNSUPPORTED),
     (dict(k=3, E=2), B.MOE_ERR_INVALID_ARG),
@@ -69,6 +80,11 @@ def test_workload_configs_are_valid(name):
     (dict(dtype="fp8w", d=384), B.MOE_ERR_UNSUPPORTED),
     (dict(dtype="fp8w", f=64), B.MOE_ERR_UNSUPPORTED),
     (dict(dtype="fp8w", n_shared=1, f_shared=64), B.MOE_ERR_UNSUPPORTED),
+    # FP8 up projection: the same tile widths (one fused launch)
+    (dict(dtype="fp8up", d=384), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="fp8up", f=64), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="fp8up", n_shared=1, f_shared=64), B.MOE_ERR_UNSUPPORTED),
+    (dict(dtype="fp8up", d=256, f=128, n_shared=1, f_shared=128), B.MOE_OK),
     (dict(dtype="f32", d=96), B.MOE_ERR_UNSUPPORTED),
     # accepted: the smallest shapes of each mode, an empty batch, the affinity drop
     (dict(dtype="fp8w", d=256, f=128, n_shared=1, f_shared=128), B.MOE_OK),
@@ -145,9 +161,10 @@ def test_valid_call_without_gpu_reports_cuda_error():
 
 # Kernels each call launches (moe_launch_count; bench.py's gpu_launches is K times the
 # forward count), per stage: route, dispatch, grouped FFN, combine, forward.
-#   route:    tensor-core router GEMM (W_r read in place) = 1; with fewer than 74 token
-#             tiles and a long d, split-K GEMM + select = 2; Expert Choice adds the
-#             column select; E not a multiple of 8 adds the W_r transpose; fp32: 1
+#   route:    tensor-core router GEMM (W_r read in place) = 1, also with fewer than 74
+#             token tiles and a long d (split-K in clusters, reduced and selected in
+#             the same launch); Expert Choice adds the column select; E not a
+#             multiple of 8 adds the W_r transpose; fp32: 1
 #   dispatch: single-CTA plan + gather = 2 (at most 32768 assignments), else count,
 #             scan, rank + gather = 4; Expert Choice: slots + gather = 2
 #   FFN:      one fused tensor-core launch; fp32: up + down = 2
@@ -156,13 +173,17 @@ def test_valid_call_without_gpu_reports_cuda_error():
 LAUNCHES = {
     "tiny_top2_fp32": [1, 2, 2, 1, 6],
     "switch_top1_cap1.25": [1, 2, 1, 1, 4],
-    "mixtral_T16": [2, 2, 1, 1, 6],
-    "mixtral_T4096": [2, 2, 1, 1, 6],
+    "mixtral_T16": [1, 2, 1, 1, 5],
+    "mixtral_T4096": [1, 2, 1, 1, 5],
     "mixtral_T16384": [1, 2, 1, 1, 5],
-    "deepseek_v3": [2, 2, 1, 1, 6],
+    "deepseek_v3": [1, 2, 1, 1, 5],
     "expert_choice_zipf": [2, 2, 1, 1, 6],
 }
 LAUNCH_EXTRA = {
+    # FP8 up projection: the forward quantises x once; the FFN stage quantises its
+    # rows (and the shared experts' input) before the fused launch
+    "fp8up_switch": (WORKLOADS["switch_top1_cap1.25"].with_(dtype="fp8up", name="fp8up_sw"), [1, 2, 2, 1, 5]),
+    "fp8up_deepseek": (WORKLOADS["deepseek_v3"].with_(dtype="fp8up", name="fp8up_ds"), [1, 2, 3, 1, 6]),
     "transposed_router": (WORKLOADS["mixtral_T256"].with_(T=500, d=256, E=12, f=128, name="e12"), [2, 2, 1, 1, 6]),
     "multi_cta_dispatch": (WORKLOADS["mixtral_T256"].with_(T=20000, d=256, E=16, f=128, name="n40000"),
                            [1, 4, 1, 1, 7]),

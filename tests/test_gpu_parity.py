@@ -61,6 +61,8 @@ SMALL_TC = {
     "t1": WORKLOADS["mixtral_T16"].with_(T=1, d=128, f=64, name="t1"),
     # few token tiles and a long d: the router splits K over CTAs and selects per warp
     "sigmoid_top8_splitk": WORKLOADS["deepseek_v3"].with_(T=200, d=2048, f=128, f_shared=128, name="sig8_split"),
+    # 47 token tiles: clusters of 3 K splits, each CTA selecting 43 of its tile's rows
+    "sigmoid_top8_split3": WORKLOADS["deepseek_v3"].with_(T=6000, d=1024, f=128, f_shared=128, name="sig8_split3"),
     # W_r read in place by the tensor-core router: two 64-expert chunks (E = 128), and
     # E = 24 (a multiple of 8, not of 64: the chunk past E is zero-filled); E = 12 is
     # not a multiple of 8 and takes the transposed copy of W_r

@@ -52,7 +52,7 @@ class Workload:
     ec_capacity: int = 0           # expert choice: tokens per expert
     n_shared: int = 0
     f_shared: int = 0
-    dtype: str = "bf16"            # "f32" | "bf16" | "fp8w" (bf16 tensors; the library stores FP8 weights)
+    dtype: str = "bf16"            # "f32" | "bf16" | "fp8w" | "fp8up" (bf16 tensors; the library quantises)
     drop_policy: str = "token"     # capacity drop: "token" order or "affinity" (largest gate weights kept)
     logit_offsets: str = "none"    # "none" | "normal_var0.5" | "zipf1.1"
     sel_bias: str = "none"         # "none" | "uniform0.1"
