@@ -52,6 +52,8 @@ STAGES = ("route", "dispatch", "ffn", "combine")
 # workloads of the per_config table (the headline's own is skipped there)
 PER_CONFIG = ("tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T16", "mixtral_T256", "mixtral_T4096",
               "mixtral_T16384", "deepseek_v3", "expert_choice_zipf")
+# the same layers with the up projection on E4M3 operands (MOE_BF16_FP8UP), beside them
+PER_CONFIG_FP8UP = ("switch_top1_cap1.25", "mixtral_T4096", "mixtral_T16384", "deepseek_v3")
 KERNEL_SOURCES = {   # files whose content defines each stage's kernels (for the ncu traffic record)
     "ffn": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
     "route": ["csrc/route.cu", "csrc/route_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
@@ -76,7 +78,9 @@ def layer_config(wl, ws_n):
     return {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "d_ff": wl.f, "k": wl.k, "gate": wl.gate,
             "mode": wl.mode, "capacity_factor": wl.capacity_factor, "ec_capacity": wl.ec_capacity,
             "n_shared": wl.n_shared, "f_shared": wl.f_shared,
-            "expert_weights": "e4m3 + fp32 scale per output channel" if wl.dtype == "fp8w" else wl.dtype,
+            "expert_weights": {"fp8w": "e4m3 + fp32 scale per output channel",
+                               "fp8up": "W1|W3 e4m3 + scale per channel, x e4m3 + scale per token, W2 bf16"}.get(
+                                   wl.dtype, wl.dtype),
             "drop_policy": wl.drop_policy,
             "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU"}
 
@@ -208,6 +212,7 @@ def work_model(wl, off, E_used):
     A = assignments computed; touched = experts with at least one row."""
     b = 4 if wl.dtype == "f32" else 2
     bw = 1 if wl.dtype == "fp8w" else b   # bytes per stored expert weight (E4M3 codes)
+    up8 = wl.dtype == "fp8up"             # E4M3 up projection: W1|W3 one byte, W2 bf16
     T, d, E, f = wl.T, wl.d, wl.E, wl.f
     A = int(off[-1])
     touched = int(E_used)
@@ -226,6 +231,14 @@ def work_model(wl, off, E_used):
     m["ffn"] = {"bytes": touched * (3 * d * f * bw + sc) + 2 * A * d * b + 2 * A * f * b
                          + (3 * d * fs * bw + scs + 2 * Ts * d * b + 2 * Ts * fs * b),
                 "flops": 6 * A * d * f + 6 * Ts * d * fs}
+    if up8:
+        # weights: E4M3 W1|W3 + one scale per column, bf16 W2; rows: the stage quantises
+        # x_perm (and x) to E4M3 (read bf16, write codes), the up tiles read the codes
+        m["ffn"]["bytes"] = (touched * (2 * d * f + 4 * 2 * f + d * f * 2) + A * d * (2 + 1 + 1) + 2 * A * f * 2
+                             + A * d * 2 + (2 * d * fs + 4 * 2 * fs + d * fs * 2 + Ts * d * (2 + 1 + 1)
+                                            + 2 * Ts * fs * 2 + Ts * d * 2))
+        # the up FLOPs run at twice the bf16 rate: their bf16-equivalent count is half
+        m["ffn"]["flops_bf16_equiv"] = 4 * A * d * f + 4 * Ts * d * fs
     m["combine"] = {"bytes": A * d * b + T * kslots * 8 + T * d * b + Ts * d * b, "flops": 2 * A * d}
     return m, A, touched
 
@@ -360,7 +373,7 @@ def stage_table(stage_s, model, peaks):
 
 def layer_roofline_ms(model, peaks):
     layer_bytes = sum(model[s]["bytes"] for s in STAGES)
-    flops = model["ffn"]["flops"]
+    flops = model["ffn"].get("flops_bf16_equiv", model["ffn"]["flops"])
     return max(flops / (peaks["bf16_tflops"] * 1e12), layer_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e3, layer_bytes
 
 
@@ -423,6 +436,8 @@ def run_gpu(args):
         wl = wl.with_(T=args.T)
     if args.fp8_weights:
         wl = wl.with_(dtype="fp8w")
+    if args.fp8_up:
+        wl = wl.with_(dtype="fp8up")
     if args.affinity_drop:
         wl = wl.with_(drop_policy="affinity")
     if ws_n > 1:   # each replica gets its own batch of tokens
@@ -597,7 +612,7 @@ def run_gpu(args):
     roof["kernel"] = dom
     roof["peak_source"] = (f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'}), "
                            f"{peak_kind}")
-    roof["traffic"] = recorded_traffic(dom, wl.name)
+    roof["traffic"] = recorded_traffic(dom, wl.name + {"fp8up": "+fp8up", "fp8w": "+fp8w"}.get(wl.dtype, ""))
     roof["algorithmic_bytes_per_launch"] = model[dom]["bytes"]
     roof["algorithmic_flops_per_launch"] = model[dom]["flops"]
 
@@ -617,7 +632,8 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": {"bf16": "bf16", "f32": "f32", "fp8w": "bf16 (E4M3 expert weights)"}[wl.dtype],
+        "dtype": {"bf16": "bf16", "f32": "f32", "fp8w": "bf16 (E4M3 expert weights)",
+                  "fp8up": "bf16 (E4M3 up projection)"}[wl.dtype],
         "data": "synthetic (seeded; random-init expert weights)",
         "config": {**layer_config(wl, ws_n),
                    "assignments_computed": A, "experts_touched": touched,
@@ -660,10 +676,18 @@ def run_gpu(args):
             except Exception as ex:   # report, keep the headline
                 per[name] = {"error": str(ex).splitlines()[0][:200]}
                 torch.cuda.empty_cache()
+        for name in PER_CONFIG_FP8UP:
+            key = name + "+fp8up"
+            try:
+                per[key] = measure_config(WORKLOADS[name].with_(dtype="fp8up"), dev, peaks, clocks)
+            except Exception as ex:   # report, keep the headline
+                per[key] = {"error": str(ex).splitlines()[0][:200]}
+                torch.cuda.empty_cache()
         out["per_config"] = {"method": "moe_forward timed over about 0.4 s of steps (CUDA events); stages from "
                                        "CUDA-graph replays of 10 calls; fractions of MEASURED_PEAKS.json "
                                        "(burst bf16, copy bandwidth); sm_mhz = median nvidia-smi SM clock "
-                                       "during the forward loop", **per}
+                                       "during the forward loop; '+fp8up' = the same layer with the up "
+                                       "projection on E4M3 operands (MOE_BF16_FP8UP)", **per}
     clocks.close()
     if ws_n > 1:
         dist.destroy_process_group()
@@ -684,6 +708,10 @@ def run_stage(args):
     wl = WORKLOADS[args.workload]
     if args.T:
         wl = wl.with_(T=args.T)
+    if args.fp8_weights:
+        wl = wl.with_(dtype="fp8w")
+    if args.fp8_up:
+        wl = wl.with_(dtype="fp8up")
     S = args.stage
     st = torch.cuda.current_stream()
     cfg = B.config_from_workload(wl)
@@ -870,6 +898,8 @@ def main():
                     help="capacity drop by descending gate weight (DeepSeek-V2) instead of token order")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="store the expert weights as FP8 E4M3 with per-channel scales (MOE_BF16_FP8W)")
+    ap.add_argument("--fp8-up", action="store_true",
+                    help="run the up projection on E4M3 activations and weights (MOE_BF16_FP8UP)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

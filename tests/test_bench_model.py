@@ -46,3 +46,15 @@ def test_fp8_weights_halve_the_weight_bytes():
     weights16 = 64 * 3 * 1024 * 4096 * 2
     weights8 = 64 * (3 * 1024 * 4096 + 4 * (2 * 4096 + 1024))   # E4M3 codes + one fp32 scale per output channel
     assert m16["ffn"]["bytes"] - m8["ffn"]["bytes"] == weights16 - weights8
+
+
+def test_fp8_up_projection_weight_bytes():
+    # E4M3 W1|W3 with one fp32 scale per hidden column of each, bf16 W2
+    m16, _, _ = _switch_model("bf16")
+    m8, _, _ = _switch_model("fp8up")
+    up16, up8 = 64 * 2 * 1024 * 4096 * 2, 64 * (2 * 1024 * 4096 + 4 * 2 * 4096)
+    rows16 = 2 * 8168 * 1024 * 2                           # x_perm read, Y written (bf16)
+    rows8 = 8168 * 1024 * (2 + 1 + 1) + 8168 * 1024 * 2    # quantised (read, write codes, read codes), Y
+    assert m16["ffn"]["bytes"] - m8["ffn"]["bytes"] == (up16 - up8) + (rows16 - rows8)
+    # the up projection's FLOPs count half at the FP8 rate
+    assert m8["ffn"]["flops_bf16_equiv"] == 4 * 8168 * 1024 * 4096
