@@ -357,6 +357,51 @@ def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
         assert rel_err(Yn[T * k:], sref) <= TOL[dt]
 
 
+# Long segments (at least 512 buffer rows per expert) run the fused launch on CTA
+# pairs: M = 256 MMAs over two consecutive 128-row M tiles of a segment.  The
+# segment sizes put a lone last M tile in a pair (1, 257 rows), a second tile of
+# one row (129, 385), a segment of exactly one pair (256) and none (0); the shared
+# segment spans several pairs.  Every row is compared with the oracle.
+PAIR_CASES = [
+    # T, d, f, f_shared, counts of the 8 routed experts
+    (2048, 256, 256, 128, [0, 1, 128, 129, 256, 257, 385, 700]),
+    (2048, 1024, 512, 256, [700, 385, 257, 1, 0, 129, 256, 128]),
+]
+
+
+@pytest.mark.parametrize("T,d,f,fs,counts", PAIR_CASES)
+def test_grouped_ffn_pairs(T, d, f, fs, counts, cuda_device):
+    E, k = 8, 2
+    A = int(sum(counts))
+    assert T * k // E >= 512 and A <= T * k
+    cfg = B.config(T=T, d=d, E=E, f=f, k=k, n_shared=1, f_shared=fs)
+    g = torch.Generator(device="cpu").manual_seed(9090 + d)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).bfloat16()
+    Ws = [(torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, fs, d, generator=g) / fs ** 0.5).bfloat16()]
+    off = np.zeros(E + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    x_perm = torch.zeros(T * k, d, dtype=torch.bfloat16)
+    x_perm[:A] = random_rows(A, d, seed=91 + d, dtype=torch.bfloat16)
+    x = random_rows(T, d, seed=92 + d, dtype=torch.bfloat16)
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    for _ in range(2):   # twice: the second call reuses the workspace and its counters
+        Y = layer.grouped_ffn(x_perm.to(dev), torch.from_numpy(off).to(dev), x.to(dev))
+        _check_device_error()
+        Yn = _np(Y)
+        for e in range(E):
+            a, b = int(off[e]), int(off[e + 1])
+            if b > a:
+                ref = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
+                assert rel_err(Yn[a:b], ref) <= TOL["bf16"], f"expert {e} ({b - a} rows)"
+        sref = oracle.expert_rows(x, Ws[0][0], Ws[1][0], Ws[2][0], nthreads=NTH)
+        assert rel_err(Yn[T * k:], sref) <= TOL["bf16"]
+
+
 # The fine-grained layout at its widest: 256 routed experts plus one shared expert
 # (257 segments) with small d and f, so that every row of every segment can be
 # compared with the oracle.  The segment sizes are seeded and skewed and include
@@ -613,6 +658,16 @@ E2E_SMALL = {
     "small_k_eq_E": WORKLOADS["mixtral_T256"].with_(T=200, d=256, E=4, k=4, f=128, name="small_k_eq_E"),
     "small_dense_E1": WORKLOADS["mixtral_T256"].with_(T=130, d=256, E=1, k=1, f=256, name="small_dense_E1"),
     "small_one_token": WORKLOADS["mixtral_T16"].with_(T=1, d=256, f=128, name="small_one_token"),
+    # at least 512 buffer rows per expert: the fused expert FFN runs on CTA pairs
+    # (top-2 softmax; capacity with the gated down store of k = 1; sigmoid + shared;
+    # Expert Choice)
+    "small_pairs_top2": WORKLOADS["mixtral_T256"].with_(T=2048, d=256, f=256, name="small_pairs_top2"),
+    "small_pairs_switch": WORKLOADS["switch_top1_cap1.25"].with_(T=4096, d=256, E=8, f=256,
+                                                                  logit_offsets="normal_var0.5",
+                                                                  name="small_pairs_switch"),
+    "small_pairs_shared": WORKLOADS["deepseek_v3"].with_(T=2048, d=256, E=8, k=2, f=128, f_shared=128,
+                                                          name="small_pairs_shared"),
+    "small_pairs_ec": WORKLOADS["expert_choice_zipf"].with_(T=1024, d=256, E=4, f=256, name="small_pairs_ec"),
 }
 
 
