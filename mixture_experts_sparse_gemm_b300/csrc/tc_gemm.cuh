@@ -1147,10 +1147,11 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
 
 // CTA-pair launch (clusters of two, M = 256 MMAs): as many pairs as can be resident
 // at once (at most half the SMs, at most max_tiles).  B comes from the tile images
-// through b0 (a map of 128-byte rows from args.wbase).  A kEpiFfn launch is
-// cooperative when the runtime accepts that together with clusters; otherwise
-// every pair is still resident (the grid is sized to the resident count) and the
-// bounded waits report a pair that never ran.
+// through b0 (a map of 128-byte rows from args.wbase).  The launch is a plain
+// cluster launch (the profiler does not replay a cooperative cluster launch): the
+// grid is the resident count, so on a GPU that runs nothing else every pair of a
+// kEpiFfn launch is resident at once, and if one is not, the bounded waits of the
+// down tiles report it instead of waiting for it.
 template <int BN, int EPI>
 cudaError_t launch_gemm_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &a2,
                              const CUtensorMap &a3, const TcArgs &args_in, int64_t max_tiles, cudaStream_t s) {
@@ -1165,14 +1166,8 @@ cudaError_t launch_gemm_pair(const CUtensorMap &a0, const CUtensorMap &a1, const
     if (pairs <= 0) return cudaErrorInvalidConfiguration;
     pairs = std::min(pairs, num_sms() / 2);
     if (max_tiles < pairs) pairs = (int)(max_tiles > 1 ? max_tiles : 1);
-    err = launch_dependent_cluster(kern, dim3(2 * pairs), dim3(C::kThreadsCta), smem, s, 2, EPI == kEpiFfn, a0, a1, b0,
-                                   b0, a2, a3, args);
-    if (err != cudaSuccess && EPI == kEpiFfn) {
-        (void)cudaGetLastError();
-        err = launch_dependent_cluster(kern, dim3(2 * pairs), dim3(C::kThreadsCta), smem, s, 2, false, a0, a1, b0, b0,
-                                       a2, a3, args);
-    }
-    return err;
+    return launch_dependent_cluster(kern, dim3(2 * pairs), dim3(C::kThreadsCta), smem, s, 2, false, a0, a1, b0, b0,
+                                    a2, a3, args);
 }
 
 // Cluster-reduced split-K router (kEpiSplitRoute + KPL): one CTA per (token tile,
