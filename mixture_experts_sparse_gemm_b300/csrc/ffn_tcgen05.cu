@@ -98,18 +98,6 @@ bool down_gemm(const moe_config &c, const Sizes &z, const void *H, const void *H
     return ok;
 }
 
-// CTA pairs (M = 256 MMAs, each CTA copying half of every weight tile) for the
-// fused bf16 launch when the experts' segments are long: at least this many
-// routed rows per expert on average (buffer rows / E).  Short segments would leave
-// half of many pairs idle (a lone last M tile still occupies both CTAs).
-#ifndef MOE_PAIR_MIN_ROWS
-#define MOE_PAIR_MIN_ROWS 512
-#endif
-
-bool use_pairs(const moe_config &c, const Sizes &z) {
-    return !fp8_weights(c) && !fp8_up(c) && c.E > 0 && z.rows_routed / c.E >= MOE_PAIR_MIN_ROWS;
-}
-
 // Upper bound on the M tiles of a launch (real count is known on the device only).
 int64_t max_mtiles(const moe_config &c, const Sizes &z) {
     return (z.rows_routed + kBM - 1) / kBM + c.E + (c.n_shared > 0 ? (c.T + kBM - 1) / kBM : 0);
@@ -168,16 +156,6 @@ cudaError_t launch_ffn_fused_tcgen05(const moe_config &c, const Sizes &z, const 
         if (e != cudaSuccess) return e;
     }
     const int64_t tiles = max_mtiles(c, z) * (g.p[0].g.nblk_routed + g.p[1].g.nblk_routed);
-    if (use_pairs(c, z)) {
-        // every tile image (up and down, routed and shared) lies in [w13, sc13) of the
-        // packed weights; 128-byte rows of it are the B copies of the CTA pairs
-        const PackedLayout L = packed_layout(c);
-        const uint8_t *pk = static_cast<const uint8_t *>(packed);
-        CUtensorMap wmap;
-        if (!make_tmap_rows128(&wmap, pk + L.w13, (uint64_t)(L.sc13 - L.w13) / 128)) return cudaErrorInvalidValue;
-        g.wbase = pk + L.w13;
-        return launch_gemm_pair<256, kEpiFfn>(mu.a0, mu.a1, wmap, md.a0, md.a1, g, tiles, s);
-    }
     if (fp8_weights(c)) return launch_gemm<256, kEpiFfn, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
     if (f8) return launch_gemm<256, kEpiFfn, false, true>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);
     return launch_gemm<256, kEpiFfn>(mu.a0, mu.a1, mu.a0, mu.a1, md.a0, md.a1, g, tiles, s);

@@ -357,21 +357,6 @@ bool make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t c
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Packed tile images read as rows of 128 bytes ([rows][64] bf16), boxes of 128 rows
-// copied verbatim (the images carry their 128-byte swizzle already).
-bool make_tmap_rows128(CUtensorMap *map, const void *ptr, uint64_t rows) {
-    EncodeTiledFn encode = tmap_encoder();
-    if (!encode) return false;
-    if (rows == 0) rows = 1;
-    const cuuint64_t dims[2] = {64, rows};
-    const cuuint64_t strides[1] = {128};
-    const cuuint32_t box[2] = {64, 128};
-    const cuuint32_t estr[2] = {1, 1};
-    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace moe
 
 using namespace moe;

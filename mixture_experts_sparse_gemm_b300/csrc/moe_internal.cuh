@@ -249,56 +249,25 @@ cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size
 }
 
 // A dependent launch (as above) of thread-block clusters of `cluster` CTAs along x
-// (gridDim.x a multiple of it), cooperative on request.
+// (gridDim.x a multiple of it).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_dependent_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                     int cluster, bool cooperative, Args &&...args) {
+                                     int cluster, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[3];
-    unsigned n = 0;
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-    attr[n].id = cudaLaunchAttributeClusterDimension;
-    attr[n].val.clusterDim.x = (unsigned)cluster;
-    attr[n].val.clusterDim.y = 1;
-    attr[n].val.clusterDim.z = 1;
-    ++n;
-    if (cooperative) {
-        attr[n].id = cudaLaunchAttributeCooperative;
-        attr[n].val.cooperative = 1;
-        ++n;
-    }
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = n;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
-// Clusters of `cluster` CTAs of `kern` (block threads, smem bytes) that can be
-// resident at once, 0 when the query fails.
-template <typename... KArgs>
-int max_active_clusters(void (*kern)(KArgs...), dim3 block, size_t smem, int cluster) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)cluster * 64u);
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
 }
 
 // ----------------------------------------------------------------------------- device helpers
@@ -358,7 +327,9 @@ __device__ __forceinline__ int build_tile_table(const GroupedShape &g, int *tile
     return S;
 }
 
-template <int BM>
+// GM > 0: the M blocks of a segment are taken in groups of GM, and a group's tiles
+// (every N block of it, M fastest) all come before the next group's.
+template <int BM, int GM = 0>
 __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *tile_start, const int *seg_rows,
                                             int S, int tile, int &s, int &mb, int &nb) {
     int lo = 0, hi = S - 1;   // last s with tile_start[s] <= tile
@@ -369,8 +340,16 @@ __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *ti
     s = lo;
     const int local = tile - tile_start[s];
     const int mblk = (seg_rows[s] + BM - 1) / BM;
-    mb = local % mblk;
-    nb = local / mblk;
+    if constexpr (GM > 0) {
+        const int nblk = (s < g.E) ? g.nblk_routed : g.nblk_shared;
+        const int grp = local / (GM * nblk), rem = local - grp * GM * nblk;
+        const int gm = min(GM, mblk - grp * GM);   // the last group may be short
+        mb = grp * GM + rem % gm;
+        nb = rem / gm;
+    } else {
+        mb = local % mblk;
+        nb = local / mblk;
+    }
 }
 
 }  // namespace moe

@@ -56,34 +56,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// The same with acquire at cluster scope: the phase was completed by arrivals of
-// the other CTA of a pair (release at cluster scope) or by its copies.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Wait for the phase of parity `parity` to complete.  Returns false when the CTA
 // aborts (another role gave up) or when this wait itself gives up after
-// `limit_ns` (then it records the timeout and raises the abort flag).  CLUSTER:
-// acquire at cluster scope.
-template <bool CLUSTER = false>
+// `limit_ns` (then it records the timeout and raises the abort flag).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              unsigned *err, uint64_t limit_ns) {
-    auto try_wait = [](uint32_t b, uint32_t p) {
-        return CLUSTER ? mbar_try_wait_cluster(b, p) : mbar_try_wait(b, p);
-    };
-    if (try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > limit_ns) {
@@ -182,53 +163,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// ---------------------------------------------------------------- tcgen05, CTA pair
-// A pair of CTAs (ranks 0 and 1 of a cluster of two) runs one MMA of M = 256: each
-// CTA holds 128 rows of A and half the N rows of B in its shared memory at the
-// same offsets, and 128 rows x N columns of D in its own TMEM.  Rank 0 issues the
-// MMAs; allocation and release of TMEM are collective over the pair.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t holder, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish_pair() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                              uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on the mbarrier at offset `bar` of both CTAs of the pair once every
-// tcgen05 operation issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"((uint16_t)3)
-        : "memory");
-}
-// 2-D tiled TMA load into this CTA's shared memory that completes (complete_tx) on
-// an mbarrier of either CTA of the pair (`bar` is a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                                 uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-        "%3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-// arrive (release at cluster scope) on an mbarrier given by its shared::cluster address
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 // 32 TMEM lanes x 16 consecutive 32-bit columns: lane i of the warp gets row
 // (lane base + i), columns [col, col + 16).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
@@ -291,8 +225,6 @@ constexpr uint32_t kIdescBMajorMN = 1u << 16;
 
 // host: 2-D bf16 tensor map [rows][cols] row-major, box = [box_rows][64], 128-byte swizzle
 bool make_tmap_bf16(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
-// host: packed tile images as [rows][64] bf16 (128-byte rows), box = 128 rows, no swizzle
-bool make_tmap_rows128(CUtensorMap *map, const void *ptr, uint64_t rows);
 // host: 2-D one-byte (E4M3 codes) tensor map [rows][cols], box = [box_rows][128], 128-byte swizzle
 bool make_tmap_u8(CUtensorMap *map, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_rows);
 

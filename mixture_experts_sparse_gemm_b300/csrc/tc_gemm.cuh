@@ -16,12 +16,6 @@
 //               ahead of the MMA (warp 0 then brings only A, into its own ring)
 //   warps 6..15 (split-K router only) selection warps, idle until the tile's
 //               partial logits are reduced across the cluster
-// PAIR instantiations (fused bf16 expert FFN on long segments) run as clusters of
-// two CTAs: a tile is two consecutive 128-row M tiles of a segment, rank r of the
-// pair computes M tile 2 mb + r, each CTA copies its A rows and half of the weight
-// tile into its own ring (both copies complete on rank 0's barrier), and rank 0
-// issues tcgen05.mma.cta_group::2 (M = 256) whose commits arrive on both CTAs'
-// barriers; each CTA's epilogue drains its own TMEM.
 // F8A instantiations run the tiles of a GEMM marked a_f8 (the up projection) on
 // E4M3 operands: kind::f8f6f4 MMAs of K = 32, a k block of 128 one-byte elements
 // (the same 128-byte swizzled rows as a bf16 block of 64), and the epilogue scales
@@ -48,8 +42,6 @@
 #include <cuda_fp16.h>
 #include <float.h>
 
-#include <algorithm>
-
 #include "route_common.cuh"
 #include "tc_common.cuh"
 
@@ -60,6 +52,12 @@ using namespace tc;
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
+// Expert GEMM tile order: a segment's M tiles in groups of 16, each group's tiles
+// (all N blocks, M fastest) before the next group's.  The ~148 tiles in flight then
+// cover at most 16 M tiles of one expert, whose A rows (the down projection's H:
+// 16 x 128 rows of f bf16, 59 MB at f = 14336) stay in L2 while every N block
+// reads them; a segment of up to 16 M tiles keeps the plain M-fastest order.
+constexpr int kTileGroupM = 16;
 constexpr int kThreads = 192;
 constexpr int kEpiSwiGLU = 0;   // up projection (+ SwiGLU)
 constexpr int kEpiStore = 1;    // down projection (optionally gated, see TcArgs::gated)
@@ -84,16 +82,13 @@ constexpr int kSplitSelectWarps = 10;   // extra warps of a split-K router CTA (
 // Shared memory: stages (bf16: A | B; W8: A) | W8: bf16 B buffers | W8: FP8 slots.
 // EXTRA: warps beyond the GEMM roles (the cluster-reduced split-K router adds
 // kSplitSelectWarps that only take part in its selection phase).
-// PAIR: CTA pairs (clusters of two) running M = 256 MMAs; a stage holds this CTA's
-// 128 rows of A and half (BN / 2 rows) of the B tile.
-template <int BN, bool W8 = false, int EXTRA = 0, bool PAIR = false>
+template <int BN, bool W8 = false, int EXTRA = 0>
 struct TcCfg {
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = BN * kBK * 2;      // bf16 B tile, as the MMA reads it
     static constexpr int kB8Bytes = BN * kBK;         // FP8 B tile, as the copy brings it (W8)
-    static constexpr int kBStage = PAIR ? kBBytes / 2 : kBBytes;   // B bytes of a stage in this CTA
-    static constexpr int kStageBytes = kABytes + (W8 ? 0 : kBStage);
-    static constexpr int kStages = PAIR ? 6 : (W8 ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8)));
+    static constexpr int kStageBytes = kABytes + (W8 ? 0 : kBBytes);
+    static constexpr int kStages = W8 ? 3 : ((BN == 256) ? 4 : (BN == 128 ? 6 : 8));
     static constexpr int kBBufs = W8 ? 3 : 0;         // bf16 B buffers (W8)
     static constexpr int kB8Stages = W8 ? 4 : 0;      // FP8 ring slots
     static constexpr int kConvWarps = W8 ? 12 : 0;
@@ -163,9 +158,6 @@ struct TcArgs {
     RouteEpi route;
     unsigned *err;
     uint64_t wait_ns;     // limit of every bounded wait (set by launch_gemm)
-    // CTA-pair launches: the tile images are copied through the tensor map tmB0 of
-    // 128-byte rows starting at wbase (both phases' images lie in one allocation)
-    const uint8_t *wbase;
 };
 
 // SiLU(z) = z / (1 + e^-z) with the fast exponential and division (the result is
@@ -534,19 +526,17 @@ struct TileAt {
     int phase, s, mb, nb;
 };
 
-template <int BN, int EPI, bool W8, bool F8A = false, bool PAIR = false>
-__global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0, PAIR>::kThreadsCta, 1)
+template <int BN, int EPI, bool W8, bool F8A = false>
+__global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0>::kThreadsCta, 1)
     tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                            const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmA3,
                            TcArgs a) {
-    using C = TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0, PAIR>;
+    using C = TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0>;
     constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
-    static_assert(!PAIR || (BN == 256 && !W8 && !F8A && EPI <= kEpiFfn), "CTA pairs: bf16 expert GEMMs");
-    // rows of A one tile covers: a CTA pair takes two consecutive M tiles of a segment
-    constexpr int kTileRows = PAIR ? 2 * kBM : kBM;
-    // PAIR: rank in the pair; rank 0 issues the MMAs and holds the stage barriers
-    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+    // expert GEMMs take a segment's M tiles in groups of kTileGroupM (the router's
+    // tile order is its K split layout and stays as it is)
+    constexpr int kTileGroup = (EPI <= kEpiFfn) ? kTileGroupM : 0;
     constexpr bool kRouter = EPI >= kEpiPartial;   // router launches may read B (W_r) MN-major
     constexpr bool kFusedRoute = EPI > kEpiRoute && EPI < kEpiSplitRoute;
     constexpr bool kSplitRoute = EPI > kEpiSplitRoute;
@@ -586,7 +576,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull[i]), 1);
-            mbar_init(smem_u32(&tempty[i]), PAIR ? 8 : 4);   // PAIR: the epilogue warps of both CTAs
+            mbar_init(smem_u32(&tempty[i]), 4);
         }
         mbar_init(smem_u32(drain), 1);
         if (W8) {
@@ -603,7 +593,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
         fence_mbarrier_init();
         prefetch_tmap(&tmA0);
         prefetch_tmap(&tmA1);
-        if (a.p[0].Bt0 == nullptr || PAIR) {
+        if (a.p[0].Bt0 == nullptr) {
             prefetch_tmap(&tmB0);
             prefetch_tmap(&tmB1);
         }
@@ -613,22 +603,16 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
         }
     }
     if (warp == 1) {
-        if constexpr (PAIR) {
-            tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
-            tmem_relinquish_pair();
-        } else {
-            tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
-            tmem_relinquish();
-        }
+        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+        tmem_relinquish();
         fence_before();
     }
     __syncthreads();
-    if constexpr (PAIR) cluster_sync();   // both CTAs' barriers are initialised before any remote use
     fence_after();
     pdl_wait();      // the previous kernel's outputs (segment offsets, A rows) are visible from here on
     pdl_trigger();
     const uint32_t tmem_base = *tmem_holder;
-    const int S = build_tile_table<kTileRows>(a.p[0].g, tile_start0, seg_row0, seg_rows);
+    const int S = build_tile_table<kBM>(a.p[0].g, tile_start0, seg_row0, seg_rows);
     const int total0 = tile_start0[S];
     int total = total0;
     if (kPhases == 2) {
@@ -636,10 +620,9 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             int t1 = 0, m = 0;
             for (int s = 0; s < S; ++s) {
                 const int mblk = (seg_rows[s] + kBM - 1) / kBM;
-                const int tblk = (seg_rows[s] + kTileRows - 1) / kTileRows;
                 tile_start1[s] = t1;
-                mtile_start[s] = m;   // one dependency counter per 128-row M tile
-                t1 += tblk * ((s < a.p[1].g.E) ? a.p[1].g.nblk_routed : a.p[1].g.nblk_shared);
+                mtile_start[s] = m;
+                t1 += mblk * ((s < a.p[1].g.E) ? a.p[1].g.nblk_routed : a.p[1].g.nblk_shared);
                 m += mblk;
             }
             tile_start1[S] = t1;
@@ -653,10 +636,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
     // take the K splits of one token tile: split = rank, M block = block / splits.
     const int mblk0 = (seg_rows[0] + kBM - 1) / kBM;
     int tile0 = blockIdx.x, tstep = gridDim.x;
-    if constexpr (PAIR) {   // a pair (cluster of two consecutive blocks) takes each tile
-        tile0 = blockIdx.x >> 1;
-        tstep = gridDim.x >> 1;
-    }
     if constexpr (kSplitRoute) {
         const int splits = a.p[0].ksplit;
         tile0 = (int)(blockIdx.x % splits) * mblk0 + (int)(blockIdx.x / splits);
@@ -681,19 +660,13 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
         TileAt t;
         if (kPhases == 2 && tile >= total0) {
             t.phase = 1;
-            decode_tile<kTileRows>(a.p[1].g, tile_start1, seg_rows, S, tile - total0, t.s, t.mb, t.nb);
+            decode_tile<kBM, kTileGroup>(a.p[1].g, tile_start1, seg_rows, S, tile - total0, t.s, t.mb, t.nb);
         } else {
             t.phase = 0;
-            decode_tile<kTileRows>(a.p[0].g, tile_start0, seg_rows, S, tile, t.s, t.mb, t.nb);
+            decode_tile<kBM, kTileGroup>(a.p[0].g, tile_start0, seg_rows, S, tile, t.s, t.mb, t.nb);
         }
         return t;
     };
-    // the 128-row M tile of the segment that this CTA computes in a tile (PAIR: rank
-    // 1's may lie past the segment's end: its rows are computed and never stored)
-    auto my_mtile = [&](const TileAt &t) { return PAIR ? 2 * t.mb + (int)crank : t.mb; };
-    // a finished up tile adds kDepPerTile to the counter of its M tile (PAIR: each
-    // epilogue warp adds 1 for its 32 rows)
-    constexpr int kDepPerTile = PAIR ? 4 : 1;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -706,12 +679,11 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                 const TileAt t = locate(tile);
                 const TcGemm &G = a.p[t.phase];
                 const bool routed = t.s < G.g.E;
-                const int mt = my_mtile(t);
-                if (kPhases == 2 && t.phase == 1 && mt * kBM < seg_rows[t.s]) {
+                if (kPhases == 2 && t.phase == 1) {
                     // H rows of this (segment, M tile) come from the up tiles: wait until all
                     // of them have published (release/acquire through dep), bounded
-                    const int need = kDepPerTile * (routed ? a.p[0].g.nblk_routed : a.p[0].g.nblk_shared);
-                    if (!wait_counter_bounded(a.dep + mtile_start[t.s] + mt, need, abort_flag, a.err, a.wait_ns)) {
+                    const int need = routed ? a.p[0].g.nblk_routed : a.p[0].g.nblk_shared;
+                    if (!wait_counter_bounded(a.dep + mtile_start[t.s] + t.mb, need, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -719,7 +691,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                 }
                 const CUtensorMap *mA = (t.phase == 0) ? (routed ? &tmA0 : &tmA1) : (routed ? &tmA2 : &tmA3);
                 const CUtensorMap *mB = routed ? &tmB0 : &tmB1;
-                const int arow = seg_row0[t.s] + mt * kBM;
+                const int arow = seg_row0[t.s] + t.mb * kBM;
                 const int brow = (routed ? t.s * G.b_rows0 : 0) + (G.ksplit > 1 ? 0 : t.nb * BN);
                 int kb0, nk;
                 krange(t, G, kb0, nk);
@@ -747,17 +719,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                     }
                     const uint32_t fb = smem_u32(&full[stage]);
                     uint8_t *st = tiles + (size_t)stage * C::kStageBytes;
-                    if constexpr (PAIR) {
-                        // both CTAs' copies complete on rank 0's barrier, which expects the
-                        // bytes of both: A rows of this CTA's M tile and its half of the B
-                        // tile (image rows [crank * BN/2, +BN/2), 128 bytes each)
-                        const uint32_t fb0 = mapa_shared(fb, 0);
-                        if (crank == 0) mbar_arrive_expect_tx(fb, 2 * C::kStageBytes);
-                        tma_load_2d_pair(smem_u32(st), mA, (kb0 + kb) * kBK, arow, fb0);
-                        const int wrow = (int)((size_t)(bt + (size_t)(kb0 + kb) * img_bytes - a.wbase) >> 7) +
-                                         (int)crank * (BN / 2);
-                        tma_load_2d_pair(smem_u32(st + C::kABytes), &tmB0, 0, wrow, fb0);
-                    } else {
                     mbar_arrive_expect_tx(fb, C::kABytes + (W8 ? 0 : kBCopy));   // A + B (W8: A only)
                     tma_load_2d(smem_u32(st), mA, (kb0 + kb) * (tile_f8(t) ? 128 : kBK), arow, fb);
                     if (W8)
@@ -770,7 +731,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                                         (G.ksplit > 1 ? 0 : t.nb * BN) + 64 * j, (kb0 + kb) * kBK, fb);
                     else
                         tma_load_2d(smem_u32(st + C::kABytes), mB, (kb0 + kb) * kBK, brow, fb);
-                    }
                     ++issued;
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -778,38 +738,27 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                     }
                 }
             }
-            // leave no copy in flight: wait (bounded) for the last stages issued to land.
-            // PAIR rank 1's copies complete on rank 0's barriers, so it waits (always)
-            // until the MMA has consumed them; rank 0 outlives every MMA.
-            const bool peer = PAIR && crank != 0;
-            if (!ok || peer) {
+            if (!ok) {
+                // leave no copy in flight: wait (bounded) for the last stages issued
                 const int n = issued < C::kStages ? issued : C::kStages;
                 int st = stage;
                 uint32_t ph = phase;
-                const uint64_t t0 = globaltimer();
                 for (int i = 0; i < n; ++i) {
                     if (--st < 0) {
                         st = C::kStages - 1;
                         ph ^= 1u;
                     }
-                    const uint32_t fb = smem_u32(peer ? &empty[st] : &full[st]);
+                    const uint32_t fb = smem_u32(&full[st]);
+                    const uint64_t t0 = globaltimer();
                     while (!mbar_try_wait(fb, ph) && globaltimer() - t0 < kDrainLimitNs) {
                     }
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && crank == 0) {
+        if (lane == 0) {
             // ------------------------------------------------------------ MMA issuer
-            // (PAIR: rank 0 only, M = 256 over both CTAs; every commit arrives on the
-            // barrier in both CTAs)
-            constexpr uint32_t kIdesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, BN);
-            auto commit = [](uint32_t bar) {
-                if constexpr (PAIR)
-                    mma_commit_pair(bar);
-                else
-                    mma_commit(bar);
-            };
+            constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, BN);
             constexpr uint32_t kIdescF8 = idesc_e4m3_f32(kBM, BN);
             int stage = 0;
             uint32_t phase = 0;
@@ -825,14 +774,14 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                 const bool f8 = tile_f8(t);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-                if (!wait_bounded<PAIR>(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
+                if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, a.err, a.wait_ns)) {
                     ok = false;
                     break;
                 }
                 fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = 0; kb < nk; ++kb) {
-                    if (!wait_bounded<PAIR>(smem_u32(&full[stage]), phase, abort_flag, a.err, a.wait_ns)) {
+                    if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, a.err, a.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -859,16 +808,11 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                             mma_f8(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + 2 * kk, kIdescF8, (kb | kk) != 0);
                     } else {
 #pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            if constexpr (PAIR)
-                                mma_bf16_pair(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc,
-                                              (kb | kk) != 0);
-                            else
-                                mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc,
-                                         (kb | kk) != 0);
-                        }
+                        for (int kk = 0; kk < kBK / 16; ++kk)
+                            mma_bf16(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + bstep * kk, idesc,
+                                     (kb | kk) != 0);
                     }
-                    commit(smem_u32(&empty[stage]));
+                    mma_commit(smem_u32(&empty[stage]));
                     if constexpr (W8) {
                         mma_commit(smem_u32(&bempty[bb]));
                         if (++bb == C::kBBufs) {
@@ -882,10 +826,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                     }
                 }
                 if (!ok) break;
-                commit(smem_u32(&tfull[acc]));
+                mma_commit(smem_u32(&tfull[acc]));
             }
             // every MMA issued has finished before TMEM is released
-            commit(smem_u32(drain));
+            mma_commit(smem_u32(drain));
             const uint64_t t0 = globaltimer();
             while (!mbar_try_wait(smem_u32(drain), 0) && globaltimer() - t0 < kDrainLimitNs) {
             }
@@ -1012,9 +956,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             if (!ok) break;
             fence_after();
             const bool routed = t.s < G.g.E;
-            const int mt = my_mtile(t);
-            const int rows = min(kBM, seg_rows[t.s] - mt * kBM);   // <= 0: a PAIR tile's missing half
-            const int grow = seg_row0[t.s] + mt * kBM + row;
+            const int rows = min(kBM, seg_rows[t.s] - t.mb * kBM);
+            const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (kFusedRoute) {
                 route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows, psum_cta);
@@ -1058,19 +1001,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             }
             fence_before();
             __syncwarp();
-            if constexpr (PAIR) {
-                if (lane == 0) {
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));   // rank 0's MMA reuses it
-                    if (EPI == kEpiFfn && t.phase == 0 && rows > 0) {
-                        // publish this warp's 32 H rows of the up tile (the whole warp's
-                        // stores precede this lane's fence through __syncwarp)
-                        __threadfence();
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        int *cnt = a.dep + mtile_start[t.s] + mt;
-                        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
-                    }
-                }
-            } else {
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
             if (EPI == kEpiFfn && t.phase == 0 && warp == 2 && lane == 0) {
                 // publish this up tile's H rows to the down tiles (any CTA) that read them:
@@ -1083,7 +1013,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                     int *cnt = a.dep + mtile_start[t.s] + t.mb;
                     asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(cnt) : "memory");
                 }
-            }
             }
         }
     }
@@ -1101,14 +1030,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             for (int e = threadIdx.x; e < a.route.E; e += C::kThreadsCta) atomicAdd(row + e, psum_cta[e]);
         }
     }
-    if constexpr (PAIR) cluster_sync();   // neither CTA leaves while the pair's MMAs or copies may use it
     if (warp == 1) {
         __syncwarp();
         fence_after();
-        if constexpr (PAIR)
-            tmem_dealloc_pair(tmem_base, C::kTmemCols);
-        else
-            tmem_dealloc(tmem_base, C::kTmemCols);
+        tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 
@@ -1145,31 +1070,6 @@ cudaError_t launch_gemm(const CUtensorMap &a0, const CUtensorMap &a1, const CUte
     return err;
 }
 
-// CTA-pair launch (clusters of two, M = 256 MMAs): as many pairs as can be resident
-// at once (at most half the SMs, at most max_tiles).  B comes from the tile images
-// through b0 (a map of 128-byte rows from args.wbase).  The launch is a plain
-// cluster launch (the profiler does not replay a cooperative cluster launch): the
-// grid is the resident count, so on a GPU that runs nothing else every pair of a
-// kEpiFfn launch is resident at once, and if one is not, the bounded waits of the
-// down tiles report it instead of waiting for it.
-template <int BN, int EPI>
-cudaError_t launch_gemm_pair(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b0, const CUtensorMap &a2,
-                             const CUtensorMap &a3, const TcArgs &args_in, int64_t max_tiles, cudaStream_t s) {
-    auto kern = tc_grouped_gemm_kernel<BN, EPI, false, false, true>;
-    using C = TcCfg<BN, false, 0, true>;
-    TcArgs args = args_in;
-    args.wait_ns = wait_limit_ns();
-    const size_t smem = C::kSmem;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    int pairs = max_active_clusters(kern, dim3(C::kThreadsCta), smem, 2);
-    if (pairs <= 0) return cudaErrorInvalidConfiguration;
-    pairs = std::min(pairs, num_sms() / 2);
-    if (max_tiles < pairs) pairs = (int)(max_tiles > 1 ? max_tiles : 1);
-    return launch_dependent_cluster(kern, dim3(2 * pairs), dim3(C::kThreadsCta), smem, s, 2, false, a0, a1, b0, b0,
-                                    a2, a3, args);
-}
-
 // Cluster-reduced split-K router (kEpiSplitRoute + KPL): one CTA per (token tile,
 // K split), clusters of `splits` CTAs, each cluster one token tile.
 template <int BN, int EPI>
@@ -1185,8 +1085,8 @@ cudaError_t launch_gemm_split_route(const CUtensorMap &a0, const CUtensorMap &b0
     const size_t smem = TcCfg<BN, false>::kSmem;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    return launch_dependent_cluster(kern, dim3(tiles * splits), dim3(kBlock), smem, s, splits, false, a0, a0, b0, b0,
-                                    a0, a0, args);
+    return launch_dependent_cluster(kern, dim3(tiles * splits), dim3(kBlock), smem, s, splits, a0, a0, b0, b0, a0, a0,
+                                    args);
 }
 
 // Single-GEMM launches pass their A maps again for the unused second phase.

@@ -357,23 +357,22 @@ def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
         assert rel_err(Yn[T * k:], sref) <= TOL[dt]
 
 
-# Long segments (at least 512 buffer rows per expert) run the fused launch on CTA
-# pairs: M = 256 MMAs over two consecutive 128-row M tiles of a segment.  The
-# segment sizes put a lone last M tile in a pair (1, 257 rows), a second tile of
-# one row (129, 385), a segment of exactly one pair (256) and none (0); the shared
-# segment spans several pairs.  Every row is compared with the oracle.
-PAIR_CASES = [
+# Long segments: the expert GEMMs take a segment's M tiles in groups of 16 (all N
+# blocks of a group before the next), so segments of more than 16 M tiles (2048
+# rows) are walked group by group.  The sizes give a last group of one M tile of
+# one row (2049), of a full tile (4096 + 2048 rows: exactly 16 and 48 M tiles), a
+# short last tile (2100, 4097), short segments next to them (0, 1, 129, 300) and a
+# shared segment of several groups.  Every row is compared with the oracle.
+LONG_SEG_CASES = [
     # T, d, f, f_shared, counts of the 8 routed experts
-    (2048, 256, 256, 128, [0, 1, 128, 129, 256, 257, 385, 700]),
-    (2048, 1024, 512, 256, [700, 385, 257, 1, 0, 129, 256, 128]),
+    (5400, 256, 256, 128, [0, 1, 2049, 129, 4097, 2048, 300, 2100]),
+    (5400, 512, 384, 256, [4096, 129, 0, 2049, 1, 2100, 300, 1800]),
 ]
-
-
-@pytest.mark.parametrize("T,d,f,fs,counts", PAIR_CASES)
-def test_grouped_ffn_pairs(T, d, f, fs, counts, cuda_device):
+@pytest.mark.parametrize("T,d,f,fs,counts", LONG_SEG_CASES)
+def test_grouped_ffn_long_segments(T, d, f, fs, counts, cuda_device):
     E, k = 8, 2
     A = int(sum(counts))
-    assert T * k // E >= 512 and A <= T * k
+    assert max(counts) > 16 * 128 and A <= T * k
     cfg = B.config(T=T, d=d, E=E, f=f, k=k, n_shared=1, f_shared=fs)
     g = torch.Generator(device="cpu").manual_seed(9090 + d)
     W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
@@ -658,16 +657,12 @@ E2E_SMALL = {
     "small_k_eq_E": WORKLOADS["mixtral_T256"].with_(T=200, d=256, E=4, k=4, f=128, name="small_k_eq_E"),
     "small_dense_E1": WORKLOADS["mixtral_T256"].with_(T=130, d=256, E=1, k=1, f=256, name="small_dense_E1"),
     "small_one_token": WORKLOADS["mixtral_T16"].with_(T=1, d=256, f=128, name="small_one_token"),
-    # at least 512 buffer rows per expert: the fused expert FFN runs on CTA pairs
-    # (top-2 softmax; capacity with the gated down store of k = 1; sigmoid + shared;
-    # Expert Choice)
-    "small_pairs_top2": WORKLOADS["mixtral_T256"].with_(T=2048, d=256, f=256, name="small_pairs_top2"),
-    "small_pairs_switch": WORKLOADS["switch_top1_cap1.25"].with_(T=4096, d=256, E=8, f=256,
-                                                                  logit_offsets="normal_var0.5",
-                                                                  name="small_pairs_switch"),
-    "small_pairs_shared": WORKLOADS["deepseek_v3"].with_(T=2048, d=256, E=8, k=2, f=128, f_shared=128,
-                                                          name="small_pairs_shared"),
-    "small_pairs_ec": WORKLOADS["expert_choice_zipf"].with_(T=1024, d=256, E=4, f=256, name="small_pairs_ec"),
+    # segments longer than 16 M tiles (2048 rows), walked in groups of 16 M tiles:
+    # top-2 softmax, and capacity with the gated down store of k = 1
+    "small_long_top2": WORKLOADS["mixtral_T256"].with_(T=9000, d=256, f=256, name="small_long_top2"),
+    "small_long_switch": WORKLOADS["switch_top1_cap1.25"].with_(T=24000, d=256, E=8, f=256,
+                                                                 logit_offsets="normal_var0.5",
+                                                                 name="small_long_switch"),
 }
 
 
