@@ -5,7 +5,8 @@
 //   warp 0      TMA producer: 128x64 A tile + BNx64 B tile per stage, 128-byte
 //               swizzle, into a STAGES-deep shared-memory ring (full/empty mbarriers)
 //   warp 1      TMEM allocator and MMA issuer: 4 x tcgen05.mma (M=128, N=BN, K=16)
-//               per stage into one of two TMEM accumulators
+//               per stage into one of two TMEM accumulators; an expert tile of at
+//               most 64 rows uses M=64 (its rows 16 q + i land in TMEM lanes 32 q + i)
 //   warps 2..5  epilogue: tcgen05.ld of the finished accumulator (one row per
 //               thread), then the epilogue of the instantiation; it overlaps the
 //               next tile's main loop through the second accumulator
@@ -800,12 +801,18 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                     // K step of 16: 32 bytes inside the K-major swizzle atom, or 16 rows of
                     // the MN-major tile (encoded >> 4)
                     const uint64_t bstep = bmn ? (2048 >> 4) : 2;
-                    const uint32_t idesc = bmn ? (kIdesc | kIdescBMajorMN) : kIdesc;
+                    // an expert tile of at most 64 rows runs M = 64 MMAs on the first half of
+                    // its A rows: less energy for the same result, which the power cap
+                    // gives back as clock
+                    const uint32_t idesc0 = bmn ? (kIdesc | kIdescBMajorMN) : kIdesc;
+                    const bool m64 = (EPI <= kEpiFfn) && (seg_rows[t.s] - t.mb * kBM) <= 64;
+                    const uint32_t idesc = m64 ? idesc_bf16_f32(64, BN) : idesc0;
+                    const uint32_t idesc_f8 = m64 ? idesc_e4m3_f32(64, BN) : kIdescF8;
                     if (F8A && f8) {
                         // four K steps of 32 E4M3 elements, 32 bytes each
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_f8(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + 2 * kk, kIdescF8, (kb | kk) != 0);
+                            mma_f8(d_tmem, adesc + (uint64_t)(2 * kk), bdesc + 2 * kk, idesc_f8, (kb | kk) != 0);
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -943,7 +950,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
     } else {
         // ---------------------------------------------------------------- epilogue
         const int quarter = warp & 3;   // TMEM lanes [32*quarter, 32*quarter + 32)
-        const int row = quarter * 32 + lane;
         int it = 0;
         for (int tile = tile0; tile < total; tile += tstep, ++it) {
             const TileAt t = locate(tile);
@@ -957,6 +963,9 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             fence_after();
             const bool routed = t.s < G.g.E;
             const int rows = min(kBM, seg_rows[t.s] - t.mb * kBM);
+            // M = 64 tiles: row 16 q + i of the accumulator is in TMEM lane 32 q + i (i < 16)
+            const bool m64 = (EPI <= kEpiFfn) && rows <= 64;
+            const int row = m64 ? (lane < 16 ? quarter * 16 + lane : kBM) : quarter * 32 + lane;
             const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (kFusedRoute) {
