@@ -102,20 +102,41 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta)
     }
 }
 
-// The same three steps in one CTA of 32 warps, for up to kPlanMax assignments.
-// Warp w owns one contiguous segment of the assignments (segments in warp order
-// are assignment order) and holds it in registers: lane l keeps assignments
-// a0 + 32 q + l, q < PER, all loaded at once.  Pass 1: each warp counts its
-// segment per expert into its own shared-memory counters.  Then thread e turns
-// the 32 per-warp counts of expert e into per-warp rank bases and the raw count;
-// warp 0 caps and scans the counts into off[].  Pass 2: each warp ranks its
-// segment in order from its bases; lanes holding the same expert are found with
-// ballots (warp_peers9).  row_token is assembled in shared memory and written out
-// in row order at the end.
+// The same three steps in one launch of a thread-block cluster of Q CTAs (Q = 1,
+// 2, 4 or 8: one per 2048 assignments) of 32 warps each, for up to kPlanMax assignments.  The
+// 32 Q warps own consecutive segments of the assignments (warp order = assignment
+// order) and hold them in registers: lane l keeps assignments a0 + 32 q + l,
+// q < PER, all loaded at once.  Pass 1: each warp counts its segment per expert
+// into its own shared-memory counters; thread e turns its CTA's 32 per-warp counts
+// of expert e into per-warp rank bases and the CTA's count.  After a cluster
+// barrier every CTA reads the other CTAs' counts (distributed shared memory): the
+// sum over the CTAs before it is its base, the sum over all the raw count; warp 0
+// caps and scans the counts into off[] (every CTA the same; CTA 0 writes them).
+// Pass 2: each warp ranks its segment in order from its bases; lanes holding the
+// same expert are found with ballots (warp_peers9); slot_of and row_token are
+// written directly.
 constexpr int kPlanWarps = 32;
-constexpr int64_t kPlanMax = 32 * kPlanWarps * 32;   // 32 assignments per lane
+constexpr int64_t kPlanMax = 32 * kPlanWarps * 32;   // the multi-kernel path above this
+constexpr int kPlanMaxCtas = 8;
 
-size_t plan_smem_bytes(int n, int E) { return sizeof(int) * ((size_t)kPlanWarps * E + E + 1 + (size_t)n); }
+size_t plan_smem_bytes(int E) { return sizeof(int) * ((size_t)kPlanWarps * E + 3 * (size_t)E + 1); }
+
+__device__ __forceinline__ uint32_t plan_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void plan_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the int at shared-memory address `p` of this CTA, in CTA `rank` of the cluster
+__device__ __forceinline__ int plan_ld_remote(const int *p, uint32_t rank) {
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p)), r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    int v;
+    asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(r) : "memory");
+    return v;
+}
 
 template <int PER>
 __global__ void __launch_bounds__(32 * kPlanWarps)
@@ -123,13 +144,17 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
                          int32_t *slot_of, int32_t *row_token, unsigned *err) {
     extern __shared__ int sm[];
     int *wcnt = sm;                        // [kPlanWarps][E]: counts, then rank bases
-    int *offs = wcnt + kPlanWarps * E;     // [E + 1]
-    int *rows_tok = offs + E + 1;          // [n]: token of each kept row
+    int *ctot = wcnt + kPlanWarps * E;     // [E]: this CTA's count per expert
+    int *cbase = ctot + E;                 // [E]: the counts of the CTAs before this one
+    int *offs = cbase + E;                 // [E + 1]
     pdl_wait();
     pdl_trigger();
+    const int Q = (int)gridDim.x;          // the whole grid is one cluster (or one CTA)
+    const int rank = Q > 1 ? (int)plan_ctarank() : 0;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int seg = ((n + kPlanWarps - 1) / kPlanWarps + 31) & ~31;   // <= 32 * PER
-    const int a0 = warp * seg, a1 = min(n, a0 + seg);
+    const int gwarps = kPlanWarps * Q;
+    const int seg = ((n + gwarps - 1) / gwarps + 31) & ~31;   // <= 32 * PER
+    const int a0 = min(n, (rank * kPlanWarps + warp) * seg), a1 = min(n, a0 + seg);
     int *my = wcnt + warp * E;
     for (int e = lane; e < E; e += 32) my[e] = 0;
     int ev[PER];
@@ -151,9 +176,22 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
             wcnt[w * E + e] = s;
             s += c;
         }
-        offs[e] = s;   // raw count, scanned below
+        ctot[e] = s;
     }
-    __syncthreads();
+    if (Q > 1) plan_cluster_sync();   // every CTA's counts are visible to the cluster
+    else __syncthreads();
+    for (int e = tid; e < E; e += blockDim.x) {
+        int before = 0, all = 0;
+        for (int c = 0; c < Q; ++c) {
+            const int v = (c == rank) ? ctot[e] : plan_ld_remote(ctot + e, (uint32_t)c);
+            if (c < rank) before += v;
+            all += v;
+        }
+        cbase[e] = before;
+        offs[e] = all;   // raw count, scanned below
+    }
+    if (Q > 1) plan_cluster_sync();   // no CTA's counts are read after this (a CTA may leave)
+    else __syncthreads();
     if (warp == 0) {   // kept counts and their exclusive scan, 32 experts per step
         int carry = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
@@ -161,7 +199,7 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
             int kept = 0;
             if (e < E) {
                 const int raw = offs[e];
-                cnt_raw[e] = raw;
+                if (rank == 0) cnt_raw[e] = raw;
                 kept = (cap < 0) ? raw : min(raw, cap);
             }
             int incl = kept;
@@ -176,7 +214,8 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
         if (lane == 0) offs[E] = carry;
     }
     __syncthreads();
-    for (int e = tid; e <= E; e += blockDim.x) off[e] = offs[e];
+    if (rank == 0)
+        for (int e = tid; e <= E; e += blockDim.x) off[e] = offs[e];
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
         if (a0 + q * 32 >= a1) break;   // warp-uniform
@@ -194,28 +233,27 @@ __global__ void __launch_bounds__(32 * kPlanWarps)
         if (valid && rank_in == 0) my[e] = base + __popc(peers);
         __syncwarp();
         if (valid) {
-            const int r = base + rank_in;
+            const int r = cbase[e] + base + rank_in;
             const int slot = (cap < 0 || r < cap) ? offs[e] + r : -1;
             slot_of[a] = slot;
-            if (slot >= 0) rows_tok[slot] = a / k;
+            if (slot >= 0) row_token[slot] = a / k;
         }
     }
-    __syncthreads();
-    const int rows = offs[E];
-    for (int r = tid; r < rows; r += blockDim.x) row_token[r] = rows_tok[r];
 }
 
 template <int PER>
 cudaError_t launch_plan(const int32_t *idx, int n, int k, int E, int cap, int32_t *cnt_raw, int32_t *off,
-                        int32_t *slot_of, int32_t *row_token, unsigned *err, cudaStream_t s) {
-    const size_t smem = plan_smem_bytes(n, E);
+                        int32_t *slot_of, int32_t *row_token, unsigned *err, int ctas, cudaStream_t s) {
+    const size_t smem = plan_smem_bytes(E);
     cudaError_t ce = cudaFuncSetAttribute(dispatch_plan_kernel<PER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem);
     if (ce != cudaSuccess) return ce;
-    return launch_dependent(dispatch_plan_kernel<PER>, dim3(1), dim3(32 * kPlanWarps), smem, s, false, idx, n, k, E,
-                            cap, cnt_raw, off, slot_of, row_token, err);
+    if (ctas == 1)
+        return launch_dependent(dispatch_plan_kernel<PER>, dim3(1), dim3(32 * kPlanWarps), smem, s, false, idx, n, k, E,
+                                cap, cnt_raw, off, slot_of, row_token, err);
+    return launch_dependent_cluster(dispatch_plan_kernel<PER>, dim3(ctas), dim3(32 * kPlanWarps), smem, s, ctas, idx,
+                                    n, k, E, cap, cnt_raw, off, slot_of, row_token, err);
 }
-
 
 // x_perm[row] = x[row_token[row]] for row < *rows (read on the device).  One warp
 // per (row, span of the row), four 16-byte vectors per lane in flight; a span is
@@ -371,9 +409,12 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
                                const GatherZero &zero, int row_bytes) {
     const int64_t n = (int64_t)c.T * c.k;
     if (n <= kPlanMax) {
-        const int per = (int)((n + 32 * kPlanWarps - 1) / (32 * kPlanWarps));   // assignments per lane
-        auto plan = per <= 8 ? launch_plan<8> : per <= 16 ? launch_plan<16> : launch_plan<32>;
-        const cudaError_t ce = plan(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, s);
+        // one CTA per 2048 assignments, up to a cluster of eight
+        const int ctas = n <= 2048 ? 1 : n <= 4096 ? 2 : n <= 8192 ? 4 : kPlanMaxCtas;
+        const int per = (int)((n + 32 * kPlanWarps * ctas - 1) / (32 * kPlanWarps * ctas));   // per lane
+        auto plan = per <= 1 ? launch_plan<1> : per <= 2 ? launch_plan<2> : per <= 4 ? launch_plan<4>
+                  : per <= 8 ? launch_plan<8> : per <= 16 ? launch_plan<16> : launch_plan<32>;
+        const cudaError_t ce = plan(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, ctas, s);
         if (ce != cudaSuccess) return ce;
     } else {
         const int nchunks = (int)((n + kChunk - 1) / kChunk);

@@ -165,7 +165,7 @@ def test_valid_call_without_gpu_reports_cuda_error():
 #             token tiles and a long d (split-K in clusters, reduced and selected in
 #             the same launch); Expert Choice adds the column select; E not a
 #             multiple of 8 adds the W_r transpose; fp32: 1
-#   dispatch: single-CTA plan + gather = 2 (at most 32768 assignments), else count,
+#   dispatch: plan (one cluster) + gather = 2 (at most 32768 assignments), else count,
 #             scan, rank + gather = 4; Expert Choice: slots + gather = 2
 #   FFN:      one fused tensor-core launch; fp32: up + down = 2
 #   forward:  the stages, without the combine when it is folded into the down

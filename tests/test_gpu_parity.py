@@ -192,10 +192,13 @@ DISPATCH_CASES = [
     (7, 8, 2, 0.0, 0.0, 1152, "bf16"),      # few rows: each split into spans, the last one ragged
     (300, 8, 2, 0.01, 0.0, 128, "bf16"),     # capacity 0: every assignment dropped
     (500, 8, 2, 1.25, 1.0, 64, "f32"),
-    (6000, 32, 2, 1.25, 1.0, 128, "bf16"),   # 12000 assignments: 16 per lane in the single-CTA plan
-    (16384, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 32768: the largest single-CTA plan (32 per lane)
+    (6000, 32, 2, 1.25, 1.0, 128, "bf16"),   # 12000 assignments: the plan on a cluster of 8 CTAs
+    (16384, 256, 2, 1.0, 0.3, 128, "bf16"),  # exactly 32768: the largest plan (8 CTAs, 4 per lane)
+    (2049, 8, 1, 1.25, 1.0, 128, "bf16"),    # 2049: a plan of 2 CTAs, the second one nearly empty
+    (4097, 64, 1, 1.25, 1.0, 128, "bf16"),   # 4097: 4 CTAs
+    (2731, 16, 3, 0.8, 1.0, 128, "bf16"),    # 8193: 8 CTAs, drops
     (70, 8, 1, 0.5, 2.0, 128, "bf16"),       # fewer assignments than one warp's share, drops
-    (16385, 8, 2, 1.0, 1.0, 128, "bf16"),    # 32770: just past it, the multi-CTA count/scan/rank path
+    (16385, 8, 2, 1.0, 1.0, 128, "bf16"),    # 32770: just past it, the multi-kernel count/scan/rank path
     (40000, 16, 2, 1.1, 1.0, 128, "bf16"),   # 80000: multi-CTA
     (32768, 256, 2, 1.0, 0.3, 128, "bf16"),  # 65536: multi-CTA with E = 256
 ]

@@ -64,7 +64,7 @@ def test_noalloc_dispatch_matches_moe_dispatch_twice(cuda_device):
         (B.config(T=8192, d=256, E=256, f=64, k=8, capacity_factor=1.0), 1.2, 16),
         (B.config(T=65536, d=128, E=64, f=64, k=1, capacity_factor=1.25), 1.0, 17),
         (B.config(T=20000, d=128, E=128, f=64, k=2, capacity_factor=1.0), 0.8, 18),
-        # back to a single-CTA call after the array was filled by the larger ones
+        # back to a one-launch plan after the array was filled by the larger ones
         (B.config(T=777, d=128, E=8, f=64, k=2, capacity_factor=0.9), 1.5, 19),
     ]
     for cfg, skew, seed in cases:
