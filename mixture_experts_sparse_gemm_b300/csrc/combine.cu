@@ -174,10 +174,18 @@ cudaError_t launch_combine(const moe_config &c, const Sizes &z, const void *Y, c
     a.span = (int)(((a.vecs + nch - 1) / nch + kStepVecs - 1) / kStepVecs * kStepVecs);
     const int64_t items = (int64_t)c.T * ((a.vecs + a.span - 1) / a.span);
     int64_t blocks = (items + kWarps - 1) / kWarps;
-    const int64_t cap = (int64_t)num_sms() * 8;
+    auto kern = c.dtype == MOE_F32 ? combine_kernel<float> : combine_kernel<__nv_bfloat16>;
+    // no more blocks than are resident at once (the warps loop over the items): a
+    // second wave of blocks would start only as the first one drains
+    static int resident[2] = {0, 0};
+    int &per_sm = resident[c.dtype == MOE_F32 ? 1 : 0];
+    if (per_sm == 0 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kWarps, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        per_sm = 0;
+    }
+    const int64_t cap = (int64_t)num_sms() * (per_sm > 0 ? per_sm : 8);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    auto kern = c.dtype == MOE_F32 ? combine_kernel<float> : combine_kernel<__nv_bfloat16>;
     return launch_dependent(kern, dim3((unsigned)blocks), dim3(32 * kWarps), 0, s, false, a);
 }
 
