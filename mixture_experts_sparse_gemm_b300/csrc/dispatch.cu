@@ -412,9 +412,17 @@ cudaError_t launch_dispatch_tc(const moe_config &c, int32_t cap, const int32_t *
         // one CTA per 2048 assignments, up to a cluster of eight
         const int ctas = n <= 2048 ? 1 : n <= 4096 ? 2 : n <= 8192 ? 4 : kPlanMaxCtas;
         const int per = (int)((n + 32 * kPlanWarps * ctas - 1) / (32 * kPlanWarps * ctas));   // per lane
-        auto plan = per <= 1 ? launch_plan<1> : per <= 2 ? launch_plan<2> : per <= 4 ? launch_plan<4>
-                  : per <= 8 ? launch_plan<8> : per <= 16 ? launch_plan<16> : launch_plan<32>;
-        const cudaError_t ce = plan(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, ctas, s);
+        auto pick = [](int p) {
+            return p <= 1 ? launch_plan<1> : p <= 2 ? launch_plan<2> : p <= 4 ? launch_plan<4>
+                 : p <= 8 ? launch_plan<8> : p <= 16 ? launch_plan<16> : launch_plan<32>;
+        };
+        cudaError_t ce = pick(per)(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, ctas, s);
+        if (ce != cudaSuccess && ctas > 1) {
+            // a device that cannot place the cluster (SMs held elsewhere): one CTA does it all
+            (void)cudaGetLastError();
+            const int per1 = (int)((n + 32 * kPlanWarps - 1) / (32 * kPlanWarps));
+            ce = pick(per1)(topk_idx, (int)n, c.k, c.E, cap, cnt_raw, off, slot_of, row_token, err, 1, s);
+        }
         if (ce != cudaSuccess) return ce;
     } else {
         const int nchunks = (int)((n + kChunk - 1) / kChunk);
