@@ -328,8 +328,10 @@ __device__ __forceinline__ int build_tile_table(const GroupedShape &g, int *tile
 }
 
 // GM > 0: the M blocks of a segment are taken in groups of GM, and a group's tiles
-// (every N block of it, M fastest) all come before the next group's.
-template <int BM, int GM = 0>
+// (every N block of it, M fastest) all come before the next group's.  GN > 0: within
+// a group, the N blocks are taken in chunks of GN (all M blocks of the group for a
+// chunk before the next chunk).
+template <int BM, int GM = 0, int GN = 0>
 __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *tile_start, const int *seg_rows,
                                             int S, int tile, int &s, int &mb, int &nb) {
     int lo = 0, hi = S - 1;   // last s with tile_start[s] <= tile
@@ -344,8 +346,14 @@ __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *ti
         const int nblk = (s < g.E) ? g.nblk_routed : g.nblk_shared;
         const int grp = local / (GM * nblk), rem = local - grp * GM * nblk;
         const int gm = min(GM, mblk - grp * GM);   // the last group may be short
-        mb = grp * GM + rem % gm;
-        nb = rem / gm;
+        if constexpr (GN > 0) {
+            const int chunk = rem / (gm * GN), rem2 = rem - chunk * gm * GN;
+            mb = grp * GM + rem2 % gm;
+            nb = chunk * GN + rem2 / gm;
+        } else {
+            mb = grp * GM + rem % gm;
+            nb = rem / gm;
+        }
     } else {
         mb = local % mblk;
         nb = local / mblk;
