@@ -295,8 +295,9 @@ __device__ __forceinline__ unsigned warp_peers9(unsigned key) {
 
 // Tile table of a grouped problem, built once per CTA in shared memory:
 // tile_start[s] = first tile of segment s (tile_start[S] = total tiles).
-// Segment tiles are ordered N-block-major with the M-block fastest, so the
-// CTAs that share a weight tile run at the same time.
+// The order of a segment's tiles is decode_tile's: N-block-major with the M block
+// fastest, or the same inside groups of M blocks (and chunks of N blocks), so that
+// the CTAs sharing a weight tile run at the same time.
 template <int BM>
 __device__ __forceinline__ int build_tile_table(const GroupedShape &g, int *tile_start, int *seg_row0,
                                                 int *seg_rows) {
