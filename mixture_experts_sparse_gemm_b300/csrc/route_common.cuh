@@ -43,9 +43,11 @@ __device__ __forceinline__ int slot_expert(int lane, int i) {
 // the lower expert index, and writes indices and (renormalised) weights.
 // With a.psum_rows, every score is also added to the lane's running sums pacc
 // (same slots), which the caller flushes once.
+// bias (nullable): the lane's selection biases of its KPL slots, loaded once by a
+// caller that selects many tokens; null reads them from a.sel_bias here.
 template <int KPL, bool BLOCKED = false>
 __device__ __forceinline__ void warp_score_select(const RouteArgs &a, const float (&u)[KPL], int t, int lane,
-                                                  float (&pacc)[KPL]) {
+                                                  float (&pacc)[KPL], const float *bias = nullptr) {
     constexpr int kPerLane = KPL;
     const int E = a.E;
     float p[kPerLane];
@@ -93,7 +95,7 @@ __device__ __forceinline__ void warp_score_select(const RouteArgs &a, const floa
 #pragma unroll
     for (int i = 0; i < kPerLane; ++i) {
         const int e = slot_expert<KPL, BLOCKED>(lane, i);
-        float kf = (e < E) ? p[i] + (a.sel_bias ? a.sel_bias[e] : 0.f) : -INFINITY;
+        float kf = (e < E) ? p[i] + (bias ? bias[i] : (a.sel_bias ? a.sel_bias[e] : 0.f)) : -INFINITY;
         if (kf != kf) kf = -INFINITY;
         const uint32_t b = __float_as_uint(kf);
         key[i] = (b & 0x80000000u) ? ~b : (b | 0x80000000u);   // ordered like the floats; -inf > 0

@@ -409,9 +409,13 @@ __device__ __forceinline__ void split_route_select(const RouteEpi &r, const uint
     a.scores_t = r.scores_t;
     a.psum_rows = r.psum_rows;
     const uint32_t base = smem_u32(red);
-    float pacc[KPL];
+    float pacc[KPL], bias[KPL];   // the lane's experts are the same in every row: biases once
 #pragma unroll
-    for (int i = 0; i < KPL; ++i) pacc[i] = 0.f;
+    for (int i = 0; i < KPL; ++i) {
+        pacc[i] = 0.f;
+        const int e = lane * KPL + i;
+        bias[i] = (e < a.E && a.sel_bias) ? a.sel_bias[e] : 0.f;
+    }
     for (int rr = lo + warp; rr < hi; rr += nwarps) {
         // every split's values of the row are loaded before the sums (split order kept)
         float pv[kMaxRouteSplits][KPL];
@@ -430,7 +434,7 @@ __device__ __forceinline__ void split_route_select(const RouteEpi &r, const uint
             if (e < a.E && a.logit_offset) v += a.logit_offset[e];
             u[i] = (e < a.E) ? v : -FLT_MAX;
         }
-        warp_score_select<KPL, true>(a, u, row0 + rr, lane, pacc);
+        warp_score_select<KPL, true>(a, u, row0 + rr, lane, pacc, bias);
     }
     flush_prob_sum<KPL, true>(a, pacc, lane, sacc);
 }
