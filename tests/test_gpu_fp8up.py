@@ -24,7 +24,9 @@ pytestmark = pytest.mark.gpu
 GAP = 1e-4
 TOL = 2e-2
 NTH = os.cpu_count() or 1
-EDGE_COUNTS = [1, 15, 16, 17, 111, 112, 113, 127, 128, 129, 240, 0]
+# segment sizes on both sides of the 16-row MMA step, of the 64-row limit of the
+# M = 64 tiles (also as a second M tile: 192, 193) and of the 128-row M tile
+EDGE_COUNTS = [1, 15, 16, 17, 63, 64, 65, 111, 112, 113, 127, 128, 129, 192, 193, 240, 0]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -148,8 +150,8 @@ def test_fp8up_packing_is_exact(cuda_device):
 
 
 def test_fp8up_grouped_ffn_tile_edges(cuda_device):
-    """Segments of 1..240 rows and an empty one around the 128-row M tile, plus a
-    shared expert over all rows; every row compared.  An all-zero token row
+    """Segments of 1..240 rows and an empty one around the 64- and 128-row tile
+    limits, plus a shared expert over all rows; every row compared.  An all-zero token row
     (scale 0) is among them."""
     E, d, f, fs = len(EDGE_COUNTS), 256, 256, 128
     T = sum(EDGE_COUNTS)

@@ -463,7 +463,9 @@ def test_grouped_ffn_257_segments(d, f, fs, cuda_device):
 # Segment sizes around the 128-row M tile: 1, 15, 16, 17, 111, 112, 113, 127, 128,
 # 129, 240 rows and an empty expert; the shared segment (T = 1029 rows) ends in a
 # 5-row tile.
-EDGE_COUNTS = [1, 15, 16, 17, 111, 112, 113, 127, 128, 129, 240, 0]
+# segment sizes on both sides of the 16-row MMA step, of the 64-row limit of the
+# M = 64 tiles (also as a second M tile: 192, 193) and of the 128-row M tile
+EDGE_COUNTS = [1, 15, 16, 17, 63, 64, 65, 111, 112, 113, 127, 128, 129, 192, 193, 240, 0]
 
 
 @pytest.mark.parametrize("d,f", [(256, 256), (384, 128)])
