@@ -635,16 +635,38 @@ def _segment_tails(gi, g_slot, usable, E):
     return toks, len(with_rows), exact
 
 
+def _segment_group_rows(gi, g_slot, g_off, usable, E):
+    """For every expert, the tokens of the rows that open and close each group of 16
+    M tiles of its segment (segment rows 0, 2047, 2048, 4095, 4096, ... and its last
+    row) in the GPU's own routing, where the routing agrees with the oracle's: the
+    tiles on both sides of every group boundary of the expert GEMMs' tile order."""
+    T, k = gi.shape
+    toks = []
+    for e in range(E):
+        n = int(g_off[e + 1] - g_off[e])
+        if n == 0:
+            continue
+        ranks = {0, n - 1}
+        for r0 in range(2048, n, 2048):
+            ranks.update((r0 - 1, r0))
+        rel = g_slot - g_off[e]
+        for t, j in zip(*np.nonzero((gi == e) & (g_slot >= 0))):
+            if int(rel[t, j]) in ranks and usable[t]:
+                toks.append(int(t))
+    return np.unique(np.array(toks, np.int64))
+
+
 # tokens compared at full size: None = all; an int = a seeded sample of that many;
 # "tails" = the last row of every expert segment (+ a seeded sample of 24 and the
-# shared segment's last token), so each segment's tail M tile is checked
+# shared segment's last token), so each segment's tail M tile is checked;
+# "groups" = the rows at every group boundary of every expert segment (+ 12 sampled)
 E2E_CASES = {
     "tiny_top2_fp32": None,
     "switch_top1_cap1.25": 48,
     "mixtral_T16": None,
     "mixtral_T256": 24,
     "mixtral_T4096": 16,
-    "mixtral_T16384": 12,
+    "mixtral_T16384": "groups",
     "deepseek_v3": "tails",
     "expert_choice_zipf": 16,
 }
@@ -711,6 +733,11 @@ def _run_e2e(wl, n_sample, cuda_device):
                   f"the segment's last row compared for {n_tail} of them")
             assert len(reached) == n_rows and n_tail >= 0.95 * n_rows
             toks = _sample_tokens(T, 24, T, list(tails) + [T - 1])
+        elif n_sample == "groups":
+            bounds = _segment_group_rows(gi, g_slot, g_off, same, wl.E)
+            print(f"{wl.name}: {len(bounds)} tokens at group boundaries of the expert segments")
+            assert len(bounds) >= wl.E
+            toks = _sample_tokens(T, 12, T, list(bounds))
         else:
             toks = np.arange(T) if n_sample is None else _sample_tokens(T, n_sample, T, dropped[:64])
         toks = np.array([t for t in toks if same[t]], np.int64)
