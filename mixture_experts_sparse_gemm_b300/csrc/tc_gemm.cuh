@@ -103,7 +103,7 @@ struct TcCfg {
     static constexpr int kThreadsCta = kThreads + 32 * kConvWarps + (W8 ? 32 : 0) + 32 * EXTRA;
     static constexpr int kTmemCols = (2 * BN < 32) ? 32 : 2 * BN;
     static constexpr int kBarBytes = (2 * kStages + 5 + 2 * kBBufs + 2 * kB8Stages) * 8;
-    static constexpr int kMiscBytes = 64 + sizeof(int) * (6 * (kMaxE + 2));
+    static constexpr int kMiscBytes = 64 + sizeof(int) * (8 * (kMaxE + 2));
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kBBufs * kBBytes +
                                     (size_t)kB8Stages * kB8Bytes + kBarBytes + kMiscBytes;
 };
@@ -234,9 +234,11 @@ __device__ __forceinline__ void topk_insert(float (&tk)[KMAX], int (&ti)[KMAX], 
 //   pass 2: softmax normaliser sum_e exp(u_e - max).
 //   then the k weights (renormalised when asked), or for Expert Choice every
 //   score written expert-major.
+// loff / bias: the E logit offsets and selection biases in shared memory (zeros
+// where the caller gave none), read from there in every pass.
 template <int BN, int KMAX>
 __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr, int t, bool valid,
-                                               float *psum_cta) {
+                                               float *psum_cta, const float *loff, const float *bias) {
     const int E = r.E, T = r.T;
     constexpr int kChunks = BN / 16;
     const bool softmax = r.gate == MOE_GATE_SOFTMAX;
@@ -259,13 +261,13 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
         for (int i = 0; i < 16; ++i) {
             const int e = c * 16 + i;
             if (e < E) {
-                const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
+                const float u = __uint_as_float(v[i]) + loff[e];
                 if (softmax) {
                     mx = fmaxf(mx, u);
                     if (!ec) topk_insert<KMAX>(tk, ti, tu, u, e, u);
                 } else {
                     const float s = __fdividef(1.f, 1.f + __expf(-u));
-                    topk_insert<KMAX>(tk, ti, tu, s + (r.sel_bias ? r.sel_bias[e] : 0.f), e, u);
+                    topk_insert<KMAX>(tk, ti, tu, s + bias[e], e, u);
                 }
             }
         }
@@ -281,7 +283,7 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int e = c * 16 + i;
-                if (e < E) sum += __expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx);
+                if (e < E) sum += __expf(__uint_as_float(v[i]) + loff[e] - mx);
             }
         }
         inv = 1.f / sum;
@@ -300,7 +302,7 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
                 const int e = c * 16 + i;
                 float pe = 0.f;
                 if (e < E && valid) {
-                    const float u = __uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f);
+                    const float u = __uint_as_float(v[i]) + loff[e];
                     pe = softmax ? __expf(u - mx) * inv : __fdividef(1.f, 1.f + __expf(-u));
                 }
 #pragma unroll
@@ -320,7 +322,7 @@ __device__ __forceinline__ void route_epilogue(const RouteEpi &r, uint32_t taddr
                 const int e = c * 16 + i;
                 if (e < E && valid)
                     r.scores_t[(size_t)e * T + t] =
-                        __expf(__uint_as_float(v[i]) + (r.logit_offset ? r.logit_offset[e] : 0.f) - mx) * inv;
+                        __expf(__uint_as_float(v[i]) + loff[e] - mx) * inv;
             }
         }
         return;
@@ -576,6 +578,8 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
     int *seg_rows = seg_row0 + (kMaxE + 2);
     int *mtile_start = seg_rows + (kMaxE + 2);                      // first M tile of each segment
     float *psum_cta = reinterpret_cast<float *>(mtile_start + (kMaxE + 2));   // router score sums of this CTA
+    float *s_loff = psum_cta + (kMaxE + 2);   // fused router: logit offsets (0 without), staged once
+    float *s_bias = s_loff + (kMaxE + 2);     // fused router: selection biases (0 without)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if constexpr (kFusedRoute) {
@@ -624,6 +628,12 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
     fence_after();
     pdl_wait();      // the previous kernel's outputs (segment offsets, A rows) are visible from here on
     pdl_trigger();
+    if constexpr (kFusedRoute) {   // made visible to the epilogue by the barrier in build_tile_table
+        for (int e = threadIdx.x; e < a.route.E; e += C::kThreadsCta) {
+            s_loff[e] = a.route.logit_offset ? a.route.logit_offset[e] : 0.f;
+            s_bias[e] = a.route.sel_bias ? a.route.sel_bias[e] : 0.f;
+        }
+    }
     const uint32_t tmem_base = *tmem_holder;
     const int S = build_tile_table<kBM>(a.p[0].g, tile_start0, seg_row0, seg_rows);
     const int total0 = tile_start0[S];
@@ -981,7 +991,7 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
             const int grow = seg_row0[t.s] + t.mb * kBM + row;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
             if constexpr (kFusedRoute) {
-                route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows, psum_cta);
+                route_epilogue<BN, EPI - kEpiRoute>(a.route, taddr, grow, row < rows, psum_cta, s_loff, s_bias);
             } else if constexpr (kSplitRoute) {
                 // this CTA's partial logits of the tile -> shared memory, row r at r * (BN + 4)
                 // floats (the stage ring is idle: every MMA of the tile has completed)
