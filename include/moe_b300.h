@@ -332,6 +332,22 @@ moe_status moe_set_wait_limit_ns(uint64_t limit_ns);
 moe_status moe_get_wait_limit_ns(uint64_t *limit_ns);
 
 /*
+ * Tile order of the tensor-core expert GEMMs (a tuning knob of the library; the
+ * pages prescribe no schedule).  Each expert segment's 128-row M tiles are taken
+ * in groups of nearly equal size, every N block of a group before the next group,
+ * so that a group's activation rows stay in L2 while the group streams the
+ * expert's weights once.  A group holds at most as many M tiles as fit `up_bytes`
+ * of x_perm rows (up projection: 128 x d x 2 bytes per tile) or `down_bytes` of H
+ * rows (down projection: 128 x f x 2 bytes per tile), and at least one.  The
+ * order changes which tiles run together, never a result: every output element is
+ * computed by one tile with the same k order.  Process-wide, read when a call
+ * launches its kernels; 0 restores a default (40 MiB up, 64 MiB down); values
+ * above 2^40 return MOE_ERR_INVALID_ARG.  No CUDA call.
+ */
+moe_status moe_set_tile_group_bytes(uint64_t up_bytes, uint64_t down_bytes);
+moe_status moe_get_tile_group_bytes(uint64_t *up_bytes, uint64_t *down_bytes);
+
+/*
  * Probe of the failure path of the bounded waits (the pages define no failure
  * behaviour; this is a diagnostic of the library).  Launches one small kernel on
  * `stream` that runs the two wait routines of the tensor-core kernels with the

@@ -26,7 +26,8 @@ EXPORTS = ("moe_status_string", "moe_validate_config", "moe_expert_capacity", "m
            "moe_workspace_size", "moe_packed_weights_size", "moe_pack_weights", "moe_route", "moe_dispatch",
            "moe_grouped_ffn", "moe_grouped_ffn_up", "moe_grouped_ffn_down", "moe_combine", "moe_forward",
            "moe_launch_count", "moe_check_device_error", "moe_dispatch_noalloc", "moe_load_stats",
-           "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_wait_probe")
+           "moe_set_wait_limit_ns", "moe_get_wait_limit_ns", "moe_wait_probe", "moe_set_tile_group_bytes",
+           "moe_get_tile_group_bytes")
 MOE_DISPATCH_NOALLOC_MAX_ASSIGNMENTS = 65536
 
 
@@ -78,6 +79,8 @@ def lib():
             "moe_load_stats": [cfgp, vp, vp, vp, vp, vp, vp, vp],
             "moe_set_wait_limit_ns": [ctypes.c_uint64],
             "moe_get_wait_limit_ns": [ctypes.POINTER(ctypes.c_uint64)],
+            "moe_set_tile_group_bytes": [ctypes.c_uint64, ctypes.c_uint64],
+            "moe_get_tile_group_bytes": [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)],
             "moe_wait_probe": [vp, ctypes.c_int32, vp],
         }
         for name, args in sigs.items():
@@ -237,6 +240,16 @@ def moe_get_wait_limit_ns() -> int:
     v = ctypes.c_uint64()
     _check(lib().moe_get_wait_limit_ns(ctypes.byref(v)), "moe_get_wait_limit_ns")
     return int(v.value)
+
+
+def moe_set_tile_group_bytes(up_bytes: int, down_bytes: int):
+    _check(lib().moe_set_tile_group_bytes(int(up_bytes), int(down_bytes)), "moe_set_tile_group_bytes")
+
+
+def moe_get_tile_group_bytes() -> tuple[int, int]:
+    u, d = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib().moe_get_tile_group_bytes(ctypes.byref(u), ctypes.byref(d)), "moe_get_tile_group_bytes")
+    return int(u.value), int(d.value)
 
 
 def moe_wait_probe(flag, target=1, stream=None):

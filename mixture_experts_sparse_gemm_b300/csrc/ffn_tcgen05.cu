@@ -25,6 +25,15 @@ struct FfnMaps {
     CUtensorMap a0, a1;
 };
 
+// M tiles per group of the tile order (tc_gemm.cuh): as many 128-row blocks of A as
+// fit `share` bytes, which stay in L2 while the group's N blocks stream the weights.
+// By default x_perm rows of the up projection take 40 MiB and H rows of the down
+// projection 64 MiB: the L2 (126 MB) spans two dies, and rows that CTAs on both dies
+// read are held on both, so a group fills at most about half of it.
+int tile_group(uint64_t share, int K) {
+    return (int)std::min<uint64_t>(1u << 20, std::max<uint64_t>(1, share / ((uint64_t)kBM * K * 2)));
+}
+
 // Up projection: A = x_perm (routed) / x (shared), B = [W1|W3] images, C = H / Hs.
 // FP8 up projection (f8 != nullptr): x_perm and x hold E4M3 codes, with the row
 // scales of f8.
@@ -59,6 +68,7 @@ bool up_gemm(const moe_config &c, const Sizes &z, const void *x_perm, const int3
         G.rs1 = f8->rs1;
     }
     G.img_rows = bn;
+    G.group_m = tile_group(tile_group_bytes(0), c.d);
     G.C0 = H;
     G.C1 = Hs;
     G.ldc0 = c.f;
@@ -91,6 +101,7 @@ bool down_gemm(const moe_config &c, const Sizes &z, const void *H, const void *H
         G.sc1 = reinterpret_cast<const float *>(pk + L.sc2s);
     }
     G.img_rows = bn;
+    G.group_m = tile_group(tile_group_bytes(1), c.f);
     G.C0 = Y;
     G.C1 = static_cast<__nv_bfloat16 *>(Y) + (size_t)z.rows_routed * c.d;
     G.ldc0 = c.d;

@@ -20,6 +20,9 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;   // 2 s
 constexpr uint64_t kMinWaitNs = 1000ull;             // 1 us
 constexpr uint64_t kMaxWaitNs = 60000000000ull;      // 60 s
 std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+constexpr uint64_t kDefaultGroupBytes[2] = {40ull << 20, 64ull << 20};   // up, down
+constexpr uint64_t kMaxGroupBytes = 1ull << 40;
+std::atomic<uint64_t> g_group_bytes[2] = {kDefaultGroupBytes[0], kDefaultGroupBytes[1]};
 int g_sm_count[kMaxDevices];
 int g_arch_ok[kMaxDevices];   // 0 unknown, 1 sm_103, -1 other
 unsigned *g_err_ptr[kMaxDevices];
@@ -294,6 +297,8 @@ PackedLayout packed_layout(const moe_config &c) {
 moe_status device_ready(unsigned **err_word) { return device_setup(err_word); }
 
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+uint64_t tile_group_bytes(int down) { return g_group_bytes[down ? 1 : 0].load(std::memory_order_relaxed); }
 
 int num_sms() {
     int dev = 0;
@@ -734,6 +739,20 @@ moe_status moe_set_wait_limit_ns(uint64_t limit_ns) {
     if (limit_ns == 0) limit_ns = kDefaultWaitNs;
     if (limit_ns < kMinWaitNs || limit_ns > kMaxWaitNs) return MOE_ERR_INVALID_ARG;
     g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+moe_status moe_set_tile_group_bytes(uint64_t up_bytes, uint64_t down_bytes) {
+    if (up_bytes > kMaxGroupBytes || down_bytes > kMaxGroupBytes) return MOE_ERR_INVALID_ARG;
+    g_group_bytes[0].store(up_bytes ? up_bytes : kDefaultGroupBytes[0], std::memory_order_relaxed);
+    g_group_bytes[1].store(down_bytes ? down_bytes : kDefaultGroupBytes[1], std::memory_order_relaxed);
+    return MOE_OK;
+}
+
+moe_status moe_get_tile_group_bytes(uint64_t *up_bytes, uint64_t *down_bytes) {
+    if (!up_bytes || !down_bytes) return MOE_ERR_INVALID_ARG;
+    *up_bytes = tile_group_bytes(0);
+    *down_bytes = tile_group_bytes(1);
     return MOE_OK;
 }
 

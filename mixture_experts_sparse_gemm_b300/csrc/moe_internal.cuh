@@ -203,6 +203,9 @@ int num_sms();
 moe_status device_ready(unsigned **err_word);
 // limit of the bounded device-side waits (process-wide; moe_set_wait_limit_ns)
 uint64_t wait_limit_ns();
+// share of L2 that one group of the expert GEMMs' tile order fills with A rows
+// (down = 0: x_perm rows of the up projection, 1: H rows of the down projection)
+uint64_t tile_group_bytes(int down);
 // Per-row E4M3 quantisation of bf16 rows: s[r] = amax_r / 448, q[r][i] = E4M3(x / s[r])
 // (fp32 division, round to nearest even, saturated; an all-zero row gets s = 0 and
 // zero codes).  rows x d, one warp per row.
@@ -328,13 +331,13 @@ __device__ __forceinline__ int build_tile_table(const GroupedShape &g, int *tile
     return S;
 }
 
-// GM > 0: the M blocks of a segment are taken in groups of GM, and a group's tiles
-// (every N block of it, M fastest) all come before the next group's.  GN > 0: within
-// a group, the N blocks are taken in chunks of GN (all M blocks of the group for a
-// chunk before the next chunk).
-template <int BM, int GM = 0, int GN = 0>
+// group_m > 0: the M blocks of a segment are split into ceil(mblk / group_m) groups
+// of nearly equal size (the first mblk mod #groups are one block larger), and a
+// group's tiles (every N block of it, M fastest) all come before the next group's.
+// group_m = 0: the segment's tiles M fastest.
+template <int BM>
 __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *tile_start, const int *seg_rows,
-                                            int S, int tile, int &s, int &mb, int &nb) {
+                                            int S, int tile, int &s, int &mb, int &nb, int group_m = 0) {
     int lo = 0, hi = S - 1;   // last s with tile_start[s] <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -343,18 +346,25 @@ __device__ __forceinline__ void decode_tile(const GroupedShape &g, const int *ti
     s = lo;
     const int local = tile - tile_start[s];
     const int mblk = (seg_rows[s] + BM - 1) / BM;
-    if constexpr (GM > 0) {
+    if (group_m > 0 && mblk > group_m) {
         const int nblk = (s < g.E) ? g.nblk_routed : g.nblk_shared;
-        const int grp = local / (GM * nblk), rem = local - grp * GM * nblk;
-        const int gm = min(GM, mblk - grp * GM);   // the last group may be short
-        if constexpr (GN > 0) {
-            const int chunk = rem / (gm * GN), rem2 = rem - chunk * gm * GN;
-            mb = grp * GM + rem2 % gm;
-            nb = chunk * GN + rem2 / gm;
+        const int ng = (mblk + group_m - 1) / group_m;
+        const int base = mblk / ng, big = mblk - base * ng;   // big groups of base + 1 blocks first
+        const int big_tiles = big * (base + 1) * nblk;
+        int gm, m0, rem;
+        if (local < big_tiles) {
+            gm = base + 1;
+            const int grp = local / (gm * nblk);
+            rem = local - grp * gm * nblk;
+            m0 = grp * gm;
         } else {
-            mb = grp * GM + rem % gm;
-            nb = rem / gm;
+            gm = base;
+            const int l2 = local - big_tiles, grp = l2 / (gm * nblk);
+            rem = l2 - grp * gm * nblk;
+            m0 = big * (base + 1) + grp * gm;
         }
+        mb = m0 + rem % gm;
+        nb = rem / gm;
     } else {
         mb = local % mblk;
         nb = local / mblk;

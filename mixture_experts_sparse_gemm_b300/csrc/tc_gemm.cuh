@@ -54,17 +54,11 @@ using namespace tc;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 // Expert GEMM tile order (the ~148 tiles in flight share their operands through L2):
-// a segment's M tiles in groups, each group's tiles before the next group's, and
-// inside a group its N blocks in chunks, all M tiles of the group per N block.
-//   up tiles:   groups of 32 M tiles, chunks of 28 N blocks: a group's A rows (at
-//               most 32 x 128 rows of x_perm) stay in L2 for a chunk, and an
-//               expert's W1|W3 is read once per group;
-//   down tiles: groups of 16 M tiles, all N blocks: the group's H rows (16 x 128
-//               rows of f bf16, 59 MB at f = 14336) stay in L2 while every N block
-//               reads them.
-// Separate up and down launches take the down order.
-constexpr int kTileUpM = 32, kTileUpN = 28;
-constexpr int kTileGroupM = 16;
+// a segment's M tiles in groups of nearly equal size, at most TcGemm::group_m each,
+// every N block of a group (M fastest) before the next group.  A group's A rows
+// stay in L2 while its N blocks stream the weights once; the host sizes group_m so
+// that a group's A rows fill a set share of L2 (x_perm rows of the up projection,
+// H rows of the down projection).
 constexpr int kThreads = 192;
 constexpr int kEpiSwiGLU = 0;   // up projection (+ SwiGLU)
 constexpr int kEpiStore = 1;    // down projection (optionally gated, see TcArgs::gated)
@@ -150,6 +144,9 @@ struct TcGemm {
     const float *rs0;
     const int32_t *rtok0;
     const float *rs1;
+    // expert GEMMs: M tiles per group of the tile order (0: M fastest over the whole
+    // segment; the router keeps 0, its tile order is its K split layout)
+    int group_m;
 };
 
 struct TcArgs {
@@ -547,11 +544,6 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
                            TcArgs a) {
     using C = TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitSelectWarps : 0>;
     constexpr int kPhases = (EPI == kEpiFfn) ? 2 : 1;
-    // expert GEMMs take their tiles in the grouped order above (the router's tile
-    // order is its K split layout and stays as it is)
-    constexpr int kTileGroup = (EPI <= kEpiFfn) ? kTileGroupM : 0;
-    constexpr int kUpM = (EPI == kEpiFfn) ? kTileUpM : kTileGroup;
-    constexpr int kUpN = (EPI == kEpiFfn) ? kTileUpN : 0;
     constexpr bool kRouter = EPI >= kEpiPartial;   // router launches may read B (W_r) MN-major
     constexpr bool kFusedRoute = EPI > kEpiRoute && EPI < kEpiSplitRoute;
     constexpr bool kSplitRoute = EPI > kEpiSplitRoute;
@@ -683,10 +675,10 @@ __global__ void __launch_bounds__(TcCfg<BN, W8, (EPI > kEpiSplitRoute) ? kSplitS
         TileAt t;
         if (kPhases == 2 && tile >= total0) {
             t.phase = 1;
-            decode_tile<kBM, kTileGroup>(a.p[1].g, tile_start1, seg_rows, S, tile - total0, t.s, t.mb, t.nb);
+            decode_tile<kBM>(a.p[1].g, tile_start1, seg_rows, S, tile - total0, t.s, t.mb, t.nb, a.p[1].group_m);
         } else {
             t.phase = 0;
-            decode_tile<kBM, kUpM, kUpN>(a.p[0].g, tile_start0, seg_rows, S, tile, t.s, t.mb, t.nb);
+            decode_tile<kBM>(a.p[0].g, tile_start0, seg_rows, S, tile, t.s, t.mb, t.nb, a.p[0].group_m);
         }
         return t;
     };

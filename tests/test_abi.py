@@ -217,5 +217,23 @@ def test_wait_limit_setting_is_host_only_and_checked():
     finally:
         B.moe_set_wait_limit_ns(0)
     assert L.moe_get_wait_limit_ns(None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_tile_group_setting_is_host_only_and_checked():
+    build_mod.build()
+    L = B.lib()
+    assert B.moe_get_tile_group_bytes() == (40 << 20, 64 << 20)
+    try:
+        B.moe_set_tile_group_bytes(3 * 128 * 256 * 2, 1)
+        assert B.moe_get_tile_group_bytes() == (3 * 128 * 256 * 2, 1)
+        assert L.moe_set_tile_group_bytes((1 << 40) + 1, 0) == B.MOE_ERR_INVALID_ARG
+        assert L.moe_set_tile_group_bytes(0, (1 << 40) + 1) == B.MOE_ERR_INVALID_ARG
+        assert B.moe_get_tile_group_bytes() == (3 * 128 * 256 * 2, 1)   # a rejected pair changes nothing
+        B.moe_set_tile_group_bytes(0, 1 << 40)                           # 0 restores a default
+        assert B.moe_get_tile_group_bytes() == (40 << 20, 1 << 40)
+    finally:
+        B.moe_set_tile_group_bytes(0, 0)
+    assert B.moe_get_tile_group_bytes() == (40 << 20, 64 << 20)
+    assert L.moe_get_tile_group_bytes(None, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_wait_probe(None, 1, None) == B.MOE_ERR_INVALID_ARG
     assert L.moe_wait_probe(0x10002, 1, None) == B.MOE_ERR_MISALIGNED

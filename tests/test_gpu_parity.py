@@ -360,19 +360,24 @@ def test_grouped_ffn(T, d, E, f, k, skew, ns, fs, dt, cuda_device):
         assert rel_err(Yn[T * k:], sref) <= TOL[dt]
 
 
-# Long segments: the expert GEMMs take a segment's M tiles in groups of 16 (all N
-# blocks of a group before the next), so segments of more than 16 M tiles (2048
-# rows) are walked group by group.  The sizes give a last group of one M tile of
-# one row (2049), of a full tile (4096 + 2048 rows: exactly 16 and 48 M tiles), a
-# short last tile (2100, 4097), short segments next to them (0, 1, 129, 300) and a
-# shared segment of several groups.  Every row is compared with the oracle.
+# Long segments: the expert GEMMs take a segment's M tiles in groups of nearly equal
+# size (every N block of a group before the next), at most as many per group as fit
+# the tile-group share of L2 (moe_set_tile_group_bytes).  The default shares group
+# nothing at these small d and f, so the test also forces groups of 16 and of 3 (up)
+# / 5 (down) M tiles.  The sizes give segments of 1, 2, 3, 16, 17 and 33 M tiles
+# (last tiles of one row, 2049, of a full tile, 2048 and 4096, and short ones, 2100,
+# 4097), short segments next to them (0, 1, 129, 300) and a shared segment of 43 M
+# tiles: groups of 3 split 17 into 3+3+3+3+3+2 and 16 into 3+3+3+3+2+2, groups of 5
+# split 17 into 5+4+4+4.  Every row is compared with the oracle.
 LONG_SEG_CASES = [
     # T, d, f, f_shared, counts of the 8 routed experts
     (5400, 256, 256, 128, [0, 1, 2049, 129, 4097, 2048, 300, 2100]),
     (5400, 512, 384, 256, [4096, 129, 0, 2049, 1, 2100, 300, 1800]),
 ]
+TILE_GROUPS = [None, (16, 16), (3, 5)]   # M tiles per group (up, down); None: the default shares
+@pytest.mark.parametrize("groups", TILE_GROUPS)
 @pytest.mark.parametrize("T,d,f,fs,counts", LONG_SEG_CASES)
-def test_grouped_ffn_long_segments(T, d, f, fs, counts, cuda_device):
+def test_grouped_ffn_long_segments(T, d, f, fs, counts, groups, cuda_device):
     E, k = 8, 2
     A = int(sum(counts))
     assert max(counts) > 16 * 128 and A <= T * k
@@ -391,17 +396,22 @@ def test_grouped_ffn_long_segments(T, d, f, fs, counts, cuda_device):
     x = random_rows(T, d, seed=92 + d, dtype=torch.bfloat16)
     dev = cuda_device
     layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
-    for _ in range(2):   # twice: the second call reuses the workspace and its counters
-        Y = layer.grouped_ffn(x_perm.to(dev), torch.from_numpy(off).to(dev), x.to(dev))
-        _check_device_error()
-        Yn = _np(Y)
-        for e in range(E):
-            a, b = int(off[e]), int(off[e + 1])
-            if b > a:
-                ref = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
-                assert rel_err(Yn[a:b], ref) <= TOL["bf16"], f"expert {e} ({b - a} rows)"
-        sref = oracle.expert_rows(x, Ws[0][0], Ws[1][0], Ws[2][0], nthreads=NTH)
-        assert rel_err(Yn[T * k:], sref) <= TOL["bf16"]
+    try:
+        if groups is not None:   # bytes of A rows per group: M tiles x 128 rows x K x 2 bytes
+            B.moe_set_tile_group_bytes(groups[0] * 128 * d * 2, groups[1] * 128 * f * 2)
+        for _ in range(2):   # twice: the second call reuses the workspace and its counters
+            Y = layer.grouped_ffn(x_perm.to(dev), torch.from_numpy(off).to(dev), x.to(dev))
+            _check_device_error()
+            Yn = _np(Y)
+            for e in range(E):
+                a, b = int(off[e]), int(off[e + 1])
+                if b > a:
+                    ref = oracle.expert_rows(x_perm[a:b], W1[e], W3[e], W2[e], nthreads=NTH)
+                    assert rel_err(Yn[a:b], ref) <= TOL["bf16"], f"expert {e} ({b - a} rows)"
+            sref = oracle.expert_rows(x, Ws[0][0], Ws[1][0], Ws[2][0], nthreads=NTH)
+            assert rel_err(Yn[T * k:], sref) <= TOL["bf16"]
+    finally:
+        B.moe_set_tile_group_bytes(0, 0)
 
 
 # The fine-grained layout at its widest: 256 routed experts plus one shared expert
@@ -635,20 +645,38 @@ def _segment_tails(gi, g_slot, usable, E):
     return toks, len(with_rows), exact
 
 
-def _segment_group_rows(gi, g_slot, g_off, usable, E):
-    """For every expert, the tokens of the rows that open and close each group of 16
-    M tiles of its segment (segment rows 0, 2047, 2048, 4095, 4096, ... and its last
-    row) in the GPU's own routing, where the routing agrees with the oracle's: the
-    tiles on both sides of every group boundary of the expert GEMMs' tile order."""
-    T, k = gi.shape
+def _group_starts(mblk, group_m):
+    """First M tile of every group of a segment of mblk M tiles in the expert GEMMs'
+    tile order: ceil(mblk / group_m) groups of nearly equal size, the larger first."""
+    if group_m <= 0 or mblk <= group_m:
+        return [0]
+    ng = -(-mblk // group_m)
+    base, big = divmod(mblk, ng)
+    starts, m = [], 0
+    for i in range(ng):
+        starts.append(m)
+        m += base + (1 if i < big else 0)
+    return starts
+
+
+def _segment_group_rows(gi, g_slot, g_off, usable, wl):
+    """For every expert, the tokens of the rows that open and close each group of M
+    tiles of its segment in the up and in the down projection (the default shares of
+    moe_set_tile_group_bytes: 40 MiB of x_perm rows, 64 MiB of H rows), and its first
+    and last row, in the GPU's own routing, where the routing agrees with the
+    oracle's: the tiles on both sides of every group boundary of the tile order."""
+    up_bytes, down_bytes = B.moe_get_tile_group_bytes()
+    gms = (max(1, up_bytes // (128 * wl.d * 2)), max(1, down_bytes // (128 * wl.f * 2)))
     toks = []
-    for e in range(E):
+    for e in range(wl.E):
         n = int(g_off[e + 1] - g_off[e])
         if n == 0:
             continue
+        mblk = -(-n // 128)
         ranks = {0, n - 1}
-        for r0 in range(2048, n, 2048):
-            ranks.update((r0 - 1, r0))
+        for gm in gms:
+            for m0 in _group_starts(mblk, gm)[1:]:
+                ranks.update((128 * m0 - 1, 128 * m0))
         rel = g_slot - g_off[e]
         for t, j in zip(*np.nonzero((gi == e) & (g_slot >= 0))):
             if int(rel[t, j]) in ranks and usable[t]:
@@ -734,7 +762,7 @@ def _run_e2e(wl, n_sample, cuda_device):
             assert len(reached) == n_rows and n_tail >= 0.95 * n_rows
             toks = _sample_tokens(T, 24, T, list(tails) + [T - 1])
         elif n_sample == "groups":
-            bounds = _segment_group_rows(gi, g_slot, g_off, same, wl.E)
+            bounds = _segment_group_rows(gi, g_slot, g_off, same, wl)
             print(f"{wl.name}: {len(bounds)} tokens at group boundaries of the expert segments")
             assert len(bounds) >= wl.E
             toks = _sample_tokens(T, 12, T, list(bounds))
