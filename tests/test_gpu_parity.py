@@ -414,6 +414,67 @@ def test_grouped_ffn_long_segments(T, d, f, fs, counts, groups, cuda_device):
         B.moe_set_tile_group_bytes(0, 0)
 
 
+# The same long segments with forced groups of 3 (up) / 5 (down) M tiles in every
+# kernel that walks the grouped tile order: the bf16 and FP8-weight (W8) kernels as
+# one fused launch and as separate up and down launches, and the fused launch with
+# the E4M3 up projection.  Every row compared with the oracle of the mode.
+@pytest.mark.parametrize("dt", ["bf16", "fp8w", "fp8up"])
+def test_grouped_ffn_long_segments_forced_groups(dt, cuda_device):
+    T, d, f, fs, counts = LONG_SEG_CASES[0]
+    E, k = 8, 2
+    A = int(sum(counts))
+    cfg = B.config(T=T, d=d, E=E, f=f, k=k, n_shared=1, f_shared=fs, dtype=dt)
+    g = torch.Generator(device="cpu").manual_seed(9191)
+    W1 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W3 = (torch.randn(E, d, f, generator=g) / d ** 0.5).bfloat16()
+    W2 = (torch.randn(E, f, d, generator=g) / f ** 0.5).bfloat16()
+    Ws = [(torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, d, fs, generator=g) / d ** 0.5).bfloat16(),
+          (torch.randn(1, fs, d, generator=g) / fs ** 0.5).bfloat16()]
+    off = np.zeros(E + 1, np.int32)
+    off[1:] = np.cumsum(counts)
+    x_perm = torch.zeros(T * k, d, dtype=torch.bfloat16)
+    x_perm[:A] = random_rows(A, d, seed=93, dtype=torch.bfloat16)
+    x = random_rows(T, d, seed=94, dtype=torch.bfloat16)
+
+    def ref_rows(X, w1, w3, w2):
+        Xf = X.float().numpy()
+        if dt == "fp8w":
+            return oracle.expert_rows_fp8(Xf, *_fp8_quant(w1, w3, w2))
+        if dt == "fp8up":
+            return oracle.expert_rows_fp8up(Xf, w1.float().numpy(), w3.float().numpy(), w2.float().numpy())
+        return oracle.expert_rows(X, w1, w3, w2, nthreads=NTH)
+
+    ref = np.zeros((T * k + T, d))
+    for e in range(E):
+        a, b = int(off[e]), int(off[e + 1])
+        if b > a:
+            ref[a:b] = ref_rows(x_perm[a:b], W1[e], W3[e], W2[e])
+    ref[T * k:] = ref_rows(x, Ws[0][0], Ws[1][0], Ws[2][0])
+    dev = cuda_device
+    layer = MoELayer(cfg, W1.to(dev), W3.to(dev), W2.to(dev), *(w.to(dev) for w in Ws))
+    off_d, xp_d, x_d = torch.from_numpy(off).to(dev), x_perm.to(dev), x.to(dev)
+    try:
+        B.moe_set_tile_group_bytes(3 * 128 * d * 2, 5 * 128 * f * 2)
+        outs = [_np(layer.grouped_ffn(xp_d, off_d, x_d))]
+        if dt != "fp8up":   # the E4M3 up projection has no separate launches
+            H = torch.empty(T * k, f, dtype=torch.bfloat16, device=dev)
+            Hs = torch.empty(T, fs, dtype=torch.bfloat16, device=dev)
+            Y2 = torch.empty(T * k + T, d, dtype=torch.bfloat16, device=dev)
+            B.moe_grouped_ffn_up(cfg, xp_d, off_d, layer.packed, x_d, H, Hs)
+            B.moe_grouped_ffn_down(cfg, H, Hs, off_d, layer.packed, Y2)
+            outs.append(_np(Y2))
+        _check_device_error()
+    finally:
+        B.moe_set_tile_group_bytes(0, 0)
+    for got in outs:
+        for e in range(E):
+            a, b = int(off[e]), int(off[e + 1])
+            if b > a:
+                assert rel_err(got[a:b], ref[a:b]) <= TOL["bf16"], (dt, e, b - a)
+        assert rel_err(got[T * k:], ref[T * k:]) <= TOL["bf16"]
+
+
 # The fine-grained layout at its widest: 256 routed experts plus one shared expert
 # (257 segments) with small d and f, so that every row of every segment can be
 # compared with the oracle.  The segment sizes are seeded and skewed and include
