@@ -55,7 +55,9 @@ PER_CONFIG = ("tiny_top2_fp32", "switch_top1_cap1.25", "mixtral_T16", "mixtral_T
 # the same layers with the up projection on E4M3 operands (MOE_BF16_FP8UP), beside them
 PER_CONFIG_FP8UP = ("switch_top1_cap1.25", "mixtral_T4096", "mixtral_T16384", "deepseek_v3")
 KERNEL_SOURCES = {   # files whose content defines each stage's kernels (for the ncu traffic record)
-    "ffn": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh", "csrc/moe_internal.cuh"],
+    # moe_api.cu holds the default tile-group shares that set the FFN's tile order
+    "ffn": ["csrc/ffn_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh", "csrc/moe_internal.cuh",
+            "csrc/moe_api.cu"],
     "route": ["csrc/route.cu", "csrc/route_tcgen05.cu", "csrc/tc_gemm.cuh", "csrc/tc_common.cuh"],
     "dispatch": ["csrc/dispatch.cu"],
     "combine": ["csrc/combine.cu"],
