@@ -773,8 +773,9 @@ E2E_SMALL = {
     "small_k_eq_E": WORKLOADS["mixtral_T256"].with_(T=200, d=256, E=4, k=4, f=128, name="small_k_eq_E"),
     "small_dense_E1": WORKLOADS["mixtral_T256"].with_(T=130, d=256, E=1, k=1, f=256, name="small_dense_E1"),
     "small_one_token": WORKLOADS["mixtral_T16"].with_(T=1, d=256, f=128, name="small_one_token"),
-    # segments longer than 16 M tiles (2048 rows), walked in groups of 16 M tiles:
-    # top-2 softmax, and capacity with the gated down store of k = 1
+    # segments longer than 16 M tiles (2048 rows): top-2 softmax, and capacity with
+    # the gated down store of k = 1 (at this d and f the default tile-group shares keep
+    # each segment in one group; the forced-group tests walk such segments in groups)
     "small_long_top2": WORKLOADS["mixtral_T256"].with_(T=9000, d=256, f=256, name="small_long_top2"),
     "small_long_switch": WORKLOADS["switch_top1_cap1.25"].with_(T=24000, d=256, E=8, f=256,
                                                                  logit_offsets="normal_var0.5",
